@@ -1,0 +1,295 @@
+/*
+ * Plain, slow fp64 CPU oracle for paged decode attention and the paged KV
+ * cache operations.  TEST INFRASTRUCTURE ONLY: it exists to check the CUDA
+ * library and is used by the tests, by the smoke check and by the CPU-baseline
+ * leg of the benchmark.  Nothing in the product path may load or call it.
+ *
+ * It shares no code, header, table or helper with the CUDA library.  Every
+ * routine is the textbook definition written out with straight loops:
+ * no blocking, no online softmax, no split of the context.
+ *
+ * Storage conventions (the KV pool as the pages describe it):
+ *   one pool per layer for K and one for V, each laid out as
+ *   [num_blocks][block_size][num_kv_heads][head_dim]
+ *   ("vLLM Framework and Inference Engine Design", section "What is the
+ *   essence of vLLM's PagedAttention?", and section "How is vLLM's KV cache
+ *   paged?", the per-layer tensor [2, num_blocks, block_size, kv_heads,
+ *   head_dim]).  Elements are stored as 16-bit patterns: IEEE-754 binary16
+ *   (dtype 0) or bfloat16 (dtype 1).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_F16 0
+#define OR_BF16 1
+
+/* ---------------------------------------------------------------------------
+ * Element decoding, from the formats' definitions.
+ * ------------------------------------------------------------------------- */
+
+/* IEEE-754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Normal: (-1)^s * 2^(e-15) * (1 + f/1024); subnormal: (-1)^s * 2^-14 * f/1024.
+ * Exponent 31 encodes infinity (f == 0) or NaN (f != 0).  Exact in fp64. */
+double or_f16_to_f64(uint16_t h) {
+    int s = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);               /* 2^-14 * f / 2^10 */
+    } else if (e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    }
+    return s ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE-754 binary32 (1 sign, 8 exponent bits
+ * with bias 127, 7 fraction bits). */
+double or_bf16_to_f64(uint16_t b) {
+    int s = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -133);              /* 2^-126 * f / 2^7 */
+    } else if (e == 255) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp(1.0 + (double)f / 128.0, e - 127);
+    }
+    return s ? -v : v;
+}
+
+static double or_decode(uint16_t x, int dtype) {
+    return dtype == OR_BF16 ? or_bf16_to_f64(x) : or_f16_to_f64(x);
+}
+
+void or_decode_array(const uint16_t* src, int64_t n, int dtype, double* dst) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = or_decode(src[i], dtype);
+}
+
+/* ---------------------------------------------------------------------------
+ * Address translation ("vLLM Framework and Inference Engine Design", section
+ * "What is the essence of vLLM's PagedAttention?"):
+ *   token t -> logical block j = floor(t / B), slot r = t mod B,
+ *   physical block p = block_table[j]; its K and V are K_cache[p][r], V_cache[p][r].
+ *   A sequence of T tokens holds ceil(T / B) blocks.
+ * ------------------------------------------------------------------------- */
+
+int64_t or_blocks_for(int64_t T, int32_t B) {
+    int64_t n = 0;
+    /* ceil by counting whole blocks, the definition read literally */
+    while (n * (int64_t)B < T) ++n;
+    return n;
+}
+
+/* Flat slot of token t: block_table[floor(t/B)] * B + (t mod B)
+ * ("How is vLLM's KV cache paged?", bullet "Writing": the slot mapping). */
+int64_t or_slot(const int32_t* table_row, int64_t t, int32_t B) {
+    int64_t j = t / B;
+    int64_t r = t % B;
+    return (int64_t)table_row[j] * B + r;
+}
+
+/* Slot mapping for a list of new tokens given as (sequence index, position). */
+void or_slot_mapping(const int32_t* block_tables, int64_t table_stride,
+                     const int32_t* token_seq, const int32_t* token_pos, int64_t n,
+                     int32_t B, int64_t* slots) {
+    for (int64_t k = 0; k < n; ++k) {
+        const int32_t* row = block_tables + (int64_t)token_seq[k] * table_stride;
+        slots[k] = or_slot(row, token_pos[k], B);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Cache write: each new token's K and V rows ([num_kv_heads][head_dim]) are
+ * stored at their flat slot of the pool.  A negative slot marks a padding
+ * token that writes nothing (a reading of ours: the pages are silent).
+ * ------------------------------------------------------------------------- */
+void or_cache_write(uint16_t* k_cache, uint16_t* v_cache,
+                    const uint16_t* k, const uint16_t* v,
+                    const int64_t* slots, int64_t n, int64_t row_elems) {
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t s = slots[i];
+        if (s < 0) continue;
+        for (int64_t e = 0; e < row_elems; ++e) {
+            k_cache[s * row_elems + e] = k[i * row_elems + e];
+            v_cache[s * row_elems + e] = v[i * row_elems + e];
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Copy-on-write block copy ("What operations can cause memory fragmentation,
+ * and how does vLLM avoid it?", bullet "Sharing instead of copying"): the whole
+ * block src is copied to block dst, K and V.  Pairs are applied in order.
+ * ------------------------------------------------------------------------- */
+void or_copy_blocks(uint16_t* k_cache, uint16_t* v_cache,
+                    const int32_t* pairs, int64_t n, int64_t block_elems) {
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t src = pairs[2 * i];
+        int64_t dst = pairs[2 * i + 1];
+        for (int64_t e = 0; e < block_elems; ++e) {
+            k_cache[dst * block_elems + e] = k_cache[src * block_elems + e];
+            v_cache[dst * block_elems + e] = v_cache[src * block_elems + e];
+        }
+    }
+}
+
+/* Gather the first T tokens of one sequence, one KV head, into a contiguous
+ * fp64 array out[T][D] by following the block table token by token. */
+void or_gather_head(const uint16_t* cache, int dtype, const int32_t* table_row,
+                    int64_t T, int32_t B, int32_t H_kv, int32_t D, int32_t h,
+                    double* out) {
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = or_slot(table_row, t, B);
+        const uint16_t* row = cache + (slot * H_kv + h) * (int64_t)D;
+        for (int32_t d = 0; d < D; ++d) out[t * D + d] = or_decode(row[d], dtype);
+    }
+}
+
+/* Raw 16-bit gather of all heads: out[T][H_kv][D], bit patterns unchanged. */
+void or_gather_bits(const uint16_t* cache, const int32_t* table_row, int64_t T,
+                    int32_t B, int32_t H_kv, int32_t D, uint16_t* out) {
+    int64_t row_elems = (int64_t)H_kv * D;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = or_slot(table_row, t, B);
+        memcpy(out + t * row_elems, cache + slot * row_elems,
+               (size_t)row_elems * sizeof(uint16_t));
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Single-query attention on contiguous fp64 arrays, textbook two-pass softmax
+ * ("What is the essence of vLLM's PagedAttention?": scores = q.K^T * scale,
+ * weights = softmax(scores), output = weights.V).
+ *   q[D], K[T][D], V[T][D] -> out[D]
+ *   s_t = scale * sum_d q_d K_td;  w_t = exp(s_t - max s) / sum exp(s - max s)
+ *   out_d = sum_t w_t V_td
+ * scratch must hold T doubles.
+ * ------------------------------------------------------------------------- */
+void or_attention_1q(const double* q, const double* K, const double* V,
+                     int64_t T, int32_t D, double scale, double* out,
+                     double* scratch) {
+    double m = -INFINITY;
+    for (int64_t t = 0; t < T; ++t) {
+        double dot = 0.0;
+        for (int32_t d = 0; d < D; ++d) dot += q[d] * K[t * D + d];
+        scratch[t] = scale * dot;
+        if (scratch[t] > m) m = scratch[t];
+    }
+    double z = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        scratch[t] = exp(scratch[t] - m);
+        z += scratch[t];
+    }
+    for (int32_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < T; ++t) acc += scratch[t] * V[t * D + d];
+        out[d] = acc / z;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Paged single-query decode for a list of sequences.
+ *   q        [num_seqs][Hq][D]           (16-bit, dtype)
+ *   pools    [num_blocks][B][H_kv][D]    (16-bit, dtype)
+ *   block_tables [num_seqs][table_stride] int32, seq_lens[num_seqs] int32
+ *   seq_ids  the n_ids sequences to evaluate; out[n_ids][Hq][D] fp64.
+ * Query head hq reads KV head floor(hq / G), G = Hq / H_kv (contiguous query
+ * groups: our reading of grouped-query attention, which the pages name in
+ * "How big the KV cache is: a formula and a real measurement" without giving
+ * the head mapping).  A sequence of length 0 yields a zero row (our reading).
+ * Returns 0, or -1 on an allocation failure.
+ * ------------------------------------------------------------------------- */
+int or_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                    int dtype, const int32_t* block_tables, int64_t table_stride,
+                    const int32_t* seq_lens, const int32_t* seq_ids, int32_t n_ids,
+                    int32_t Hq, int32_t H_kv, int32_t D, int32_t B, double scale,
+                    double* out, int threads) {
+    int32_t G = Hq / H_kv;
+    int64_t n_work = (int64_t)n_ids * H_kv;
+    int failed = 0;
+#ifdef _OPENMP
+    if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+    for (int64_t w = 0; w < n_work; ++w) {
+        int32_t idx = (int32_t)(w / H_kv);
+        int32_t h = (int32_t)(w % H_kv);
+        int32_t i = seq_ids[idx];
+        int64_t T = seq_lens[i];
+        double* o = out + (int64_t)idx * Hq * D;
+        if (T <= 0) {
+            for (int32_t g = 0; g < G; ++g)
+                for (int32_t d = 0; d < D; ++d) o[(int64_t)(h * G + g) * D + d] = 0.0;
+            continue;
+        }
+        const int32_t* row = block_tables + (int64_t)i * table_stride;
+        double* K = (double*)malloc((size_t)(T * D) * sizeof(double));
+        double* V = (double*)malloc((size_t)(T * D) * sizeof(double));
+        double* s = (double*)malloc((size_t)T * sizeof(double));
+        double* qv = (double*)malloc((size_t)D * sizeof(double));
+        if (!K || !V || !s || !qv) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+            or_gather_head(k_cache, dtype, row, T, B, H_kv, D, h, K);
+            or_gather_head(v_cache, dtype, row, T, B, H_kv, D, h, V);
+            for (int32_t g = 0; g < G; ++g) {
+                int32_t hq = h * G + g;
+                const uint16_t* qrow = q + ((int64_t)i * Hq + hq) * D;
+                for (int32_t d = 0; d < D; ++d) qv[d] = or_decode(qrow[d], dtype);
+                or_attention_1q(qv, K, V, T, D, scale, o + (int64_t)hq * D, s);
+            }
+        }
+        free(K);
+        free(V);
+        free(s);
+        free(qv);
+    }
+    return failed ? -1 : 0;
+}
+
+/* The same single-query attention over a contiguous (unpaged) cache
+ * K[T][H_kv][D] (fp64), used to check that paging changes only the addressing
+ * ("the attention kernel is the only part of the model that has to change"). */
+void or_contiguous_decode(const double* q /*[Hq][D]*/, const double* K, const double* V,
+                          int64_t T, int32_t Hq, int32_t H_kv, int32_t D, double scale,
+                          double* out /*[Hq][D]*/) {
+    int32_t G = Hq / H_kv;
+    double* Kh = (double*)malloc((size_t)(T * D + 1) * sizeof(double));
+    double* Vh = (double*)malloc((size_t)(T * D + 1) * sizeof(double));
+    double* s = (double*)malloc((size_t)(T + 1) * sizeof(double));
+    for (int32_t h = 0; h < H_kv; ++h) {
+        for (int64_t t = 0; t < T; ++t)
+            for (int32_t d = 0; d < D; ++d) {
+                Kh[t * D + d] = K[(t * H_kv + h) * D + d];
+                Vh[t * D + d] = V[(t * H_kv + h) * D + d];
+            }
+        for (int32_t g = 0; g < G; ++g) {
+            int32_t hq = h * G + g;
+            or_attention_1q(q + (int64_t)hq * D, Kh, Vh, T, D, scale, out + (int64_t)hq * D, s);
+        }
+    }
+    free(Kh);
+    free(Vh);
+    free(s);
+}
+
+int or_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
