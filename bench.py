@@ -1,0 +1,464 @@
+"""Benchmark of the paged decode step on GB300.
+
+A step is one pass of the hot path over one batch: copy-on-write block copies
+(shared-prefix workload only), slot mapping, cache write of the step's new
+K/V, and paged decode attention (partition kernel + split reduce).  The
+default workload is the Llama-3-8B GQA decode layer (256 sequences, lognormal
+lengths with mean about 400, 32 q heads / 8 KV heads, head_dim 128, bf16,
+16-token blocks, 40,000-block pool).
+
+Prints ONE JSON line (rank 0).  `value` is sequence-steps per second over all
+ranks; `roofline` reports the decode kernels' achieved HBM bandwidth
+(algorithmic bytes / CUDA-event time) against the measured copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "Paged decode attention: achieved HBM GB/s vs GB300 peak; seq-steps/sec"
+UNIT = "seq-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+DATASHEET_HBM_GBS = 7900.0   # nominal GB300 HBM3e figure, for context only
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_device.cuh", "pa_decode_variants.cuh",
+                  "pa_decode.cu"]
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def algorithmic_bytes(wl):
+    """Bytes the step must move, per the method (no implementation overhead).
+
+    decode: every used K and V row of every KV head (2 * e * H_kv * D * sum T),
+    the queries and outputs (2 * N * Hq * D * e), one block-table entry per
+    used block and one length per sequence.  cache write: read the new K/V and
+    write them, plus one int64 slot per token (and the two int32 inputs of the
+    slot mapping).  copy-on-write: read and write each copied block, K and V."""
+    e = wl.elem_bytes
+    T = wl.seq_lens.astype(np.int64)
+    N = wl.num_seqs
+    kv = 2 * e * wl.num_kv_heads * wl.head_dim * int(T.sum())
+    qo = 2 * N * wl.num_q_heads * wl.head_dim * e
+    tables = 4 * int(sum(-(-int(t) // wl.block_size) for t in T))
+    lens = 4 * N
+    decode = kv + qo + tables + lens
+    n_new = wl.new_seq.size
+    write = 2 * 2 * e * n_new * wl.num_kv_heads * wl.head_dim + 8 * n_new + 16 * n_new
+    cow = 2 * 2 * wl.copy_pairs.shape[0] * wl.block_size * wl.num_kv_heads * wl.head_dim * e
+    return {"decode": decode, "kv": kv, "write": write, "cow": cow, "step": decode + write + cow}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_72_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(workload)
+    if not rec or rec.get("kernel_sha") != kernel_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+class Step:
+    """Device-resident inputs and the step as calls into the C ABI."""
+
+    def __init__(self, wl, device):
+        import torch
+        import paged_kv_cache_72_gb300 as pa
+        self.pa, self.torch, self.wl = pa, torch, wl
+        td = torch.float16 if wl.dtype == W.F16 else torch.bfloat16
+
+        def up(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(td)
+
+        self.k_cache = up(wl.k_cache)
+        self.v_cache = up(wl.v_cache)
+        self.q = up(wl.q)
+        self.k_new = up(wl.k_new)
+        self.v_new = up(wl.v_new)
+        self.block_tables = torch.from_numpy(wl.block_tables).to(device)
+        self.seq_lens = torch.from_numpy(wl.seq_lens).to(device)
+        self.new_seq = torch.from_numpy(wl.new_seq).to(device)
+        self.new_pos = torch.from_numpy(wl.new_pos).to(device)
+        self.pairs = torch.from_numpy(np.ascontiguousarray(wl.copy_pairs, np.int32)).to(device)
+        self.slots = torch.empty(wl.new_seq.size, dtype=torch.int64, device=device)
+        self.out = torch.empty_like(self.q)
+        nbytes = pa.pa_decode_workspace_size(wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                             wl.block_size, wl.dtype)
+        self.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ev0 = torch.cuda.Event(enable_timing=True)
+        self.ev1 = torch.cuda.Event(enable_timing=True)
+        self.decode_ms = []
+
+    def launches_per_step(self):
+        return (1 if self.pairs.numel() else 0) + 2 + 2
+
+    def run(self, time_decode=False):
+        pa, wl = self.pa, self.wl
+        if self.pairs.numel():
+            pa.pa_copy_blocks(self.pairs, self.k_cache, self.v_cache, err=self.err)
+        pa.pa_slot_mapping(self.block_tables, self.new_seq, self.new_pos, wl.block_size,
+                           wl.num_blocks, out=self.slots, err=self.err)
+        pa.pa_cache_write(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
+                          err=self.err)
+        if time_decode:
+            self.ev0.record()
+        pa.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
+                     wl.scale, out=self.out, workspace=self.workspace, err=self.err)
+        if time_decode:
+            self.ev1.record()
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    import paged_kv_cache_72_gb300 as pa
+    wl = W.CONFIGS[args.workload](seed=_seed(args) + rank)
+    st = Step(wl, device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    nbytes = algorithmic_bytes(wl)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        st.run()
+    torch.cuda.synchronize()
+    flags = pa.pa_get_error(st.err)
+    if flags:
+        raise RuntimeError("kernel reported error bits 0x%x" % flags)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    step_ms, decode_ms = [], []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.steps):
+        flush.fill_(float(_ + 2))
+        e0.record()
+        st.run(time_decode=True)
+        e1.record()
+        e1.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        decode_ms.append(st.ev0.elapsed_time(st.ev1))
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    flags = pa.pa_get_error(st.err)
+    if flags:
+        raise RuntimeError("kernel reported error bits 0x%x" % flags)
+
+    ms = statistics.mean(step_ms)
+    dms = statistics.mean(decode_ms)
+    ms_max = _max_over_ranks(ms, world, device)
+
+    # end to end through the public API with host buffers: per step the
+    # inputs go host -> device from pinned memory and the output comes back
+    host = {
+        "q": st.q.cpu().pin_memory(), "k_new": st.k_new.cpu().pin_memory(),
+        "v_new": st.v_new.cpu().pin_memory(), "block_tables": st.block_tables.cpu().pin_memory(),
+        "seq_lens": st.seq_lens.cpu().pin_memory(), "new_seq": st.new_seq.cpu().pin_memory(),
+        "new_pos": st.new_pos.cpu().pin_memory(), "pairs": st.pairs.cpu().pin_memory(),
+    }
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for name, t in host.items():
+            getattr(st, name).copy_(t, non_blocking=True)
+        st.run()
+        out_host.copy_(st.out, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e = statistics.mean(e2e_ms)
+    e2e_max = _max_over_ranks(e2e, world, device)
+
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes["decode"] / (dms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    return {
+        "wl": wl, "ms": ms_max, "ms_local": ms, "decode_ms": dms, "e2e_ms": e2e_max,
+        "h2d": h2d, "d2h": d2h, "bytes": nbytes, "clocks": clk,
+        "launches": st.launches_per_step() * args.steps,
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "kernel": "pa_decode: paged_decode_kernel + split_reduce_kernel",
+            "algorithmic_bytes_per_launch": nbytes["decode"],
+            "frac_of_datasheet_7.9TBps": round(achieved / DATASHEET_HBM_GBS, 4),
+        },
+    }
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world, device):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# --------------------------------------------------------------------------
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rate(wl, budget_s, seqs_cap=None):
+    """Time the fp64 oracle's step (cache write + decode) on a bounded sample
+    of sequences; returns (seq-steps/s, sample description, seconds)."""
+    import oracle
+    n_cores = cores()
+    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    slots = oracle.slot_mapping(wl.block_tables, wl.new_seq, wl.new_pos, wl.block_size)
+    N = wl.num_seqs if seqs_cap is None else min(wl.num_seqs, seqs_cap)
+    # calibrate on a few sequences, then size the sample to the budget
+    probe = np.arange(min(N, 4), dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.paged_decode(wl.q, kc, vc, wl.dtype, wl.block_tables, wl.seq_lens, wl.scale,
+                        seq_ids=probe, threads=n_cores)
+    per_seq = max((time.perf_counter() - t0) / len(probe), 1e-5)
+    n = int(min(N, max(1, budget_s / per_seq)))
+    ids = np.arange(n, dtype=np.int32)
+    mask = np.isin(wl.new_seq, ids)
+    done, t_total, reps = 0, 0.0, 0
+    while True:
+        t0 = time.perf_counter()
+        oracle.cache_write(kc, vc, wl.k_new[mask], wl.v_new[mask], slots[mask])
+        oracle.paged_decode(wl.q, kc, vc, wl.dtype, wl.block_tables, wl.seq_lens, wl.scale,
+                            seq_ids=ids, threads=n_cores)
+        t_total += time.perf_counter() - t0
+        done += n
+        reps += 1
+        if t_total >= budget_s or reps >= 1000:
+            break
+    sample = "%d of %d sequences x %d repetition(s): cache write of their new tokens + fp64 " \
+             "decode of all their query heads" % (n, wl.num_seqs, reps)
+    return done / t_total, sample, t_total, n_cores
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = W.CONFIGS[args.workload](seed=_seed(args))
+    rates = []
+    sample = None
+    n_cores = cores()
+    for i in range(args.warmup + args.steps):
+        r, sample, _, n_cores = oracle_rate(wl, budget_s=args.ref_step_seconds)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.mean(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": _config(wl, args),
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": n_cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+DEFAULT_SEEDS = {"tiny": 1, "llama2-7b": 2, "llama3-8b-gqa": 3, "qwen2-0.5b-shared-prefix": 4,
+                 "70b-long-context": 5}
+
+
+def _seed(args):
+    return DEFAULT_SEEDS[args.workload] if args.seed is None else args.seed
+
+
+def _config(wl, args):
+    return {
+        "workload": wl.name, "num_seqs": wl.num_seqs, "q_heads": wl.num_q_heads,
+        "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+        "kv_dtype": W.DTYPE_NAMES[wl.dtype], "num_blocks": wl.num_blocks,
+        "total_context_tokens": int(wl.seq_lens.sum()), "max_seq_len": wl.max_seq_len,
+        "new_tokens_per_step": int(wl.new_seq.size), "copy_pairs": int(wl.copy_pairs.shape[0]),
+        "seed": _seed(args), "recipe": wl.recipe,
+        "l2": "flushed between timed steps by a %d MiB device write" % (L2_FLUSH_BYTES >> 20),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3-8b-gqa", choices=sorted(W.CONFIGS))
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    wl = res["wl"]
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, sample, _, n_cores = oracle_rate(wl, budget_s=args.cpu_baseline_seconds)
+        cpu = {"value": round(r, 2), "unit": UNIT, "cores": n_cores, "kind": "oracle",
+               "sample": sample}
+    if rank == 0:
+        value = wl.num_seqs * world / (res["ms"] * 1e-3)
+        e2e = wl.num_seqs * world / (res["e2e_ms"] * 1e-3)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": W.DTYPE_NAMES[wl.dtype], "data": "synthetic", "config": _config(wl, args),
+            "roofline": res["roofline"], "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e, 1), "unit": UNIT, "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(res["e2e_ms"], 4)},
+            "gpu_launches": res["launches"] * world,
+            "clocks": res["clocks"],
+            "decode_ms": round(res["decode_ms"], 5),
+            "step_algorithmic_bytes": res["bytes"]["step"],
+            "step_gbs": round(res["bytes"]["step"] / (res["ms_local"] * 1e-3) / 1e9, 1),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

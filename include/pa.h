@@ -1,0 +1,189 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache library (GB300, sm_103a).
+ *
+ * The data-parallel hot path of PagedAttention: slot mapping, the slot-mapped
+ * cache write, the copy-on-write block copy and single-query decode attention
+ * over a block-paged KV pool, with its split-context reduce.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "vLLM Framework and Inference Engine Design" (vineetganti.com)
+ *   [P3] "vLLM anatomy: high-throughput LLM inference" (karya-semi.vercel.app)
+ *   [P5] "vLLM" (bibekananda.in)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All data pointers are DEVICE pointers, owned by the caller.  The library
+ *    allocates no device memory and keeps no per-call state.  Buffers must be
+ *    16-byte aligned.
+ *  - KV pool, one per layer and per K/V ([P1] "What is the essence of vLLM's
+ *    PagedAttention?"; "How is vLLM's KV cache paged?"): a contiguous array
+ *        cache[num_blocks][block_size][num_kv_heads][head_dim]
+ *    of 16-bit elements (PA_F16: IEEE binary16, PA_BF16: bfloat16).
+ *  - Block tables: int32 [num_seqs][table_stride], row i lists the physical
+ *    blocks of sequence i in logical order; entries past
+ *    ceil(seq_lens[i] / block_size) are never read.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Host-detectable errors return a PA_ERR_* status before
+ *    anything is launched.  Bad indices met on the device never fault and never
+ *    trap: the access is skipped, a PA_DEVERR_* bit is OR-ed into *err_word
+ *    (an int32 device word, may be NULL), and pa_get_error() reports it.
+ *  - Supported shapes: head_dim in {64, 128}; block_size a power of two in
+ *    [1, 256] ([2, 256] for pa_decode and pa_gather_kv); num_q_heads a
+ *    multiple of num_kv_heads with group G = num_q_heads / num_kv_heads in
+ *    [1, 16].
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+#define PA_F16 0
+#define PA_BF16 1
+
+/* status codes returned by the entry points */
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG 1   /* null pointer, negative size, misaligned buffer, bad shape */
+#define PA_ERR_UNSUPPORTED 2   /* shape outside the compiled kernels */
+#define PA_ERR_WORKSPACE 3     /* decode workspace smaller than pa_decode_workspace_size() */
+#define PA_ERR_CUDA 4          /* a CUDA runtime or driver call failed */
+#define PA_ERR_DEVICE_INDEX 5  /* pa_get_error(): a kernel reported a PA_DEVERR_* bit */
+
+/* bits a kernel ORs into *err_word */
+#define PA_DEVERR_SLOT 0x1       /* slot_mapping entry >= num_blocks * block_size */
+#define PA_DEVERR_BLOCK_ID 0x2   /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_SEQ_LEN 0x4    /* seq_len < 0 or > table_stride * block_size */
+#define PA_DEVERR_COPY_PAIR 0x8  /* copy pair out of range, repeated dst, or dst that is a src */
+#define PA_DEVERR_TIMEOUT 0x10   /* a pipeline wait passed its bound; the result is invalid */
+#define PA_DEVERR_POSITION 0x20  /* slot mapping: sequence index or position outside its table */
+
+/* pa_decode flags */
+#define PA_DECODE_AUTO 0
+#define PA_DECODE_SIMT 1  /* CUDA-core kernel (group size 1 only) */
+#define PA_DECODE_MMA 2   /* tensor-core kernel (any supported group size) */
+
+typedef void* pa_stream; /* cudaStream_t */
+
+/*
+ * pa_slot_mapping -- flat cache slot of each new token.
+ * [P1] "How is vLLM's KV cache paged?", bullet "Writing": a token at position t
+ * of a sequence is stored at slot block_table[floor(t/B)] * B + (t mod B).
+ *   block_tables  int32 [num_seqs][table_stride]
+ *   token_seq     int32 [num_tokens]  sequence index of each new token
+ *   token_pos     int32 [num_tokens]  its position t within the sequence
+ *   slot_mapping  int64 [num_tokens]  output
+ * A token whose sequence index is outside [0, num_seqs) or whose position is
+ * outside the table row gets slot -1 and sets PA_DEVERR_POSITION; a table entry
+ * outside [0, num_blocks) gives slot -1 and sets PA_DEVERR_BLOCK_ID.
+ * num_tokens == 0 is a no-op.
+ */
+int pa_slot_mapping(const int32_t* block_tables, int32_t table_stride, int32_t num_seqs,
+                    const int32_t* token_seq, const int32_t* token_pos, int64_t num_tokens,
+                    int32_t block_size, int64_t num_blocks, int64_t* slot_mapping,
+                    int32_t* err_word, pa_stream stream);
+
+/*
+ * pa_cache_write -- store each new token's K and V rows at its slot.
+ * [P1] "How is vLLM's KV cache paged?", bullet "Writing" (the slot mapping);
+ * [P1] "What is the essence of vLLM's PagedAttention?" (K_cache[p][r]).
+ *   k, v          [num_tokens][num_kv_heads][head_dim], contiguous, dtype
+ *   slot_mapping  int64 [num_tokens]; slot s addresses block s / B, row s % B;
+ *                 s < 0 marks a padding token that writes nothing;
+ *                 s >= num_blocks * B sets PA_DEVERR_SLOT and writes nothing.
+ * Bit-exact copy.  Two tokens with the same slot: one of them wins.
+ */
+int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                   void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size,
+                   int32_t num_kv_heads, int32_t head_dim, int32_t dtype, int32_t* err_word,
+                   pa_stream stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write block copies.
+ * [P1] "What operations can cause memory fragmentation, and how does vLLM avoid
+ * it?", bullet "Sharing instead of copying": a shared block is copied only when
+ * a sequence needs to write into it; [P5] "The part that is easy to miss".
+ *   src_dst_pairs int32 [num_pairs][2] (src block, dst block), device memory.
+ * Every pair copies all block_size * num_kv_heads * head_dim elements of K and
+ * of V from src to dst.  Pairs are independent: dst blocks must be distinct and
+ * no dst may also be a src.  A pair out of range, or one that breaks this rule,
+ * sets PA_DEVERR_COPY_PAIR and is not copied.
+ */
+int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cache, void* v_cache,
+                   int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t dtype, int32_t* err_word, pa_stream stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
+ * this shape on the current device (partial softmax states of contexts split
+ * across thread blocks, plus per-block bookkeeping).  num_ctas = 0 selects
+ * the default grid (a multiple of the SM count); flags as for pa_decode.
+ */
+int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t dtype, int32_t flags, int32_t num_ctas,
+                             size_t* bytes);
+
+/*
+ * pa_decode -- single-query decode attention over the paged KV pool.
+ * [P1] "What is the essence of vLLM's PagedAttention?": the kernel follows the
+ * block table (token t -> block block_table[floor(t/B)], row t mod B) instead
+ * of reading one contiguous tensor; scores = q.K^T * scale, weights =
+ * softmax(scores), output = weights.V.  [P3] "Custom CUDA Kernels for
+ * PagedAttention": decode attention is memory-bound; the kernel reads the block
+ * table on the GPU and fetches the scattered blocks in parallel.
+ *   q          [num_seqs][num_q_heads][head_dim], contiguous, dtype
+ *   seq_lens   int32 [num_seqs]: tokens in the cache, including the token
+ *              written this step; 0 gives a zero output row
+ *   out        [num_seqs][num_q_heads][head_dim], dtype; must not alias q
+ *   scale      multiplies q.k (e.g. 1/sqrt(head_dim))
+ *   workspace  device buffer of at least pa_decode_workspace_size() bytes
+ * Query head hq reads KV head hq / G (contiguous query groups).  Accumulation
+ * is fp32; the output is rounded once to dtype.  The result does not depend on
+ * where the blocks sit in the pool.  Each sequence's context is split across
+ * thread blocks in 64-token chunks and merged by a second kernel.
+ * flags: PA_DECODE_AUTO, PA_DECODE_SIMT or PA_DECODE_MMA; num_ctas: 0 = default.
+ */
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+              int32_t block_size, int64_t num_blocks, int32_t dtype, float scale, void* out,
+              void* workspace, size_t workspace_bytes, int32_t flags, int32_t num_ctas,
+              int32_t* err_word, pa_stream stream);
+
+/*
+ * pa_gather_kv -- (test support) gather every sequence's K and V rows into
+ * contiguous arrays through the same block-table walk, the same TMA staging
+ * into shared memory and the same shared-memory addressing that pa_decode
+ * uses (flags: PA_DECODE_SIMT selects the CUDA-core kernel's staging layout,
+ * anything else the tensor-core kernel's swizzled layout).
+ *   out_offsets  int64 [num_seqs]: first output row of sequence i
+ *   k_out, v_out [sum seq_lens][num_kv_heads][head_dim], dtype
+ * Bit-exact.
+ */
+int pa_gather_kv(const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 int32_t table_stride, const int32_t* seq_lens, const int64_t* out_offsets,
+                 int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                 int64_t num_blocks, int32_t dtype, int32_t flags, void* k_out, void* v_out,
+                 int32_t* err_word, pa_stream stream);
+
+/*
+ * pa_get_error -- synchronize `stream`, read *err_word into *flags (if not
+ * NULL) and clear it.  Returns PA_ERR_DEVICE_INDEX if any bit was set.
+ */
+int pa_get_error(int32_t* err_word, pa_stream stream, int32_t* flags);
+
+/* pa_strerror -- a static description of a status code. */
+const char* pa_strerror(int status);
+
+/* pa_version -- library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

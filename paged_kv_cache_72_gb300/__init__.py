@@ -1,0 +1,19 @@
+"""Paged KV-cache decode path for GB300 (sm_103a): a C-ABI CUDA library
+(``libpa.so``, declared in ``include/pa.h``) and this thin Python binding.
+
+The binding only marshals arguments (torch tensors -> device pointers, sizes
+and the current CUDA stream); every step runs in the library's kernels.  There
+is no fallback: if the library is missing, the calls raise.
+"""
+from ._lib import (PA_BF16, PA_DECODE_AUTO, PA_DECODE_MMA, PA_DECODE_SIMT, PA_DEVERR_BLOCK_ID,
+                   PA_DEVERR_COPY_PAIR, PA_DEVERR_POSITION, PA_DEVERR_SEQ_LEN, PA_DEVERR_SLOT,
+                   PA_DEVERR_TIMEOUT, PA_F16)
+from .ops import (PAError, pa_cache_write, pa_copy_blocks, pa_decode, pa_decode_workspace_size,
+                  pa_gather_kv, pa_get_error, pa_slot_mapping, pa_version)
+
+__all__ = [
+    "PAError", "pa_slot_mapping", "pa_cache_write", "pa_copy_blocks", "pa_decode",
+    "pa_decode_workspace_size", "pa_gather_kv", "pa_get_error", "pa_version", "PA_F16", "PA_BF16",
+    "PA_DECODE_AUTO", "PA_DECODE_SIMT", "PA_DECODE_MMA", "PA_DEVERR_SLOT", "PA_DEVERR_BLOCK_ID",
+    "PA_DEVERR_SEQ_LEN", "PA_DEVERR_COPY_PAIR", "PA_DEVERR_TIMEOUT", "PA_DEVERR_POSITION",
+]

@@ -1,0 +1,162 @@
+// Slot mapping, slot-mapped cache write and copy-on-write block copy.
+//
+// "vLLM Framework and Inference Engine Design", section "How is vLLM's KV cache
+// paged?", bullet "Writing": when a token's K and V are computed, a small
+// kernel stores them at slot block_table[floor(t/B)] * B + (t mod B); the list
+// of these slots is the slot mapping.  Section "What operations can cause
+// memory fragmentation, and how does vLLM avoid it?": a shared block is copied
+// only when a sequence needs to write into it.
+//
+// All three are pure data movement: 16-byte vector copies, bit-exact.
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+
+__global__ void slot_mapping_kernel(const int32_t* __restrict__ bt, int stride, int num_seqs,
+                                    const int32_t* __restrict__ tok_seq,
+                                    const int32_t* __restrict__ tok_pos, long long n, int log2B,
+                                    long long num_blocks, int64_t* __restrict__ slots,
+                                    int32_t* err) {
+  for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < n;
+       k += (long long)gridDim.x * blockDim.x) {
+    const int i = tok_seq[k];
+    const int t = tok_pos[k];
+    int64_t s = -1;
+    if (i < 0 || i >= num_seqs || t < 0 || (long long)t >= ((long long)stride << log2B)) {
+      set_error(err, PA_DEVERR_POSITION);
+    } else {
+      const int p = bt[(size_t)i * stride + (t >> log2B)];
+      if (p < 0 || (long long)p >= num_blocks) {
+        set_error(err, PA_DEVERR_BLOCK_ID);
+      } else {
+        s = ((int64_t)p << log2B) + (t & ((1 << log2B) - 1));
+      }
+    }
+    slots[k] = s;
+  }
+}
+
+// One block per new token: its K row [H_kv][D] and V row are each contiguous
+// in the input and at the destination slot.
+__global__ void cache_write_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                   const int64_t* __restrict__ slots, int vecs_per_row,
+                                   long long num_slots, uint4* __restrict__ kc,
+                                   uint4* __restrict__ vc, int32_t* err) {
+  const long long tok = blockIdx.x;
+  const long long s = slots[tok];
+  if (s < 0) return;
+  if (s >= num_slots) {
+    if (threadIdx.x == 0) set_error(err, PA_DEVERR_SLOT);
+    return;
+  }
+  const uint4* ks = k + tok * vecs_per_row;
+  const uint4* vs = v + tok * vecs_per_row;
+  uint4* kd = kc + s * vecs_per_row;
+  uint4* vd = vc + s * vecs_per_row;
+  for (int e = threadIdx.x; e < vecs_per_row; e += blockDim.x) {
+    const uint4 a = __ldg(ks + e);
+    const uint4 b = __ldg(vs + e);
+    kd[e] = a;
+    vd[e] = b;
+  }
+}
+
+// One block per (pair, K or V).  A pair is copied only if it is in range, its
+// dst appears once among the dsts and is no pair's src.
+__global__ void copy_blocks_kernel(const int32_t* __restrict__ pairs, int num_pairs,
+                                   long long num_blocks, int vecs_per_block,
+                                   uint4* __restrict__ kc, uint4* __restrict__ vc, int32_t* err) {
+  const int p = blockIdx.x;
+  const int which = blockIdx.y;  // 0 = K, 1 = V
+  const int src = pairs[2 * p], dst = pairs[2 * p + 1];
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  int mine = (src < 0 || (long long)src >= num_blocks || dst < 0 || (long long)dst >= num_blocks);
+  for (int j = threadIdx.x; j < num_pairs && !mine; j += blockDim.x) {
+    const int sj = pairs[2 * j], dj = pairs[2 * j + 1];
+    if (sj == dst || (j != p && dj == dst)) mine = 1;
+  }
+  if (mine) atomicOr(&bad, 1);
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0 && which == 0) set_error(err, PA_DEVERR_COPY_PAIR);
+    return;
+  }
+  uint4* base = which ? vc : kc;
+  const uint4* s = base + (long long)src * vecs_per_block;
+  uint4* d = base + (long long)dst * vecs_per_block;
+  for (int e = threadIdx.x; e < vecs_per_block; e += blockDim.x) d[e] = s[e];
+}
+
+static bool shape_ok(int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t dtype) {
+  return (head_dim == 64 || head_dim == 128) && num_kv_heads > 0 && is_pow2(block_size) &&
+         block_size <= 256 && (dtype == PA_F16 || dtype == PA_BF16);
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_slot_mapping(const int32_t* block_tables, int32_t table_stride, int32_t num_seqs,
+                    const int32_t* token_seq, const int32_t* token_pos, int64_t num_tokens,
+                    int32_t block_size, int64_t num_blocks, int64_t* slot_mapping,
+                    int32_t* err_word, pa_stream stream) {
+  if (num_tokens < 0 || num_seqs < 0 || table_stride < 0 || num_blocks < 0)
+    return PA_ERR_INVALID_ARG;
+  if (!is_pow2(block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!block_tables || !token_seq || !token_pos || !slot_mapping) return PA_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (int rc = current_device_info(&di)) return rc;
+  const int threads = 256;
+  long long blocks = (num_tokens + threads - 1) / threads;
+  if (blocks > (long long)di.sm_count * 16) blocks = (long long)di.sm_count * 16;
+  slot_mapping_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      block_tables, table_stride, num_seqs, token_seq, token_pos, num_tokens, ilog2(block_size),
+      num_blocks, slot_mapping, err_word);
+  return launch_status(cudaGetLastError());
+}
+
+int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                   void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size,
+                   int32_t num_kv_heads, int32_t head_dim, int32_t dtype, int32_t* err_word,
+                   pa_stream stream) {
+  if (num_tokens < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (!shape_ok(block_size, num_kv_heads, head_dim, dtype)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (num_tokens > 0x7fffffffLL) return PA_ERR_INVALID_ARG;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const int vecs = num_kv_heads * head_dim * 2 / 16;
+  const int threads = vecs >= 256 ? 256 : (vecs >= 128 ? 128 : 64);
+  cache_write_kernel<<<(unsigned)num_tokens, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, vecs,
+      num_blocks * (long long)block_size, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), err_word);
+  return launch_status(cudaGetLastError());
+}
+
+int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cache, void* v_cache,
+                   int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t dtype, int32_t* err_word, pa_stream stream) {
+  if (num_pairs < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (!shape_ok(block_size, num_kv_heads, head_dim, dtype)) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (num_pairs > 65535) return PA_ERR_INVALID_ARG;
+  if (!src_dst_pairs || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  const long long vecs = (long long)block_size * num_kv_heads * head_dim * 2 / 16;
+  if (vecs > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  dim3 grid((unsigned)num_pairs, 2);
+  copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      src_dst_pairs, num_pairs, num_blocks, (int)vecs, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), err_word);
+  return launch_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,249 @@
+// Host side of pa_decode / pa_gather_kv: shape checks, the launch plan
+// (pipeline depth, shared-memory layout, grid), the TMA tensor maps over the
+// KV pools, and the C entry points.
+#include <string.h>
+
+#include "pa_decode_kernel.cuh"
+#include "pa_decode_launch.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kMaxStages = 8;
+
+int ctrl_bytes(int stages) { return 16 * stages + 64 + 32; }
+
+int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas, bool gather,
+              DecodePlan* p) {
+  if (Hq <= 0 || Hkv <= 0 || num_ctas < 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  // one producer lane issues one TMA box of min(B, 64) rows: at most 32 boxes
+  if (!is_pow2(B) || B < 2 || B > 256) return PA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (G > 16) return PA_ERR_UNSUPPORTED;
+  if (flags != PA_DECODE_AUTO && flags != PA_DECODE_SIMT && flags != PA_DECODE_MMA)
+    return PA_ERR_INVALID_ARG;
+  DecodePlan q{};
+  q.bf16 = dtype == PA_BF16;
+  q.D = D;
+  q.G = G;
+  q.B = B;
+  if (gather) {
+    q.mode = kModeGather;
+    q.swz = (flags != PA_DECODE_SIMT) && B >= 8;
+  } else if (flags == PA_DECODE_SIMT || (flags == PA_DECODE_AUTO && G == 1)) {
+    if (G != 1) return PA_ERR_UNSUPPORTED;
+    q.mode = kModeSimt;
+    q.swz = false;
+  } else {
+    q.mode = kModeMma;
+    q.swz = B >= 8;
+  }
+  q.hi = q.mode == kModeMma && G > 8;
+  q.split_rows = q.swz && D == 128;
+  q.R = B < kChunk ? B : kChunk;
+  q.nsb = kChunk / q.R;
+  q.kv_bytes = kChunk * D * 2;
+  const int qpart = gather ? 0 : ((G * D * 2 + 1023) / 1024) * 1024;
+  q.stage_bytes = 2 * q.kv_bytes + qpart;
+  const int merge_bytes = gather ? 0 : kCWarps * (32 + G * D) * 4;
+
+  DeviceInfo di;
+  if (int rc = current_device_info(&di)) return rc;
+  q.stages = 0;
+  for (int target = 2; target >= 1 && q.stages == 0; --target) {
+    int budget = di.smem_per_sm / target - 1024;
+    if (budget > di.smem_per_block) budget = di.smem_per_block;
+    const int avail = budget - 1024 - merge_bytes - ctrl_bytes(kMaxStages);
+    int s = avail / q.stage_bytes;
+    if (s > kMaxStages) s = kMaxStages;
+    if (s >= 2) q.stages = s;
+  }
+  if (q.stages == 0) return PA_ERR_UNSUPPORTED;
+  q.merge_off = q.stages * q.stage_bytes;
+  q.ctrl_off = q.merge_off + merge_bytes;
+  q.smem_bytes = 1024 + q.ctrl_off + ctrl_bytes(q.stages);
+
+  if (num_ctas > 0) {
+    q.grid = num_ctas;
+  } else {
+    int per_sm = 0;
+    const int rc = D == 64 ? decode_ctas_per_sm_d64(q, &per_sm) : decode_ctas_per_sm_d128(q, &per_sm);
+    if (rc != PA_OK) return rc;
+    if (per_sm < 1) return PA_ERR_UNSUPPORTED;
+    q.grid = di.sm_count * per_sm;
+  }
+  q.ws_meta_bytes = gather ? 0 : (((size_t)q.grid * 8 * sizeof(int) + 255) / 256) * 256;
+  q.ws_rec_bytes = gather ? 0 : (size_t)q.grid * 2 * G * (D + 2) * sizeof(float);
+  *p = q;
+  return PA_OK;
+}
+
+// TMA map over one pool [num_blocks][B][Hkv][D]: one box = R rows of one head
+// of one block, all D elements.  With split_rows the box lands as two
+// [R][64] planes (dims: d_lo, row, d_hi, head, block); otherwise as R rows of
+// D contiguous elements (dims: d_lo, d_hi, head, row, block).
+int encode_kv_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int Hkv,
+                  long long num_blocks, bool split_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return PA_ERR_CUDA;
+  const int D = p.D, B = p.B;
+  cuuint64_t dims[5];
+  cuuint64_t strides[4];
+  cuuint32_t box[5];
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
+  if (split_rows) {
+    dims[0] = 64; dims[1] = B; dims[2] = D / 64; dims[3] = Hkv; dims[4] = num_blocks;
+    strides[0] = row; strides[1] = 128; strides[2] = (cuuint64_t)D * 2; strides[3] = row * B;
+    box[0] = 64; box[1] = p.R; box[2] = D / 64; box[3] = 1; box[4] = 1;
+  } else {
+    dims[0] = 64; dims[1] = D / 64; dims[2] = Hkv; dims[3] = B; dims[4] = num_blocks;
+    strides[0] = 128; strides[1] = (cuuint64_t)D * 2; strides[2] = row; strides[3] = row * B;
+    box[0] = 64; box[1] = D / 64; box[2] = 1; box[3] = p.R; box[4] = 1;
+  }
+  memset(map, 0, sizeof(*map));
+  const CUresult r =
+      enc(map, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
+          const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          p.swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int encode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* kc, const void* vc, DecodePlan* p,
+                int Hkv, long long nb) {
+  if (p->split_rows) {
+    if (encode_kv_map(tk, kc, *p, Hkv, nb, true) == PA_OK &&
+        encode_kv_map(tv, vc, *p, Hkv, nb, true) == PA_OK)
+      return PA_OK;
+    p->split_rows = false;  // the driver refused the plane layout: rows stay contiguous
+  }
+  if (int rc = encode_kv_map(tk, kc, *p, Hkv, nb, false)) return rc;
+  return encode_kv_map(tv, vc, *p, Hkv, nb, false);
+}
+
+void fill_layout(const DecodePlan& p, DecodeArgs* a) {
+  a->G = p.G;
+  a->B = p.B;
+  a->log2B = ilog2(p.B);
+  a->R = p.R;
+  a->log2R = ilog2(p.R);
+  a->nsb = p.nsb;
+  a->stages = p.stages;
+  a->kv_bytes = p.kv_bytes;
+  a->stage_bytes = p.stage_bytes;
+  a->merge_off = p.merge_off;
+  a->ctrl_off = p.ctrl_off;
+  a->split_rows = p.split_rows ? 1 : 0;
+  if (p.split_rows) {
+    a->hi_log2 = a->log2R + 7;
+    a->r_log2 = 7;
+  } else {
+    a->hi_log2 = 7;
+    a->r_log2 = p.D == 128 ? 8 : 7;
+  }
+}
+
+int launch(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+           cudaStream_t s) {
+  return p.D == 64 ? decode_launch_d64(p, tk, tv, a, s) : decode_launch_d128(p, tk, tv, a, s);
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t dtype, int32_t flags, int32_t num_ctas,
+                             size_t* bytes) {
+  if (!bytes) return PA_ERR_INVALID_ARG;
+  DecodePlan p;
+  if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
+                         false, &p))
+    return rc;
+  *bytes = p.ws_meta_bytes + p.ws_rec_bytes;
+  return PA_OK;
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+              int32_t block_size, int64_t num_blocks, int32_t dtype, float scale, void* out,
+              void* workspace, size_t workspace_bytes, int32_t flags, int32_t num_ctas,
+              int32_t* err_word, pa_stream stream) {
+  if (num_seqs < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  DecodePlan p;
+  if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
+                         false, &p))
+    return rc;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out || !workspace)
+    return PA_ERR_INVALID_ARG;
+  if (num_blocks == 0 || table_stride == 0 || num_blocks > 0xffffffffLL) return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace))
+    return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < p.ws_meta_bytes + p.ws_rec_bytes) return PA_ERR_WORKSPACE;
+  CUtensorMap tk, tv;
+  if (int rc = encode_maps(&tk, &tv, k_cache, v_cache, &p, num_kv_heads, num_blocks)) return rc;
+  DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.bt = block_tables;
+  a.seq_lens = seq_lens;
+  a.ws_meta = static_cast<int*>(workspace);
+  a.ws_rec = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ws_meta_bytes);
+  a.err = err_word;
+  a.num_blocks = num_blocks;
+  a.num_seqs = num_seqs;
+  a.stride = table_stride;
+  a.Hq = num_q_heads;
+  a.Hkv = num_kv_heads;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  fill_layout(p, &a);
+  return launch(p, tk, tv, a, static_cast<cudaStream_t>(stream));
+}
+
+int pa_gather_kv(const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 int32_t table_stride, const int32_t* seq_lens, const int64_t* out_offsets,
+                 int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                 int64_t num_blocks, int32_t dtype, int32_t flags, void* k_out, void* v_out,
+                 int32_t* err_word, pa_stream stream) {
+  if (num_seqs < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  DecodePlan p;
+  if (int rc = make_plan(num_kv_heads, num_kv_heads, head_dim, block_size, dtype, flags, 0, true,
+                         &p))
+    return rc;
+  if (num_seqs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_tables || !seq_lens || !out_offsets || !k_out || !v_out)
+    return PA_ERR_INVALID_ARG;
+  if (num_blocks == 0 || table_stride == 0 || num_blocks > 0xffffffffLL) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_out) || !aligned16(v_out))
+    return PA_ERR_INVALID_ARG;
+  CUtensorMap tk, tv;
+  if (int rc = encode_maps(&tk, &tv, k_cache, v_cache, &p, num_kv_heads, num_blocks)) return rc;
+  DecodeArgs a{};
+  a.bt = block_tables;
+  a.seq_lens = seq_lens;
+  a.err = err_word;
+  a.out_off = out_offsets;
+  a.k_out = static_cast<uint16_t*>(k_out);
+  a.v_out = static_cast<uint16_t*>(v_out);
+  a.num_blocks = num_blocks;
+  a.num_seqs = num_seqs;
+  a.stride = table_stride;
+  a.Hq = num_kv_heads;
+  a.Hkv = num_kv_heads;
+  fill_layout(p, &a);
+  a.G = 1;
+  return launch(p, tk, tv, a, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// Launch plan of the decode / gather kernels, shared between the planner and
+// the per-head_dim translation units that instantiate the kernels.
+#pragma once
+
+#include "pa_host.h"
+
+namespace pa {
+
+struct DecodeArgs;
+
+struct DecodePlan {
+  int mode;          // kModeSimt, kModeMma, kModeGather
+  bool bf16;
+  bool swz;          // 128-byte swizzled staging (tensor-core reads)
+  bool hi;           // group size > 8: query heads fill both MMA row halves
+  bool split_rows;   // rows of a box stored as two [R][64] planes
+  int D, G, B, R, nsb;
+  int stages;
+  int kv_bytes, stage_bytes, merge_off, ctrl_off, smem_bytes;
+  int grid;
+  size_t ws_meta_bytes, ws_rec_bytes;
+};
+
+// Per-variant occupancy (CTAs per SM) for a given dynamic shared-memory size.
+int decode_ctas_per_sm(const DecodePlan& p, int* ctas);
+
+// Launches the decode (or gather) kernel and, for decode, the split reduce.
+int decode_launch(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const DecodeArgs& a, cudaStream_t s);
+
+int decode_ctas_per_sm_d64(const DecodePlan& p, int* ctas);
+int decode_ctas_per_sm_d128(const DecodePlan& p, int* ctas);
+int decode_launch_d64(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const DecodeArgs& a, cudaStream_t s);
+int decode_launch_d128(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const DecodeArgs& a, cudaStream_t s);
+
+}  // namespace pa

@@ -1,0 +1,83 @@
+// Kernel-variant dispatch for one head_dim; included by pa_decode_d64.cu and
+// pa_decode_d128.cu so that the two head_dims compile in parallel.
+#pragma once
+
+#include "pa_decode_kernel.cuh"
+#include "pa_decode_launch.h"
+
+namespace pa {
+
+template <int D, bool BF, int MODE, bool SWZ, bool HI>
+struct Variant {
+  static decltype(&paged_decode_kernel<D, BF, MODE, SWZ, HI>) fn() {
+    return &paged_decode_kernel<D, BF, MODE, SWZ, HI>;
+  }
+};
+
+// Calls f(kernel_pointer) for the variant the plan selects.
+template <int D, class F>
+int with_variant(const DecodePlan& p, F&& f) {
+#define PA_V(BF, MODE, SWZ, HI) return f(Variant<D, BF, MODE, SWZ, HI>::fn())
+  if (p.mode == kModeSimt) {
+    if (p.bf16) PA_V(true, kModeSimt, false, false);
+    PA_V(false, kModeSimt, false, false);
+  }
+  if (p.mode == kModeGather) {
+    if (p.bf16) {
+      if (p.swz) PA_V(true, kModeGather, true, false);
+      PA_V(true, kModeGather, false, false);
+    }
+    if (p.swz) PA_V(false, kModeGather, true, false);
+    PA_V(false, kModeGather, false, false);
+  }
+  if (p.bf16) {
+    if (p.swz) {
+      if (p.hi) PA_V(true, kModeMma, true, true);
+      PA_V(true, kModeMma, true, false);
+    }
+    if (p.hi) PA_V(true, kModeMma, false, true);
+    PA_V(true, kModeMma, false, false);
+  }
+  if (p.swz) {
+    if (p.hi) PA_V(false, kModeMma, true, true);
+    PA_V(false, kModeMma, true, false);
+  }
+  if (p.hi) PA_V(false, kModeMma, false, true);
+  PA_V(false, kModeMma, false, false);
+#undef PA_V
+}
+
+template <int D>
+int ctas_per_sm_impl(const DecodePlan& p, int* ctas) {
+  return with_variant<D>(p, [&](auto kern) -> int {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, p.smem_bytes) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    *ctas = n;
+    return PA_OK;
+  });
+}
+
+template <int D>
+int launch_impl(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                const DecodeArgs& a, cudaStream_t s) {
+  int rc = with_variant<D>(p, [&](auto kern) -> int {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    kern<<<p.grid, kThreads, p.smem_bytes, s>>>(tk, tv, a);
+    return launch_status(cudaGetLastError());
+  });
+  if (rc != PA_OK || p.mode == kModeGather || p.grid < 2) return rc;
+  if (p.bf16)
+    split_reduce_kernel<D, true><<<p.grid, 128, 0, s>>>(a);
+  else
+    split_reduce_kernel<D, false><<<p.grid, 128, 0, s>>>(a);
+  return launch_status(cudaGetLastError());
+}
+
+}  // namespace pa

@@ -1,0 +1,114 @@
+"""Slot mapping, cache write and copy-on-write block copy on the GPU, compared
+bit for bit with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_72_gb300 as pa
+import workloads as W
+from harness import GpuState, OracleState, bits_of, gpu_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("make", [W.tiny, W.shared_prefix])
+def test_step_writes_are_bit_exact(cuda_device, make):
+    wl = make()
+    st = GpuState(wl)
+    _, slots = gpu_step(st, decode=False)
+    ref = OracleState(wl)
+    ref.step()
+    assert np.array_equal(slots.cpu().numpy(), ref.slots)
+    assert np.array_equal(bits_of(st.k_cache), ref.k_cache)
+    assert np.array_equal(bits_of(st.v_cache), ref.v_cache)
+    assert pa.pa_get_error(st.err) == 0
+
+
+def test_shared_prefix_sharers_read_identical_prefix(cuda_device):
+    # sequences sharing blocks see the same K/V ("vLLM": requests point at the
+    # same blocks); after the copy-on-write the 8 prefix tokens of the copied
+    # block are identical too
+    wl = W.shared_prefix()
+    st = GpuState(wl)
+    gpu_step(st, decode=False)
+    k = bits_of(st.k_cache)
+    first = [oracle.gather_bits(k, wl.block_tables[i], 1800) for i in range(wl.num_seqs)]
+    for g in first[1:]:
+        assert np.array_equal(g, first[0])
+
+
+def test_slot_mapping_random_positions(cuda_device):
+    rng = np.random.default_rng(40)
+    nb, B, N, stride = 500, 16, 37, 20
+    bt = rng.integers(0, nb, size=(N, stride)).astype(np.int32)
+    seq = rng.integers(0, N, size=3000).astype(np.int32)
+    pos = rng.integers(0, stride * B, size=3000).astype(np.int32)
+    got = pa.pa_slot_mapping(torch.from_numpy(bt).cuda(), torch.from_numpy(seq).cuda(),
+                             torch.from_numpy(pos).cuda(), B, nb)
+    assert np.array_equal(got.cpu().numpy(), oracle.slot_mapping(bt, seq, pos, B))
+
+
+def test_slot_mapping_flags_bad_positions(cuda_device):
+    bt = torch.tensor([[3, 1], [0, 2]], dtype=torch.int32, device="cuda")
+    seq = torch.tensor([0, 1, 2, 0, 1], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([5, 7, 0, 8, -1], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = pa.pa_slot_mapping(bt, seq, pos, 4, 4, err=err)
+    assert got.cpu().tolist() == [5, 11, -1, -1, -1]
+    assert pa.pa_get_error(err) == pa.PA_DEVERR_POSITION
+    bt_bad = torch.tensor([[3, 9]], dtype=torch.int32, device="cuda")
+    got = pa.pa_slot_mapping(bt_bad, seq[:1] * 0, torch.tensor([6], dtype=torch.int32,
+                                                                  device="cuda"), 4, 4, err=err)
+    assert got.cpu().tolist() == [-1]
+    assert pa.pa_get_error(err) == pa.PA_DEVERR_BLOCK_ID
+
+
+def test_cache_write_padding_and_out_of_range_slots(cuda_device):
+    rng = np.random.default_rng(41)
+    nb, B, H, D = 6, 4, 2, 64
+    kc = rng.integers(0, 65535, size=(nb, B, H, D), dtype=np.uint16)
+    vc = rng.integers(0, 65535, size=(nb, B, H, D), dtype=np.uint16)
+    k = rng.integers(0, 65535, size=(4, H, D), dtype=np.uint16)
+    v = rng.integers(0, 65535, size=(4, H, D), dtype=np.uint16)
+    slots = np.array([3, -1, nb * B, 23], np.int64)
+    dk = torch.from_numpy(kc.view(np.int16)).cuda().view(torch.float16)
+    dv = torch.from_numpy(vc.view(np.int16)).cuda().view(torch.float16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_cache_write(torch.from_numpy(k.view(np.int16)).cuda().view(torch.float16),
+                      torch.from_numpy(v.view(np.int16)).cuda().view(torch.float16),
+                      torch.from_numpy(slots).cuda(), dk, dv, err=err)
+    assert pa.pa_get_error(err) == pa.PA_DEVERR_SLOT
+    ok = slots.copy()
+    ok[2] = -1
+    oracle.cache_write(kc, vc, k, v, ok)
+    assert np.array_equal(bits_of(dk), kc) and np.array_equal(bits_of(dv), vc)
+
+
+def test_copy_blocks_rejects_conflicting_pairs(cuda_device):
+    rng = np.random.default_rng(42)
+    nb, B, H, D = 10, 16, 2, 64
+    kc = rng.integers(0, 65535, size=(nb, B, H, D), dtype=np.uint16)
+    vc = rng.integers(0, 65535, size=(nb, B, H, D), dtype=np.uint16)
+    dk = torch.from_numpy(kc.view(np.int16)).cuda().view(torch.bfloat16)
+    dv = torch.from_numpy(vc.view(np.int16)).cuda().view(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # (4 -> 5) writes a block that (5 -> 6) reads, so it is dropped; (1 -> 12)
+    # is out of range; (3 -> 9) and (0 -> 9) repeat a dst, both dropped
+    pairs = np.array([[0, 7], [4, 5], [5, 6], [1, 12], [2, 8], [3, 9], [0, 9]], np.int32)
+    pa.pa_copy_blocks(torch.from_numpy(pairs).cuda(), dk, dv, err=err)
+    assert pa.pa_get_error(err) == pa.PA_DEVERR_COPY_PAIR
+    oracle.copy_blocks(kc, vc, np.array([[0, 7], [5, 6], [2, 8]], np.int32))
+    assert np.array_equal(bits_of(dk), kc) and np.array_equal(bits_of(dv), vc)
+
+
+def test_empty_calls_are_no_ops(cuda_device):
+    z = torch.zeros(0, dtype=torch.int32, device="cuda")
+    kc = torch.zeros((4, 16, 2, 64), dtype=torch.float16, device="cuda")
+    out = pa.pa_slot_mapping(torch.zeros((1, 1), dtype=torch.int32, device="cuda"), z, z, 16, 4)
+    assert out.numel() == 0
+    pa.pa_copy_blocks(torch.zeros((0, 2), dtype=torch.int32, device="cuda"), kc, kc.clone())
+    pa.pa_cache_write(torch.zeros((0, 2, 64), dtype=torch.float16, device="cuda"),
+                      torch.zeros((0, 2, 64), dtype=torch.float16, device="cuda"),
+                      torch.zeros(0, dtype=torch.int64, device="cuda"), kc, kc.clone())
+    torch.cuda.synchronize()
