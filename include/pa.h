@@ -155,6 +155,30 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               int32_t* err_word, pa_stream stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode without a caller-provided workspace.
+ * The paper has no counterpart to this entry point: it exists for callers that
+ * cannot allocate device memory (a runtime whose device memory another
+ * allocator already owns, a C program with no device allocator, or a decode
+ * loop that cannot afford cudaMalloc's synchronization).  Arguments and result
+ * are those of pa_decode.  The workspace is a fixed array of
+ * PA_NOALLOC_SCRATCH_BYTES in the library's own device memory, held by every
+ * GPU that loads the library until the process exits; this call allocates
+ * nothing.  The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress) with that device current, so make that first call
+ * before any stream capture.  A shape whose workspace
+ * (pa_decode_workspace_size) exceeds the array returns PA_ERR_WORKSPACE.  All
+ * calls share the one array: calls that overlap on the GPU (for instance on two
+ * streams) race and must be serialized by the caller.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t dtype,
+                      float scale, void* out, int32_t flags, int32_t num_ctas,
+                      int32_t* err_word, pa_stream stream);
+
+/*
  * pa_gather_kv -- (test support) gather every sequence's K and V rows into
  * contiguous arrays through the same block-table walk, the same TMA staging
  * into shared memory and the same shared-memory addressing that pa_decode

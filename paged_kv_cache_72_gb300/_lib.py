@@ -25,6 +25,7 @@ PA_DEVERR_POSITION = 0x20
 PA_DECODE_AUTO = 0
 PA_DECODE_SIMT = 1
 PA_DECODE_MMA = 2
+PA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -41,6 +42,9 @@ SIGNATURES = {
                                                 ctypes.POINTER(_sz)]),
     "pa_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i64,
                                  _i32, ctypes.c_float, _vp, _vp, _sz, _i32, _i32, _vp, _vp]),
+    "pa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                         _i32, _i64, _i32, ctypes.c_float, _vp, _i32, _i32, _vp,
+                                         _vp]),
     "pa_gather_kv": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
                                     _i32, _i32, _vp, _vp, _vp, _vp]),
     "pa_get_error": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(_i32)]),
