@@ -98,6 +98,14 @@ def recorded_traffic(workload):
     return rec.get("dram_bytes_per_launch")
 
 
+def l2_flush(buf, k):
+    """Evict the step's data from L2: write a buffer four times the L2 size,
+    then read it back, so that the next step starts with a cold L2 that holds
+    no dirty lines (their write-back would otherwise land in the timed step)."""
+    buf.fill_(float(k % 7 + 1))
+    buf.amax()
+
+
 class ClockSampler:
     """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
 
@@ -118,6 +126,10 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0:
+                time.sleep(0.02)
+            self.lines = []
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -193,7 +205,7 @@ class Step:
     def launches_per_step(self):
         return (1 if self.pairs.numel() else 0) + 2 + 2
 
-    def run(self, time_decode=False):
+    def write_phase(self):
         pa, wl = self.pa, self.wl
         if self.pairs.numel():
             pa.pa_copy_blocks(self.pairs, self.k_cache, self.v_cache, err=self.err)
@@ -201,12 +213,30 @@ class Step:
                            wl.num_blocks, out=self.slots, err=self.err)
         pa.pa_cache_write(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
                           err=self.err)
-        if time_decode:
-            self.ev0.record()
-        pa.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
-                     wl.scale, out=self.out, workspace=self.workspace, err=self.err)
-        if time_decode:
-            self.ev1.record()
+
+    def decode_phase(self):
+        wl = self.wl
+        self.pa.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
+                          wl.scale, out=self.out, workspace=self.workspace, err=self.err)
+
+    def run(self):
+        self.write_phase()
+        self.decode_phase()
+
+    def capture(self):
+        """CUDA graphs of the two phases (the calls are the same C-ABI calls;
+        a graph removes the per-call host cost from the GPU timeline)."""
+        torch = self.torch
+        self.g_write = torch.cuda.CUDAGraph()
+        self.g_decode = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.g_write, stream=s):
+                self.write_phase()
+            with torch.cuda.graph(self.g_decode, stream=s):
+                self.decode_phase()
+        torch.cuda.current_stream().wait_stream(s)
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -214,47 +244,55 @@ def run_gpu(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     import paged_kv_cache_72_gb300 as pa
-    wl = W.CONFIGS[args.workload](seed=_seed(args) + rank)
+    kw = {"num_blocks": args.pool_blocks} if args.pool_blocks else {}
+    wl = W.CONFIGS[args.workload](seed=_seed(args) + rank, **kw)
     st = Step(wl, device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     nbytes = algorithmic_bytes(wl)
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
+    for k in range(args.warmup):
+        l2_flush(flush, k)
         st.run()
     torch.cuda.synchronize()
     flags = pa.pa_get_error(st.err)
     if flags:
         raise RuntimeError("kernel reported error bits 0x%x" % flags)
+    st.capture()
+    for _ in range(args.warmup):
+        st.g_write.replay()
+        st.g_decode.replay()
+    torch.cuda.synchronize()
 
     clocks = ClockSampler(local_rank)
     clocks.start()
     _barrier(world)
     torch.cuda.synchronize()
-    step_ms, decode_ms = [], []
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    for _ in range(args.steps):
-        flush.fill_(float(_ + 2))
-        e0.record()
-        st.run(time_decode=True)
-        e1.record()
-        e1.synchronize()
-        step_ms.append(e0.elapsed_time(e1))
-        decode_ms.append(st.ev0.elapsed_time(st.ev1))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        l2_flush(flush, k)                 # outside the timed events
+        e = ev[k]
+        e[0].record()
+        st.g_write.replay()
+        e[1].record()
+        st.g_decode.replay()
+        e[2].record()
+        e[3].record()
     torch.cuda.synchronize()
     _barrier(world)
     clk = clocks.stop()
     flags = pa.pa_get_error(st.err)
     if flags:
         raise RuntimeError("kernel reported error bits 0x%x" % flags)
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    decode_ms = [e[1].elapsed_time(e[2]) for e in ev]
 
     ms = statistics.mean(step_ms)
     dms = statistics.mean(decode_ms)
     ms_max = _max_over_ranks(ms, world, device)
 
     # end to end through the public API with host buffers: per step the
-    # inputs go host -> device from pinned memory and the output comes back
+    # inputs go host -> device from pinned memory, the C-ABI calls run eagerly
+    # and the output comes back
     host = {
         "q": st.q.cpu().pin_memory(), "k_new": st.k_new.cpu().pin_memory(),
         "v_new": st.v_new.cpu().pin_memory(), "block_tables": st.block_tables.cpu().pin_memory(),
@@ -265,8 +303,9 @@ def run_gpu(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
     e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.fill_(1.0)
+    n_e2e = min(args.steps, 200)
+    for i in range(args.warmup + n_e2e):
+        l2_flush(flush, i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for name, t in host.items():
@@ -325,37 +364,46 @@ def cores():
         return os.cpu_count() or 1
 
 
-def oracle_rate(wl, budget_s, seqs_cap=None):
-    """Time the fp64 oracle's step (cache write + decode) on a bounded sample
-    of sequences; returns (seq-steps/s, sample description, seconds)."""
-    import oracle
-    n_cores = cores()
-    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
-    slots = oracle.slot_mapping(wl.block_tables, wl.new_seq, wl.new_pos, wl.block_size)
-    N = wl.num_seqs if seqs_cap is None else min(wl.num_seqs, seqs_cap)
-    # calibrate on a few sequences, then size the sample to the budget
-    probe = np.arange(min(N, 4), dtype=np.int32)
-    t0 = time.perf_counter()
-    oracle.paged_decode(wl.q, kc, vc, wl.dtype, wl.block_tables, wl.seq_lens, wl.scale,
-                        seq_ids=probe, threads=n_cores)
-    per_seq = max((time.perf_counter() - t0) / len(probe), 1e-5)
-    n = int(min(N, max(1, budget_s / per_seq)))
-    ids = np.arange(n, dtype=np.int32)
-    mask = np.isin(wl.new_seq, ids)
-    done, t_total, reps = 0, 0.0, 0
-    while True:
+class OracleStep:
+    """The fp64 oracle's step (cache write of the sampled sequences' new tokens
+    + decode of all their query heads) on the host cores."""
+
+    def __init__(self, wl):
+        import oracle
+        self.oracle, self.wl = oracle, wl
+        self.cores = cores()
+        self.kc, self.vc = wl.k_cache.copy(), wl.v_cache.copy()
+        self.slots = oracle.slot_mapping(wl.block_tables, wl.new_seq, wl.new_pos, wl.block_size)
+
+    def run(self, n):
+        wl, o = self.wl, self.oracle
+        ids = np.arange(n, dtype=np.int32)
+        mask = np.isin(wl.new_seq, ids)
         t0 = time.perf_counter()
-        oracle.cache_write(kc, vc, wl.k_new[mask], wl.v_new[mask], slots[mask])
-        oracle.paged_decode(wl.q, kc, vc, wl.dtype, wl.block_tables, wl.seq_lens, wl.scale,
-                            seq_ids=ids, threads=n_cores)
-        t_total += time.perf_counter() - t0
+        o.cache_write(self.kc, self.vc, wl.k_new[mask], wl.v_new[mask], self.slots[mask])
+        o.paged_decode(wl.q, self.kc, self.vc, wl.dtype, wl.block_tables, wl.seq_lens, wl.scale,
+                       seq_ids=ids, threads=self.cores)
+        return time.perf_counter() - t0
+
+    def sample_size(self, budget_s):
+        """Sequences whose step fits in about budget_s seconds."""
+        probe = min(self.wl.num_seqs, 4)
+        per_seq = max(self.run(probe) / probe, 1e-6)
+        return int(min(self.wl.num_seqs, max(1, budget_s / per_seq)))
+
+
+def oracle_rate(wl, budget_s):
+    """Sequence-steps per second of the oracle over about budget_s seconds."""
+    os_ = OracleStep(wl)
+    n = os_.sample_size(min(budget_s, 2.0))
+    done, t_total, reps = 0, 0.0, 0
+    while t_total < budget_s and reps < 1000:
+        t_total += os_.run(n)
         done += n
         reps += 1
-        if t_total >= budget_s or reps >= 1000:
-            break
     sample = "%d of %d sequences x %d repetition(s): cache write of their new tokens + fp64 " \
              "decode of all their query heads" % (n, wl.num_seqs, reps)
-    return done / t_total, sample, t_total, n_cores
+    return done / t_total, sample, t_total, os_.cores
 
 
 def run_reference(args):
@@ -363,20 +411,24 @@ def run_reference(args):
     if rank != 0:
         return
     wl = W.CONFIGS[args.workload](seed=_seed(args))
+    os_ = OracleStep(wl)
+    # the whole run stays within about two minutes of CPU time
+    per_step = min(args.ref_step_seconds, max(0.05, 120.0 / (args.steps + args.warmup)))
+    n = os_.sample_size(per_step)
     rates = []
-    sample = None
-    n_cores = cores()
     for i in range(args.warmup + args.steps):
-        r, sample, _, n_cores = oracle_rate(wl, budget_s=args.ref_step_seconds)
+        t = os_.run(n)
         if i >= args.warmup:
-            rates.append(r)
+            rates.append(n / t)
     value = statistics.mean(rates)
+    sample = "%d of %d sequences per step: cache write of their new tokens + fp64 decode of " \
+             "all their query heads" % (n, wl.num_seqs)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "config": _config(wl, args),
-        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": n_cores,
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": os_.cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -401,14 +453,15 @@ def _config(wl, args):
         "total_context_tokens": int(wl.seq_lens.sum()), "max_seq_len": wl.max_seq_len,
         "new_tokens_per_step": int(wl.new_seq.size), "copy_pairs": int(wl.copy_pairs.shape[0]),
         "seed": _seed(args), "recipe": wl.recipe,
-        "l2": "flushed between timed steps by a %d MiB device write" % (L2_FLUSH_BYTES >> 20),
+        "l2": "flushed between timed steps: a %d MiB device buffer is written, then read" %
+              (L2_FLUSH_BYTES >> 20),
     }
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3-8b-gqa", choices=sorted(W.CONFIGS))
@@ -416,6 +469,8 @@ def main():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-blocks", type=int, default=None,
+                    help="smaller pool for the Llama-3-8B workload (profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

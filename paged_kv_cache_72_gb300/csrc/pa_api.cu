@@ -1,5 +1,7 @@
 // Library-wide entry points: error reporting, version, device attributes and
 // the tensor-map encoder lookup.
+#include <stdio.h>
+
 #include <mutex>
 
 #include "pa_host.h"
@@ -15,18 +17,16 @@ std::mutex g_mu;
 
 int current_device_info(DeviceInfo* info) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaError_t e = cudaGetDevice(&dev)) return launch_status(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_have[dev]) {
     DeviceInfo d{};
     d.device = dev;
-    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
-                               dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin,
-                               dev) != cudaSuccess)
-      return PA_ERR_CUDA;
+    cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (!e) e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (!e) e = cudaDeviceGetAttribute(&d.smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e) return launch_status(e, "cudaDeviceGetAttribute");
     g_info[dev] = d;
     g_have[dev] = true;
   }
@@ -46,6 +46,19 @@ EncodeTiledFn encode_tiled_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   });
   return fn;
+}
+
+namespace {
+thread_local char g_err_msg[256];
+}  // namespace
+
+void note_cuda_error(int code, const char* where) {
+  if (code >= 1000)  // a driver-API result (tensor-map encoding)
+    snprintf(g_err_msg, sizeof(g_err_msg), "CUDA call failed (%s: CUresult %d)", where,
+             code - 1000);
+  else
+    snprintf(g_err_msg, sizeof(g_err_msg), "CUDA call failed (%s: %s: %s)", where,
+             cudaGetErrorName((cudaError_t)code), cudaGetErrorString((cudaError_t)code));
 }
 
 }  // namespace pa
@@ -74,7 +87,7 @@ const char* pa_strerror(int status) {
     case PA_ERR_INVALID_ARG: return "invalid argument";
     case PA_ERR_UNSUPPORTED: return "unsupported shape";
     case PA_ERR_WORKSPACE: return "decode workspace too small";
-    case PA_ERR_CUDA: return "CUDA call failed";
+    case PA_ERR_CUDA: return pa::g_err_msg[0] ? pa::g_err_msg : "CUDA call failed";
     case PA_ERR_DEVICE_INDEX: return "a kernel reported an out-of-range index";
     default: return "unknown status";
   }

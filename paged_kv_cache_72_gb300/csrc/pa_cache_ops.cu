@@ -115,6 +115,7 @@ int pa_slot_mapping(const int32_t* block_tables, int32_t table_stride, int32_t n
   const int threads = 256;
   long long blocks = (num_tokens + threads - 1) / threads;
   if (blocks > (long long)di.sm_count * 16) blocks = (long long)di.sm_count * 16;
+  clear_stale_error();
   slot_mapping_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
       block_tables, table_stride, num_seqs, token_seq, token_pos, num_tokens, ilog2(block_size),
       num_blocks, slot_mapping, err_word);
@@ -134,6 +135,7 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, in
     return PA_ERR_INVALID_ARG;
   const int vecs = num_kv_heads * head_dim * 2 / 16;
   const int threads = vecs >= 256 ? 256 : (vecs >= 128 ? 128 : 64);
+  clear_stale_error();
   cache_write_kernel<<<(unsigned)num_tokens, threads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, vecs,
       num_blocks * (long long)block_size, static_cast<uint4*>(k_cache),
@@ -153,6 +155,7 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
   const long long vecs = (long long)block_size * num_kv_heads * head_dim * 2 / 16;
   if (vecs > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   dim3 grid((unsigned)num_pairs, 2);
+  clear_stale_error();
   copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       src_dst_pairs, num_pairs, num_blocks, (int)vecs, static_cast<uint4*>(k_cache),
       static_cast<uint4*>(v_cache), err_word);

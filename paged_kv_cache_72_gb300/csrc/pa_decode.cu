@@ -3,6 +3,8 @@
 // KV pools, and the C entry points.
 #include <string.h>
 
+#include <mutex>
+
 #include "pa_decode_kernel.cuh"
 #include "pa_decode_launch.h"
 
@@ -66,19 +68,56 @@ int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas,
   q.merge_off = q.stages * q.stage_bytes;
   q.ctrl_off = q.merge_off + merge_bytes;
   q.smem_bytes = 1024 + q.ctrl_off + ctrl_bytes(q.stages);
+  q.smem_optin = di.smem_per_block;
 
-  if (num_ctas > 0) {
-    q.grid = num_ctas;
-  } else {
-    int per_sm = 0;
-    const int rc = D == 64 ? decode_ctas_per_sm_d64(q, &per_sm) : decode_ctas_per_sm_d128(q, &per_sm);
-    if (rc != PA_OK) return rc;
-    if (per_sm < 1) return PA_ERR_UNSUPPORTED;
-    q.grid = di.sm_count * per_sm;
-  }
+  // opts the kernel in to its shared memory and reports its occupancy
+  int per_sm = 0;
+  const int rc = D == 64 ? decode_ctas_per_sm_d64(q, &per_sm) : decode_ctas_per_sm_d128(q, &per_sm);
+  if (rc != PA_OK) return rc;
+  if (per_sm < 1) return PA_ERR_UNSUPPORTED;
+  q.grid = num_ctas > 0 ? num_ctas : di.sm_count * per_sm;
   q.ws_meta_bytes = gather ? 0 : (((size_t)q.grid * 8 * sizeof(int) + 255) / 256) * 256;
   q.ws_rec_bytes = gather ? 0 : (size_t)q.grid * 2 * G * (D + 2) * sizeof(float);
   *p = q;
+  return PA_OK;
+}
+
+// Plans depend only on the shape and the device: keep them, so that a call
+// does no attribute or occupancy queries after the first one for its shape.
+struct PlanKey {
+  int dev, Hq, Hkv, D, B, dtype, flags, num_ctas, gather;
+  bool operator==(const PlanKey& o) const {
+    return dev == o.dev && Hq == o.Hq && Hkv == o.Hkv && D == o.D && B == o.B &&
+           dtype == o.dtype && flags == o.flags && num_ctas == o.num_ctas && gather == o.gather;
+  }
+};
+constexpr int kPlanCache = 64;
+PlanKey g_plan_key[kPlanCache];
+DecodePlan g_plan[kPlanCache];
+int g_plan_n = 0, g_plan_next = 0;
+std::mutex g_plan_mu;
+
+int cached_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas, bool gather,
+                DecodePlan* p) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    // still report shape errors without a device
+    return make_plan(Hq, Hkv, D, B, dtype, flags, num_ctas, gather, p);
+  }
+  const PlanKey k{dev, Hq, Hkv, D, B, dtype, flags, num_ctas, gather ? 1 : 0};
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    for (int i = 0; i < g_plan_n; ++i)
+      if (g_plan_key[i] == k) {
+        *p = g_plan[i];
+        return PA_OK;
+      }
+  }
+  if (int rc = make_plan(Hq, Hkv, D, B, dtype, flags, num_ctas, gather, p)) return rc;
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
+  g_plan_key[slot] = k;
+  g_plan[slot] = *p;
   return PA_OK;
 }
 
@@ -106,16 +145,18 @@ int encode_kv_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int 
     box[0] = 64; box[1] = D / 64; box[2] = 1; box[3] = p.R; box[4] = 1;
   }
   memset(map, 0, sizeof(*map));
-  const CUresult r =
+  CUresult r =
       enc(map, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
           const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           p.swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+  if (r == CUDA_SUCCESS) return PA_OK;
+  note_cuda_error(1000 + (int)r, "cuTensorMapEncodeTiled");
+  return PA_ERR_CUDA;
 }
 
-int encode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* kc, const void* vc, DecodePlan* p,
-                int Hkv, long long nb) {
+int encode_maps_uncached(CUtensorMap* tk, CUtensorMap* tv, const void* kc, const void* vc,
+                         DecodePlan* p, int Hkv, long long nb) {
   if (p->split_rows) {
     if (encode_kv_map(tk, kc, *p, Hkv, nb, true) == PA_OK &&
         encode_kv_map(tv, vc, *p, Hkv, nb, true) == PA_OK)
@@ -124,6 +165,58 @@ int encode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* kc, const void* vc
   }
   if (int rc = encode_kv_map(tk, kc, *p, Hkv, nb, false)) return rc;
   return encode_kv_map(tv, vc, *p, Hkv, nb, false);
+}
+
+// Tensor maps depend on the pools' addresses and shape: keep the recent ones.
+struct alignas(64) MapEntry {
+  CUtensorMap tk, tv;
+  const void* kc;
+  const void* vc;
+  long long nb;
+  int dev, Hkv, D, B, bf16, swz, split_in, split_out;
+};
+constexpr int kMapCache = 16;
+MapEntry g_maps[kMapCache];
+int g_maps_n = 0, g_maps_next = 0;
+std::mutex g_maps_mu;
+
+int encode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* kc, const void* vc, DecodePlan* p,
+                int Hkv, long long nb) {
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return launch_status(e, "cudaGetDevice");
+  const int split_in = p->split_rows ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lk(g_maps_mu);
+    for (int i = 0; i < g_maps_n; ++i) {
+      const MapEntry& m = g_maps[i];
+      if (m.kc == kc && m.vc == vc && m.nb == nb && m.dev == dev && m.Hkv == Hkv && m.D == p->D &&
+          m.B == p->B && m.bf16 == (p->bf16 ? 1 : 0) && m.swz == (p->swz ? 1 : 0) &&
+          m.split_in == split_in) {
+        *tk = m.tk;
+        *tv = m.tv;
+        p->split_rows = m.split_out != 0;
+        return PA_OK;
+      }
+    }
+  }
+  if (int rc = encode_maps_uncached(tk, tv, kc, vc, p, Hkv, nb)) return rc;
+  std::lock_guard<std::mutex> lk(g_maps_mu);
+  const int slot = g_maps_n < kMapCache ? g_maps_n++ : (g_maps_next++ % kMapCache);
+  MapEntry& m = g_maps[slot];
+  m.tk = *tk;
+  m.tv = *tv;
+  m.kc = kc;
+  m.vc = vc;
+  m.nb = nb;
+  m.dev = dev;
+  m.Hkv = Hkv;
+  m.D = p->D;
+  m.B = p->B;
+  m.bf16 = p->bf16 ? 1 : 0;
+  m.swz = p->swz ? 1 : 0;
+  m.split_in = split_in;
+  m.split_out = p->split_rows ? 1 : 0;
+  return PA_OK;
 }
 
 void fill_layout(const DecodePlan& p, DecodeArgs* a) {
@@ -165,8 +258,8 @@ int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t 
                              size_t* bytes) {
   if (!bytes) return PA_ERR_INVALID_ARG;
   DecodePlan p;
-  if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
-                         false, &p))
+  if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
+                           false, &p))
     return rc;
   *bytes = p.ws_meta_bytes + p.ws_rec_bytes;
   return PA_OK;
@@ -180,8 +273,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               int32_t* err_word, pa_stream stream) {
   if (num_seqs < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   DecodePlan p;
-  if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
-                         false, &p))
+  if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
+                           false, &p))
     return rc;
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out || !workspace)
@@ -218,8 +311,8 @@ int pa_gather_kv(const void* k_cache, const void* v_cache, const int32_t* block_
                  int32_t* err_word, pa_stream stream) {
   if (num_seqs < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   DecodePlan p;
-  if (int rc = make_plan(num_kv_heads, num_kv_heads, head_dim, block_size, dtype, flags, 0, true,
-                         &p))
+  if (int rc = cached_plan(num_kv_heads, num_kv_heads, head_dim, block_size, dtype, flags, 0, true,
+                           &p))
     return rc;
   if (num_seqs == 0) return PA_OK;
   if (!k_cache || !v_cache || !block_tables || !seq_lens || !out_offsets || !k_out || !v_out)

@@ -568,6 +568,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     meta[4] = (int)cpc;
   }
   __syncthreads();
+  // let the merge kernel (a programmatic dependent launch) get scheduled; it
+  // still waits for this whole grid before reading anything
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (n_chunks == 0) return;
   if (ctrl[0] < 0) {   // cannot happen for a consistent scan; never walk blind
     if (tid == 0) set_error(a.err, PA_DEVERR_SEQ_LEN);
@@ -730,6 +733,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(128) split_reduce_kernel(const DecodeArgs a) {
+  // wait until the decode grid has finished and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int* meta = a.ws_meta + (size_t)blockIdx.x * 8;
   if (meta[0] == 0) return;
   const int i = meta[1], h = meta[2];

@@ -17,6 +17,7 @@ struct DecodePlan {
   int D, G, B, R, nsb;
   int stages;
   int kv_bytes, stage_bytes, merge_off, ctrl_off, smem_bytes;
+  int smem_optin;    // the device's per-block shared-memory maximum
   int grid;
   size_t ws_meta_bytes, ws_rec_bytes;
 };

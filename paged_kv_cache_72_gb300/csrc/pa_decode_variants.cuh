@@ -47,16 +47,18 @@ int with_variant(const DecodePlan& p, F&& f) {
 #undef PA_V
 }
 
+// Opt the variant in to the device's full shared memory (one kernel serves
+// plans of different sizes, so the limit is the device maximum, not this
+// plan's size) and report resident CTAs per SM for this plan.
 template <int D>
 int ctas_per_sm_impl(const DecodePlan& p, int* ctas) {
   return with_variant<D>(p, [&](auto kern) -> int {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         p.smem_optin);
+    if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute");
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, p.smem_bytes) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, p.smem_bytes);
+    if (e != cudaSuccess) return launch_status(e, "occupancy query");
     *ctas = n;
     return PA_OK;
   });
@@ -65,19 +67,28 @@ int ctas_per_sm_impl(const DecodePlan& p, int* ctas) {
 template <int D>
 int launch_impl(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
                 const DecodeArgs& a, cudaStream_t s) {
+  clear_stale_error();
   int rc = with_variant<D>(p, [&](auto kern) -> int {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
     kern<<<p.grid, kThreads, p.smem_bytes, s>>>(tk, tv, a);
-    return launch_status(cudaGetLastError());
+    return launch_status(cudaGetLastError(), "decode kernel launch");
   });
   if (rc != PA_OK || p.mode == kModeGather || p.grid < 2) return rc;
-  if (p.bf16)
-    split_reduce_kernel<D, true><<<p.grid, 128, 0, s>>>(a);
-  else
-    split_reduce_kernel<D, false><<<p.grid, 128, 0, s>>>(a);
-  return launch_status(cudaGetLastError());
+  // the merge kernel is launched as a programmatic dependent of the decode
+  // grid: it is scheduled while the decode grid drains and waits on the
+  // grid-dependency barrier before it reads the partial states
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = p.bf16 ? cudaLaunchKernelEx(&cfg, split_reduce_kernel<D, true>, a)
+                         : cudaLaunchKernelEx(&cfg, split_reduce_kernel<D, false>, a);
+  return launch_status(e, "merge kernel launch");
 }
 
 }  // namespace pa

@@ -36,7 +36,22 @@ inline int ilog2(long long x) {
   return r;
 }
 
+// Records the CUDA error behind a PA_ERR_CUDA (per host thread) so that
+// pa_strerror can name it.
+void note_cuda_error(int code, const char* where);
+
 // Kernel launch status -> library status.
-inline int launch_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+inline int launch_status(cudaError_t e, const char* where = "kernel launch") {
+  if (e == cudaSuccess) return PA_OK;
+  note_cuda_error((int)e, where);
+  return PA_ERR_CUDA;
+}
+
+// Clears an error left by an earlier, already reported runtime call so that
+// the check after the next launch sees only that launch.
+inline void clear_stale_error() {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) note_cuda_error((int)e, "an earlier runtime call (cleared)");
+}
 
 }  // namespace pa

@@ -150,6 +150,15 @@ def test_bad_block_id_is_reported_not_faulted(cuda_device):
     assert pa.pa_get_error(st.err) == pa.PA_DEVERR_BLOCK_ID
 
 
+def test_alternating_shapes_of_one_kernel(cuda_device):
+    # group sizes 4 and 2 run the same kernel with different shared-memory
+    # layouts; calling them in turn must keep working
+    a = W.random_workload(15, W.BF16, 8, 2, 128, 16, [300, 5])
+    b = W.random_workload(16, W.BF16, 4, 2, 128, 16, [70, 900, 1])
+    for wl in (a, b, a, b):
+        _parity(wl)
+
+
 def test_empty_batch(cuda_device):
     q = torch.zeros((0, 8, 128), dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros((4, 16, 2, 128), dtype=torch.bfloat16, device="cuda")

@@ -226,12 +226,12 @@ def llama3_8b_lengths(seed=3, num_seqs=256):
     return np.clip(lens, 16, 4096).astype(np.int32)
 
 
-def llama3_8b(seed=3, num_seqs=256, garbage="random"):
+def llama3_8b(seed=3, num_seqs=256, garbage="random", num_blocks=40_000):
     """Llama-3-8B GQA layer: 32 q heads / 8 KV heads, head_dim 128, bf16, block
     16; 256 sequences with lognormal lengths (mean about 400, sigma 0.632 in
     log space), clipped to [16, 4096]; 40,000-block pool; K/V ~ N(0, 0.5^2)."""
     lens = llama3_8b_lengths(seed, num_seqs)
-    return decode_workload("llama3-8b-gqa", BF16, 32, 8, 128, 16, 40_000, lens, seed,
+    return decode_workload("llama3-8b-gqa", BF16, 32, 8, 128, 16, num_blocks, lens, seed,
                            q_sigma=1.0, kv_sigma=0.5, garbage=garbage,
                            recipe="T ~ round(lognormal(ln400 - 0.632^2/2, 0.632)) clipped to "
                                   "[16,4096]; q ~ N(0,1), k,v ~ N(0,0.25) bf16; free list = "
