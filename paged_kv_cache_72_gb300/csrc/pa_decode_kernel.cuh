@@ -192,24 +192,39 @@ struct MmaConsumer {
       }
       __syncwarp();
     }
-    // S = Q . K^T : two n-tiles of 8 tokens
-    float s[2][4];
+    // S = Q . K^T : two n-tiles of 8 tokens.  All K fragments are loaded
+    // first, then the MMAs run as four independent accumulation chains (two
+    // n-tiles x even / odd k-steps), so no MMA waits on a fragment load.
+    uint32_t kb[2][D / 32][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
       const int tt = tile0 + nt * 8 + (lane & 7);
 #pragma unroll
       for (int kp = 0; kp < D / 32; ++kp) {
         const int cidx = kp * 4 + (lane >> 3);
         const uint32_t ra = row_addr<D>(kpart, tt, cidx >> 3, log2R, hil, rl);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(chunk_addr<kSwz>(ra, cidx & 7), b0, b1, b2, b3);
-        mma_16816<kBF16>(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0,
-                         b1);
-        mma_16816<kBF16>(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2],
-                         qa[2 * kp + 1][3], b2, b3);
+        ldmatrix_x4(chunk_addr<kSwz>(ra, cidx & 7), kb[nt][kp][0], kb[nt][kp][1], kb[nt][kp][2],
+                    kb[nt][kp][3]);
       }
     }
+    float s[2][4], s2[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
+#pragma unroll
+    for (int kp = 0; kp < D / 32; ++kp)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        mma_16816<kBF16>(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3],
+                         kb[nt][kp][0], kb[nt][kp][1]);
+        mma_16816<kBF16>(s2[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2],
+                         qa[2 * kp + 1][3], kb[nt][kp][2], kb[nt][kp][3]);
+      }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
     // online softmax, in the log2 domain, per query-head row
     uint32_t pa[4];
 #pragma unroll
@@ -242,17 +257,20 @@ struct MmaConsumer {
       pa[hr + 2] = p23;   // tokens 8 + 2tig, 9 + 2tig
     }
     if (!kHi) { pa[1] = 0u; pa[3] = 0u; }
-    // O += P . V : pairs of n-tiles of 8 head_dim columns
+    // O += P . V : pairs of n-tiles of 8 head_dim columns; fragments first
+    uint32_t vb[D / 16][4];
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) {
       const int mat = lane >> 3;
       const int tt = tile0 + ((mat & 1) << 3) + (lane & 7);
       const int cidx = 2 * j + (mat >> 1);
       const uint32_t ra = row_addr<D>(vpart, tt, cidx >> 3, log2R, hil, rl);
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4_trans(chunk_addr<kSwz>(ra, cidx & 7), b0, b1, b2, b3);
-      mma_16816<kBF16>(o[2 * j], pa[0], pa[1], pa[2], pa[3], b0, b1);
-      mma_16816<kBF16>(o[2 * j + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+      ldmatrix_x4_trans(chunk_addr<kSwz>(ra, cidx & 7), vb[j][0], vb[j][1], vb[j][2], vb[j][3]);
+    }
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      mma_16816<kBF16>(o[2 * j], pa[0], pa[1], pa[2], pa[3], vb[j][0], vb[j][1]);
+      mma_16816<kBF16>(o[2 * j + 1], pa[0], pa[1], pa[2], pa[3], vb[j][2], vb[j][3]);
     }
   }
 
@@ -511,8 +529,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // ---- find this CTA's range of chunks -------------------------------------
+  // The work is the list of 64-token chunks over (sequence, KV head), in
+  // sequence-major, then head, then chunk order, cut into equal contiguous
+  // ranges of cpc chunks.  One pass: each thread sums the chunks of a
+  // contiguous run of sequences, one block-wide scan gives every run's offset,
+  // and the thread whose run holds this CTA's first chunk locates it.
+  const int per = (a.num_seqs + kThreads - 1) / kThreads;
+  const int run0 = min(a.num_seqs, tid * per), run1 = min(a.num_seqs, run0 + per);
   long long my_nc = 0;
-  for (int i = tid; i < a.num_seqs; i += kThreads) {
+  for (int i = run0; i < run1; ++i) {
     const int T0 = __ldg(a.seq_lens + i);
     const int T = clamp_len(T0, a.stride, a.B);
     my_nc += (T + kChunk - 1) / kChunk;
@@ -524,42 +549,26 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   }
-  // total over the block
-  {
-    long long v = my_nc;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) scan_tmp[warp] = v;
-  }
-  __syncthreads();
-  long long total_nc = 0;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) total_nc += scan_tmp[w];
-  __syncthreads();
+  long long total_nc;
+  const long long my_excl = block_scan_incl(my_nc, scan_tmp, total_nc) - my_nc;
   const long long U = total_nc * a.Hkv;
   const long long cpc = (U + gridDim.x - 1) / gridDim.x;
   const long long start = (long long)blockIdx.x * cpc;
   const long long end = min(U, start + cpc);
   const int n_chunks = (start < end) ? (int)(end - start) : 0;
-
-  if (n_chunks > 0) {
-    // locate the sequence holding chunk `start`
-    long long off = 0;
-    for (int i0 = 0; i0 < a.num_seqs; i0 += kThreads) {
-      const int i = i0 + tid;
-      int nc = 0;
-      if (i < a.num_seqs) nc = (clamp_len(__ldg(a.seq_lens + i), a.stride, a.B) + kChunk - 1) / kChunk;
-      long long tot;
-      const long long incl = block_scan_incl(nc, scan_tmp, tot);
-      const long long lo = (off + incl - nc) * a.Hkv, hi = (off + incl) * a.Hkv;
-      if (i < a.num_seqs && nc > 0 && start >= lo && start < hi) {
-        const long long rem = start - lo;
+  if (n_chunks > 0 && my_nc > 0 && start >= my_excl * a.Hkv && start < (my_excl + my_nc) * a.Hkv) {
+    long long off = my_excl * a.Hkv;
+    for (int i = run0; i < run1; ++i) {
+      const int nc = (clamp_len(__ldg(a.seq_lens + i), a.stride, a.B) + kChunk - 1) / kChunk;
+      const long long span = (long long)nc * a.Hkv;
+      if (nc > 0 && start < off + span) {
+        const long long rem = start - off;
         ctrl[0] = i;
         ctrl[1] = (int)(rem / nc);
         ctrl[2] = (int)(rem % nc);
+        break;
       }
-      off += tot;
-      if (off * a.Hkv > start) break;   // uniform across the block
+      off += span;
     }
   }
   if (kMode != kModeGather && tid == 0) {
