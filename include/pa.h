@@ -170,7 +170,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * calls share the one array: calls that overlap on the GPU (for instance on two
  * streams) race and must be serialized by the caller.
  */
-#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

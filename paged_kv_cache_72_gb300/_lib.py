@@ -25,7 +25,7 @@ PA_DEVERR_POSITION = 0x20
 PA_DECODE_AUTO = 0
 PA_DECODE_SIMT = 1
 PA_DECODE_MMA = 2
-PA_NOALLOC_SCRATCH_BYTES = 8 << 20
+PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32

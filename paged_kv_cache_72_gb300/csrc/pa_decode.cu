@@ -14,14 +14,15 @@ namespace {
 
 constexpr int kMaxStages = 8;
 
-int ctrl_bytes(int stages) { return 16 * stages + 64 + 32; }
+// mbarriers (16 B per stage, 16 B per query buffer), scan scratch (128 B),
+// control words (32 B)
+int ctrl_bytes(int stages) { return 16 * stages + 16 * kQBufs + 128 + 32; }
 
 int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas, bool gather,
               DecodePlan* p) {
   if (Hq <= 0 || Hkv <= 0 || num_ctas < 0) return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
-  // one producer lane issues one TMA box of min(B, 64) rows: at most 32 boxes
   if (!is_pow2(B) || B < 2 || B > 256) return PA_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
@@ -33,39 +34,48 @@ int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas,
   q.D = D;
   q.G = G;
   q.B = B;
+  bool want_swz;
   if (gather) {
     q.mode = kModeGather;
-    q.swz = (flags != PA_DECODE_SIMT) && B >= 8;
+    want_swz = flags != PA_DECODE_SIMT;
   } else if (flags == PA_DECODE_SIMT || (flags == PA_DECODE_AUTO && G == 1)) {
     if (G != 1) return PA_ERR_UNSUPPORTED;
     q.mode = kModeSimt;
-    q.swz = false;
+    want_swz = false;
   } else {
     q.mode = kModeMma;
-    q.swz = B >= 8;
+    want_swz = true;
   }
   q.hi = q.mode == kModeMma && G > 8;
-  q.split_rows = q.swz && D == 128;
-  q.R = B < kChunk ? B : kChunk;
-  q.nsb = kChunk / q.R;
-  q.kv_bytes = kChunk * D * 2;
-  const int qpart = gather ? 0 : ((G * D * 2 + 1023) / 1024) * 1024;
-  q.stage_bytes = 2 * q.kv_bytes + qpart;
-  const int merge_bytes = gather ? 0 : kCWarps * (32 + G * D) * 4;
+  // heads per group: the largest power of two (at most 8) dividing H_kv, with
+  // at most 64 query rows per group
+  q.HG = (Hkv % 8 == 0) ? 8 : (Hkv % 4 == 0) ? 4 : (Hkv % 2 == 0) ? 2 : 1;
+  while (q.HG > 1 && q.HG * G > 64) q.HG /= 2;
+  q.NGR = Hkv / q.HG;
+  q.TPH = kCWarps / q.HG;
+  q.CT = kTile * q.TPH;
+  q.R = B < q.CT ? B : q.CT;
+  q.nsb = q.CT / q.R;
+  if (q.nsb > 32) return PA_ERR_UNSUPPORTED;   // one producer lane per TMA box
+  const int box_bytes = q.R * q.HG * D * 2;
+  q.swz = want_swz && (box_bytes % 1024 == 0);
+  q.split_rows = true;
+  q.kv_bytes = q.CT * q.HG * D * 2;
+  q.stage_bytes = 2 * q.kv_bytes;
+  q.q_bytes = gather ? 0 : q.HG * G * D * 2;
+  q.q_stride = ((q.q_bytes + 127) / 128) * 128;
+  const int merge_bytes = (gather || q.TPH == 1) ? 0 : kCWarps * (32 + G * D) * 4;
 
   DeviceInfo di;
   if (int rc = current_device_info(&di)) return rc;
-  q.stages = 0;
-  for (int target = 2; target >= 1 && q.stages == 0; --target) {
-    int budget = di.smem_per_sm / target - 1024;
-    if (budget > di.smem_per_block) budget = di.smem_per_block;
-    const int avail = budget - 1024 - merge_bytes - ctrl_bytes(kMaxStages);
-    int s = avail / q.stage_bytes;
-    if (s > kMaxStages) s = kMaxStages;
-    if (s >= 2) q.stages = s;
-  }
-  if (q.stages == 0) return PA_ERR_UNSUPPORTED;
-  q.merge_off = q.stages * q.stage_bytes;
+  const int avail = di.smem_per_block - 1024 - kQBufs * q.q_stride - merge_bytes -
+                    ctrl_bytes(kMaxStages);
+  int st = avail / q.stage_bytes;
+  if (st > kMaxStages) st = kMaxStages;
+  if (st < 2) return PA_ERR_UNSUPPORTED;
+  q.stages = st;
+  q.q_off = q.stages * q.stage_bytes;
+  q.merge_off = q.q_off + kQBufs * q.q_stride;
   q.ctrl_off = q.merge_off + merge_bytes;
   q.smem_bytes = 1024 + q.ctrl_off + ctrl_bytes(q.stages);
   q.smem_optin = di.smem_per_block;
@@ -77,7 +87,7 @@ int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas,
   if (per_sm < 1) return PA_ERR_UNSUPPORTED;
   q.grid = num_ctas > 0 ? num_ctas : di.sm_count * per_sm;
   q.ws_meta_bytes = gather ? 0 : (((size_t)q.grid * 8 * sizeof(int) + 255) / 256) * 256;
-  q.ws_rec_bytes = gather ? 0 : (size_t)q.grid * 2 * G * (D + 2) * sizeof(float);
+  q.ws_rec_bytes = gather ? 0 : (size_t)q.grid * 2 * rec_floats(q.HG * G, D) * sizeof(float);
   *p = q;
   return PA_OK;
 }
@@ -121,10 +131,11 @@ int cached_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_cta
   return PA_OK;
 }
 
-// TMA map over one pool [num_blocks][B][Hkv][D]: one box = R rows of one head
-// of one block, all D elements.  With split_rows the box lands as two
-// [R][64] planes (dims: d_lo, row, d_hi, head, block); otherwise as R rows of
-// D contiguous elements (dims: d_lo, d_hi, head, row, block).
+// TMA map over one pool [num_blocks][B][Hkv][D]: one box = R rows of HG
+// heads of one block, all D elements.  With split_rows the box lands as
+// [HG][D/64][R][64] (dims: d_lo, row, d_hi, head, block), so that eight
+// consecutive rows of one head sit in eight consecutive 128-byte lines;
+// otherwise as [R][HG][D/64][64] (dims: d_lo, d_hi, head, row, block).
 int encode_kv_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int Hkv,
                   long long num_blocks, bool split_rows) {
   EncodeTiledFn enc = encode_tiled_fn();
@@ -138,11 +149,11 @@ int encode_kv_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int 
   if (split_rows) {
     dims[0] = 64; dims[1] = B; dims[2] = D / 64; dims[3] = Hkv; dims[4] = num_blocks;
     strides[0] = row; strides[1] = 128; strides[2] = (cuuint64_t)D * 2; strides[3] = row * B;
-    box[0] = 64; box[1] = p.R; box[2] = D / 64; box[3] = 1; box[4] = 1;
+    box[0] = 64; box[1] = p.R; box[2] = D / 64; box[3] = p.HG; box[4] = 1;
   } else {
     dims[0] = 64; dims[1] = D / 64; dims[2] = Hkv; dims[3] = B; dims[4] = num_blocks;
     strides[0] = 128; strides[1] = (cuuint64_t)D * 2; strides[2] = row; strides[3] = row * B;
-    box[0] = 64; box[1] = D / 64; box[2] = 1; box[3] = p.R; box[4] = 1;
+    box[0] = 64; box[1] = D / 64; box[2] = p.HG; box[3] = p.R; box[4] = 1;
   }
   memset(map, 0, sizeof(*map));
   CUresult r =
@@ -223,21 +234,32 @@ void fill_layout(const DecodePlan& p, DecodeArgs* a) {
   a->G = p.G;
   a->B = p.B;
   a->log2B = ilog2(p.B);
+  a->HG = p.HG;
+  a->NGR = a->Hkv / p.HG;
+  a->TPH = p.TPH;
+  a->CT = p.CT;
   a->R = p.R;
   a->log2R = ilog2(p.R);
   a->nsb = p.nsb;
   a->stages = p.stages;
   a->kv_bytes = p.kv_bytes;
   a->stage_bytes = p.stage_bytes;
+  a->q_off = p.q_off;
+  a->q_bytes = p.q_bytes;
+  a->q_stride = p.q_stride;
   a->merge_off = p.merge_off;
   a->ctrl_off = p.ctrl_off;
   a->split_rows = p.split_rows ? 1 : 0;
+  const int lrow = ilog2((long long)p.D * 2);         // one row of one head
+  a->sub_log2 = a->log2R + ilog2(p.HG) + lrow;         // one box
   if (p.split_rows) {
+    a->head_log2 = a->log2R + lrow;
     a->hi_log2 = a->log2R + 7;
     a->r_log2 = 7;
   } else {
+    a->head_log2 = lrow;
     a->hi_log2 = 7;
-    a->r_log2 = p.D == 128 ? 8 : 7;
+    a->r_log2 = ilog2(p.HG) + lrow;
   }
 }
 

@@ -7,23 +7,30 @@
 // per-layer pool [num_blocks][B][H_kv][D].  Query head hq reads KV head hq / G.
 //
 // Design (one GPU, persistent, HBM-bound):
-//  * Work is the flattened list of 64-token chunks over (sequence, KV head),
-//    split into equal contiguous ranges, one per CTA (grid = a multiple of the
-//    SM count).  Every CTA scans seq_lens once to find its range; a sequence's
-//    context may therefore be split across CTAs, whose partial softmax states
-//    (m, l, o) a second kernel merges.  The split depends only on seq_lens, so
-//    the result does not depend on block placement.
-//  * One producer warp streams each chunk's K and V rows with 5-D TMA tensor
-//    copies (one box per physical block or per 64 rows of it) into a ring of
-//    shared-memory stages guarded by mbarriers, reading the block table one
-//    chunk ahead.  The G query rows of the chunk's KV head come along by a 1-D
-//    bulk copy whenever a new (sequence, head) segment starts, so the query
-//    group shares every K/V byte it loads.
-//  * Four consumer warps each take 16 tokens of every chunk and keep their own
-//    online-softmax state in fp32; at a segment end they merge through shared
-//    memory.  The tensor-core consumer computes S = Q.K^T and O += P.V with
+//  * KV heads are taken in groups of HG (the largest of 8, 4, 2, 1 that divides
+//    H_kv).  A pipeline stage holds CT = 128 / HG tokens of every head of one
+//    group, so that one TMA box carries R = min(B, CT) rows of all HG heads of
+//    one physical block: for 16-token blocks and 8 KV heads that is one 32 KB
+//    box per block for K and one for V.
+//  * The work is the list of chunks (sequence, head group, CT tokens), cut into
+//    equal contiguous ranges, one per CTA (grid = the SM count).  Every CTA
+//    scans seq_lens once to find its range; a context may be split across
+//    CTAs, whose partial softmax states (m, l, o) a second kernel merges.  The
+//    split depends only on seq_lens, so the result does not depend on where the
+//    blocks sit.
+//  * One producer warp reads the block table one chunk ahead and streams each
+//    chunk's K and V boxes with 5-D TMA tensor copies into a ring of shared-
+//    memory stages guarded by mbarriers.  When a new (sequence, head group)
+//    segment starts it first fetches the group's HG * G query rows with a 1-D
+//    bulk copy into a small ring of query buffers.  Each K/V byte is read once
+//    and shared by the G query heads of its KV head.
+//  * Eight consumer warps: warp w takes 16 tokens (tile w % TPH, TPH = 8 / HG)
+//    of head w / TPH of every chunk and keeps its own online-softmax state in
+//    fp32.  The tensor-core consumer computes S = Q.K^T and O += P.V with
 //    m16n8k16 MMAs (query heads on M, tokens / head_dim on N); the CUDA-core
 //    consumer (group size 1) uses per-lane head_dim slices and warp shuffles.
+//    When a warp owns its head alone (HG = 8) it writes its result directly;
+//    otherwise the TPH warps of a head merge through shared memory.
 //  * Every wait is bounded; a wait that gives up sets PA_DEVERR_TIMEOUT and the
 //    CTA runs to its end without touching the pipeline again.
 #pragma once
@@ -34,11 +41,11 @@
 
 namespace pa {
 
-constexpr int kChunk = 64;     // tokens per pipeline stage
-constexpr int kTile = 16;      // tokens per consumer warp per stage
-constexpr int kCWarps = kChunk / kTile;
-constexpr int kThreads = (kCWarps + 1) * 32;
+constexpr int kTile = 16;          // tokens per consumer warp per stage
+constexpr int kCWarps = 8;         // consumer warps; stage = kCWarps * 16 token-heads
 constexpr int kProducerWarp = kCWarps;
+constexpr int kThreads = (kCWarps + 1) * 32;
+constexpr int kQBufs = 2;          // query-row buffers in flight
 
 enum Mode : int { kModeSimt = 0, kModeMma = 1, kModeGather = 2 };
 
@@ -47,22 +54,24 @@ struct DecodeArgs {
   uint16_t* out;             // [N][Hq][D]
   const int32_t* bt;         // [N][stride]
   const int32_t* seq_lens;   // [N]
-  float* ws_rec;             // [grid][2][G][D + 2]: m[G], l[G], o[G][D]
-  int* ws_meta;              // [grid][8]: needs, i, h, seg_start, cpc
+  float* ws_rec;             // [grid][2] records of rec_floats(HG*G, D): o[][D], m[], l[]
+  int* ws_meta;              // [grid][8]: needs merge, i, head group, segment start, cpc
   int32_t* err;
   const int64_t* out_off;    // gather: first output row of each sequence
   uint16_t* k_out;           // gather outputs [rows][H_kv][D]
   uint16_t* v_out;
   long long num_blocks;
-  int num_seqs, stride, Hq, Hkv, G, B, log2B, R, log2R, nsb;
+  int num_seqs, stride, Hq, Hkv, G, B, log2B;
+  int HG, NGR, TPH, CT, R, log2R, nsb;   // heads per group, groups, tiles per head, tokens per chunk
   int stages;
   float scale_log2;          // scale * log2(e)
-  int split_rows;            // 1: box rows stored as [D/64][R][64]; 0: as [R][D]
-  int hi_log2;               // log2 byte stride between the two 64-element halves of a row
-  int r_log2;                // log2 byte stride between rows of a box
-  int kv_bytes;              // bytes of one K (or V) stage part: 64 * D * 2
-  int stage_bytes;           // K part + V part + Q part (multiple of 1024)
-  int merge_off;             // byte offset of the merge buffer
+  int split_rows;            // box layout: 1 = [HG][D/64][R][64], 0 = [R][HG][D/64][64]
+  int sub_log2, head_log2, hi_log2, r_log2;   // byte strides inside a stage part (log2)
+  int kv_bytes;              // bytes of one K (or V) stage part: CT * HG * D * 2
+  int stage_bytes;           // K part + V part (multiple of 1024)
+  int q_off, q_bytes;        // query ring offset and one buffer's bytes (HG * G * D * 2)
+  int q_stride;              // bytes between query buffers (multiple of 128)
+  int merge_off;             // byte offset of the merge buffer (TPH > 1)
   int ctrl_off;              // byte offset of barriers and control words
 };
 
@@ -72,19 +81,19 @@ __device__ __forceinline__ int clamp_len(int T, int stride, int B) {
 }
 
 struct Walk {
-  int i, h, c, nc, T;
+  int i, g, c, nc, T;   // sequence, head group, chunk, chunks of the sequence, its length
 };
 
 __device__ __forceinline__ void walk_load_seq(Walk& w, const DecodeArgs& a) {
   w.T = clamp_len(__ldg(a.seq_lens + w.i), a.stride, a.B);
-  w.nc = (w.T + kChunk - 1) / kChunk;
+  w.nc = (w.T + a.CT - 1) / a.CT;
 }
 
 __device__ __forceinline__ void walk_advance(Walk& w, const DecodeArgs& a) {
   if (++w.c < w.nc) return;
   w.c = 0;
-  if (++w.h < a.Hkv) return;
-  w.h = 0;
+  if (++w.g < a.NGR) return;
+  w.g = 0;
   do {
     ++w.i;
     if (w.i >= a.num_seqs) { w.nc = 0; w.T = 0; return; }
@@ -92,7 +101,7 @@ __device__ __forceinline__ void walk_advance(Walk& w, const DecodeArgs& a) {
   } while (w.nc == 0);
 }
 
-// Block-wide inclusive scan of one int per thread (kThreads threads).
+// Block-wide inclusive scan of one value per thread (kThreads threads).
 __device__ __forceinline__ long long block_scan_incl(long long v, long long* warp_tot,
                                                      long long& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -115,18 +124,13 @@ __device__ __forceinline__ long long block_scan_incl(long long v, long long* war
   return v + off;
 }
 
-// Address of row `tt` (0..63 within the chunk), half `hi` of a stage part.
-// One TMA box holds R rows of D elements; boxes follow each other.  Inside a
-// box a row's two 64-element halves are either adjacent (r stride D*2, half
-// stride 128) or split into two [R][64] planes (r stride 128, half stride
-// R*128), which makes 8 consecutive rows hit 8 distinct swizzle phases.
-template <int D>
-__device__ __forceinline__ uint32_t row_addr(uint32_t part, int tt, int hi, int log2R, int hi_log2,
-                                             int r_log2) {
-  const int sub = tt >> log2R;
-  const int r = tt & ((1 << log2R) - 1);
-  return part + ((uint32_t)sub << (log2R + (D == 128 ? 8 : 7))) + ((uint32_t)hi << hi_log2) +
-         ((uint32_t)r << r_log2);
+// Address of token row `tt` (0..CT-1 within the chunk), half `hi` of head
+// part `hpart` (the stage part plus the head's offset).
+__device__ __forceinline__ uint32_t row_addr(uint32_t hpart, int tt, int hi, const DecodeArgs& a) {
+  const int sub = tt >> a.log2R;
+  const int r = tt & ((1 << a.log2R) - 1);
+  return hpart + ((uint32_t)sub << a.sub_log2) + ((uint32_t)hi << a.hi_log2) +
+         ((uint32_t)r << a.r_log2);
 }
 
 template <bool kSwz>
@@ -134,6 +138,12 @@ __device__ __forceinline__ uint32_t chunk_addr(uint32_t row, int j) {
   // 128-byte swizzle: the 16-byte chunk index is XOR-ed with address bits 7..9
   const int s = kSwz ? (int)((row >> 7) & 7) : 0;
   return row + ((uint32_t)(j ^ s) << 4);
+}
+
+// A partial-state record of `rows` query rows: o[rows][D], then m[rows] and
+// l[rows], padded so that every record (and every o row) starts on 16 bytes.
+__host__ __device__ __forceinline__ size_t rec_floats(int rows, int D) {
+  return (size_t)rows * D + (size_t)((2 * rows + 3) & ~3);
 }
 
 // ---------------------------------------------------------------------------
@@ -147,6 +157,7 @@ struct MmaConsumer {
   float o[NT][4];
   float m[2], l[2];
 
+  // qslot: this head's G query rows [G][D]
   __device__ __forceinline__ void begin(uint32_t qslot, int G) {
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
 #pragma unroll
@@ -174,24 +185,12 @@ struct MmaConsumer {
     l[0] = l[1] = 0.f;
   }
 
-  // 16 tokens [tile0, tile0 + 16) of the stage; `nv` of them are valid.
+  // 16 tokens [tile0, tile0 + 16) of the chunk for this warp's head; `nv` of
+  // them are valid (rows past the sequence's end may hold anything, NaN
+  // included: their scores are masked and their V values zeroed in registers).
   __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int nv,
-                                       int log2R, int hil, int rl, float sl2) {
+                                       const DecodeArgs& a, float sl2) {
     const int lane = threadIdx.x & 31, tig = lane & 3;
-    if (nv < kTile) {
-      // rows past the end of the sequence may hold anything (NaN included):
-      // zero them in V so that 0 * garbage cannot reach the accumulator
-      const int nbad = kTile - nv;
-      for (int e = lane; e < nbad * (D / 8); e += 32) {
-        const int rr = tile0 + nv + e / (D / 8);
-        const int cj = e % (D / 8);
-        const uint32_t ra = row_addr<D>(vpart, rr, cj >> 3, log2R, hil, rl);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(ra + ((cj & 7) << 4)),
-                     "r"(0)
-                     : "memory");
-      }
-      __syncwarp();
-    }
     // S = Q . K^T : two n-tiles of 8 tokens.  All K fragments are loaded
     // first, then the MMAs run as four independent accumulation chains (two
     // n-tiles x even / odd k-steps), so no MMA waits on a fragment load.
@@ -202,7 +201,7 @@ struct MmaConsumer {
 #pragma unroll
       for (int kp = 0; kp < D / 32; ++kp) {
         const int cidx = kp * 4 + (lane >> 3);
-        const uint32_t ra = row_addr<D>(kpart, tt, cidx >> 3, log2R, hil, rl);
+        const uint32_t ra = row_addr(kpart, tt, cidx >> 3, a);
         ldmatrix_x4(chunk_addr<kSwz>(ra, cidx & 7), kb[nt][kp][0], kb[nt][kp][1], kb[nt][kp][2],
                     kb[nt][kp][3]);
       }
@@ -225,6 +224,17 @@ struct MmaConsumer {
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
+    // V fragments, loaded before the softmax math so that their latency hides
+    // behind it
+    uint32_t vb[D / 16][4];
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      const int mat = lane >> 3;
+      const int tt = tile0 + ((mat & 1) << 3) + (lane & 7);
+      const int cidx = 2 * j + (mat >> 1);
+      const uint32_t ra = row_addr(vpart, tt, cidx >> 3, a);
+      ldmatrix_x4_trans(chunk_addr<kSwz>(ra, cidx & 7), vb[j][0], vb[j][1], vb[j][2], vb[j][3]);
+    }
     // online softmax, in the log2 domain, per query-head row
     uint32_t pa[4];
 #pragma unroll
@@ -257,16 +267,21 @@ struct MmaConsumer {
       pa[hr + 2] = p23;   // tokens 8 + 2tig, 9 + 2tig
     }
     if (!kHi) { pa[1] = 0u; pa[3] = 0u; }
-    // O += P . V : pairs of n-tiles of 8 head_dim columns; fragments first
-    uint32_t vb[D / 16][4];
+    if (nv < kTile) {
+      // zero the V values of tokens past the end (the low 16 bits of a
+      // fragment register hold token 2tig (+8), the high bits token 2tig+1)
+      const uint32_t mlo = (2 * tig < nv ? 0x0000ffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
+      const uint32_t mhi =
+          (8 + 2 * tig < nv ? 0x0000ffffu : 0u) | (9 + 2 * tig < nv ? 0xffff0000u : 0u);
 #pragma unroll
-    for (int j = 0; j < D / 16; ++j) {
-      const int mat = lane >> 3;
-      const int tt = tile0 + ((mat & 1) << 3) + (lane & 7);
-      const int cidx = 2 * j + (mat >> 1);
-      const uint32_t ra = row_addr<D>(vpart, tt, cidx >> 3, log2R, hil, rl);
-      ldmatrix_x4_trans(chunk_addr<kSwz>(ra, cidx & 7), vb[j][0], vb[j][1], vb[j][2], vb[j][3]);
+      for (int j = 0; j < D / 16; ++j) {
+        vb[j][0] &= mlo;
+        vb[j][2] &= mlo;
+        vb[j][1] &= mhi;
+        vb[j][3] &= mhi;
+      }
     }
+    // O += P . V : pairs of n-tiles of 8 head_dim columns
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) {
       mma_16816<kBF16>(o[2 * j], pa[0], pa[1], pa[2], pa[3], vb[j][0], vb[j][1]);
@@ -296,6 +311,41 @@ struct MmaConsumer {
       }
     }
   }
+
+  // A warp that holds a whole head's segment writes it directly: the output
+  // rows (full context) or the partial state record (rows rec_row0 ..).
+  __device__ __forceinline__ void write_direct(uint16_t* out_rows, float* rec, int rec_row0,
+                                               int rec_rows, bool full, int G) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int hr = 0; hr < (kHi ? 2 : 1); ++hr) {
+      float lt = l[hr];
+      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+      const int row = gid + 8 * hr;
+      if (row < G) {
+        if (full) {
+          const float inv = 1.f / lt;
+          uint16_t* orow = out_rows + (size_t)row * D;
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+            *reinterpret_cast<uint32_t*>(orow + n * 8 + 2 * tig) =
+                pack2<kBF16>(o[n][hr * 2] * inv, o[n][hr * 2 + 1] * inv);
+        } else {
+          const int r = rec_row0 + row;
+          if (tig == 0) {
+            rec[(size_t)rec_rows * D + r] = m[hr];
+            rec[(size_t)rec_rows * D + rec_rows + r] = lt;
+          }
+          float* orow = rec + (size_t)r * D;
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+            *reinterpret_cast<float2*>(orow + n * 8 + 2 * tig) =
+                make_float2(o[n][hr * 2], o[n][hr * 2 + 1]);
+        }
+      }
+    }
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -310,20 +360,20 @@ struct SimtConsumer {
 
   __device__ __forceinline__ int col() const { return (threadIdx.x & 31) * VEC; }
 
-  __device__ __forceinline__ void load_row(uint32_t part, int tt, int log2R, int hil, int rl,
+  __device__ __forceinline__ void load_row(uint32_t part, int tt, const DecodeArgs& a,
                                            float* x) const {
     const int c = col();
-    const uint32_t ra = row_addr<D>(part, tt, c >> 6, log2R, hil, rl) + (uint32_t)((c & 63) * 2);
+    const uint32_t ra = row_addr(part, tt, c >> 6, a) + (uint32_t)((c & 63) * 2);
     if constexpr (VEC == 4) {
       uint32_t w0, w1;
       asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(ra));
-      const float2 a = unpack2<kBF16>(w0), b = unpack2<kBF16>(w1);
-      x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+      const float2 p = unpack2<kBF16>(w0), q = unpack2<kBF16>(w1);
+      x[0] = p.x; x[1] = p.y; x[2] = q.x; x[3] = q.y;
     } else {
       uint32_t w0;
       asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(ra));
-      const float2 a = unpack2<kBF16>(w0);
-      x[0] = a.x; x[1] = a.y;
+      const float2 p = unpack2<kBF16>(w0);
+      x[0] = p.x; x[1] = p.y;
     }
   }
 
@@ -344,14 +394,14 @@ struct SimtConsumer {
   }
 
   __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int nv,
-                                       int log2R, int hil, int rl, float sl2) {
+                                       const DecodeArgs& a, float sl2) {
     const int lane = threadIdx.x & 31;
     // partial dot products of the 16 tokens over this lane's head_dim slice
     float part[kTile];
 #pragma unroll
     for (int t = 0; t < kTile; ++t) {
       float x[VEC];
-      load_row(kpart, tile0 + t, log2R, hil, rl, x);
+      load_row(kpart, tile0 + t, a, x);
       float acc = 0.f;
 #pragma unroll
       for (int v = 0; v < VEC; ++v) acc = fmaf(qf[v], x[v], acc);
@@ -391,7 +441,7 @@ struct SimtConsumer {
       for (int t = 0; t < kTile; ++t) {
         const float pt = __shfl_sync(0xffffffffu, p, 2 * t);
         float x[VEC];
-        load_row(vpart, tile0 + t, log2R, hil, rl, x);
+        load_row(vpart, tile0 + t, a, x);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) o[v] = fmaf(pt, x[v], o[v]);
       }
@@ -399,19 +449,23 @@ struct SimtConsumer {
       for (int t = 0; t < nv; ++t) {
         const float pt = __shfl_sync(0xffffffffu, p, 2 * t);
         float x[VEC];
-        load_row(vpart, tile0 + t, log2R, hil, rl, x);
+        load_row(vpart, tile0 + t, a, x);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) o[v] = fmaf(pt, x[v], o[v]);
       }
     }
   }
 
-  __device__ __forceinline__ void store(float* slot, int /*G*/) {
-    const int lane = threadIdx.x & 31;
+  __device__ __forceinline__ float total_l() const {
     float lt = l;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-    if (lane == 0) {
+    return lt;
+  }
+
+  __device__ __forceinline__ void store(float* slot, int /*G*/) {
+    const float lt = total_l();
+    if ((threadIdx.x & 31) == 0) {
       slot[0] = m;
       slot[16] = lt;
     }
@@ -419,33 +473,50 @@ struct SimtConsumer {
 #pragma unroll
     for (int v = 0; v < VEC; ++v) orow[col() + v] = o[v];
   }
+
+  __device__ __forceinline__ void write_direct(uint16_t* out_rows, float* rec, int rec_row0,
+                                               int rec_rows, bool full, int /*G*/) {
+    const float lt = total_l();
+    const int c = col();
+    if (full) {
+      const float inv = 1.f / lt;
+#pragma unroll
+      for (int v = 0; v < VEC; v += 2)
+        *reinterpret_cast<uint32_t*>(out_rows + c + v) = pack2<kBF16>(o[v] * inv, o[v + 1] * inv);
+    } else {
+      if ((threadIdx.x & 31) == 0) {
+        rec[(size_t)rec_rows * D + rec_row0] = m;
+        rec[(size_t)rec_rows * D + rec_rows + rec_row0] = lt;
+      }
+      float* orow = rec + (size_t)rec_row0 * D;
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) orow[c + v] = o[v];
+    }
+  }
 };
 
 // ---------------------------------------------------------------------------
-// Segment merge across the consumer warps and the output / partial write.
+// Segment merge across the TPH warps of each head and the output / partial
+// write (used when a head is split over several warps, TPH > 1).
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16>
 __device__ __forceinline__ void merge_and_write(const DecodeArgs& a, const float* mbuf, int i,
-                                                int h, bool full, int slot_idx) {
-  const int G = a.G;
+                                                int grp, bool full, int slot_idx) {
+  const int G = a.G, HG = a.HG, TPH = a.TPH;
+  const int rows = HG * G;
   const int slot_floats = 32 + G * D;
-  const int tid = threadIdx.x;  // 0..127 (consumer warps)
-  float* rec = a.ws_rec + ((size_t)blockIdx.x * 2 + slot_idx) * (size_t)G * (D + 2);
-  for (int e = tid; e < G * (D / 2); e += kCWarps * 32) {
-    const int g = e / (D / 2);
+  float* rec = a.ws_rec + ((size_t)blockIdx.x * 2 + slot_idx) * rec_floats(rows, D);
+  for (int e = threadIdx.x; e < rows * (D / 2); e += kCWarps * 32) {
+    const int r = e / (D / 2);             // row = head_local * G + g
     const int d = 2 * (e % (D / 2));
-    float mw[kCWarps];
+    const int hl = r / G, g = r - hl * G;
     float mx = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kCWarps; ++w) {
-      mw[w] = mbuf[w * slot_floats + g];
-      mx = fmaxf(mx, mw[w]);
-    }
+    for (int t = 0; t < TPH; ++t) mx = fmaxf(mx, mbuf[(hl * TPH + t) * slot_floats + g]);
     float L = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCWarps; ++w) {
-      const float wt = (mw[w] == -INFINITY) ? 0.f : exp2f(mw[w] - mx);
-      const float* sw = mbuf + w * slot_floats;
+    for (int t = 0; t < TPH; ++t) {
+      const float* sw = mbuf + (hl * TPH + t) * slot_floats;
+      const float mw = sw[g];
+      const float wt = (mw == -INFINITY) ? 0.f : exp2f(mw - mx);
       const float2 ov = *reinterpret_cast<const float2*>(sw + 32 + g * D + d);
       L = fmaf(wt, sw[16 + g], L);
       o0 = fmaf(wt, ov.x, o0);
@@ -453,33 +524,30 @@ __device__ __forceinline__ void merge_and_write(const DecodeArgs& a, const float
     }
     if (full) {
       const float inv = 1.f / L;
-      const uint32_t packed = pack2<kBF16>(o0 * inv, o1 * inv);
-      uint16_t* dst = a.out + ((size_t)i * a.Hq + (size_t)h * G + g) * D + d;
-      *reinterpret_cast<uint32_t*>(dst) = packed;
+      uint16_t* dst = a.out + ((size_t)i * a.Hq + (size_t)grp * rows + r) * D + d;
+      *reinterpret_cast<uint32_t*>(dst) = pack2<kBF16>(o0 * inv, o1 * inv);
     } else {
-      *reinterpret_cast<float2*>(rec + 2 * G + g * D + d) = make_float2(o0, o1);
+      *reinterpret_cast<float2*>(rec + (size_t)r * D + d) = make_float2(o0, o1);
       if (d == 0) {
-        rec[g] = mx;
-        rec[G + g] = L;
+        rec[(size_t)rows * D + r] = mx;
+        rec[(size_t)rows * D + rows + r] = L;
       }
     }
   }
 }
 
-// Gather mode: copy the valid rows of this warp's 16-token tile to the
-// contiguous outputs, undoing the shared-memory layout.
+// Gather mode: copy the valid rows of this warp's 16-token tile of its head to
+// the contiguous outputs, undoing the shared-memory layout.
 template <int D, bool kSwz>
 __device__ __forceinline__ void gather_tile(const DecodeArgs& a, uint32_t kpart, uint32_t vpart,
-                                            int tile0, int nv, int i, int h, int c) {
+                                            int tile0, int nv, int i, int head, int c) {
   const int lane = threadIdx.x & 31;
-  const long long row0 = __ldg(a.out_off + i) + (long long)c * kChunk + tile0;
+  const long long row0 = __ldg(a.out_off + i) + (long long)c * a.CT + tile0;
   for (int e = lane; e < nv * (D / 8); e += 32) {
     const int r = e / (D / 8);
     const int cj = e % (D / 8);
-    const uint32_t ka = chunk_addr<kSwz>(
-        row_addr<D>(kpart, tile0 + r, cj >> 3, a.log2R, a.hi_log2, a.r_log2), cj & 7);
-    const uint32_t va = chunk_addr<kSwz>(
-        row_addr<D>(vpart, tile0 + r, cj >> 3, a.log2R, a.hi_log2, a.r_log2), cj & 7);
+    const uint32_t ka = chunk_addr<kSwz>(row_addr(kpart, tile0 + r, cj >> 3, a), cj & 7);
+    const uint32_t va = chunk_addr<kSwz>(row_addr(vpart, tile0 + r, cj >> 3, a), cj & 7);
     uint4 kv, vv;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(kv.x), "=r"(kv.y), "=r"(kv.z), "=r"(kv.w)
@@ -487,7 +555,7 @@ __device__ __forceinline__ void gather_tile(const DecodeArgs& a, uint32_t kpart,
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(vv.x), "=r"(vv.y), "=r"(vv.z), "=r"(vv.w)
                  : "r"(va));
-    const size_t off = (((size_t)(row0 + r) * a.Hkv + h) * D) + cj * 8;
+    const size_t off = (((size_t)(row0 + r) * a.Hkv + head) * D) + cj * 8;
     *reinterpret_cast<uint4*>(a.k_out + off) = kv;
     *reinterpret_cast<uint4*>(a.v_out + off) = vv;
   }
@@ -497,7 +565,7 @@ __device__ __forceinline__ void gather_tile(const DecodeArgs& a, uint32_t kpart,
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16, int kMode, bool kSwz, bool kHi>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -510,8 +578,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int S = a.stages;
   const uint32_t bar_full = base + a.ctrl_off;      // S x 8 bytes
   const uint32_t bar_empty = bar_full + 8 * S;      // S x 8 bytes
-  long long* const scan_tmp = reinterpret_cast<long long*>(gbase + a.ctrl_off + 16 * S);
-  int* const ctrl = reinterpret_cast<int*>(gbase + a.ctrl_off + 16 * S + 8 * 8);
+  const uint32_t bar_qfull = bar_empty + 8 * S;     // kQBufs x 8 bytes
+  const uint32_t bar_qempty = bar_qfull + 8 * kQBufs;
+  const int ctrl_words = a.ctrl_off + 16 * S + 16 * kQBufs;
+  long long* const scan_tmp = reinterpret_cast<long long*>(gbase + ctrl_words);
+  int* const ctrl = reinterpret_cast<int*>(gbase + ctrl_words + 8 * 16);
   volatile int* const abort_flag = ctrl + 4;
 
   if (tid == 0) {
@@ -519,6 +590,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, kCWarps);
+    }
+    for (int s = 0; s < kQBufs; ++s) {
+      mbar_init(bar_qfull + 8 * s, 1);
+      mbar_init(bar_qempty + 8 * s, kCWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -529,18 +604,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // ---- find this CTA's range of chunks -------------------------------------
-  // The work is the list of 64-token chunks over (sequence, KV head), in
-  // sequence-major, then head, then chunk order, cut into equal contiguous
-  // ranges of cpc chunks.  One pass: each thread sums the chunks of a
-  // contiguous run of sequences, one block-wide scan gives every run's offset,
-  // and the thread whose run holds this CTA's first chunk locates it.
+  // The work is the list of chunks over (sequence, head group, CT tokens), in
+  // that order, cut into equal contiguous ranges of cpc chunks.  One pass:
+  // each thread sums the chunks of a contiguous run of sequences, one
+  // block-wide scan gives every run's offset, and the thread whose run holds
+  // this CTA's first chunk locates it.
   const int per = (a.num_seqs + kThreads - 1) / kThreads;
   const int run0 = min(a.num_seqs, tid * per), run1 = min(a.num_seqs, run0 + per);
   long long my_nc = 0;
   for (int i = run0; i < run1; ++i) {
     const int T0 = __ldg(a.seq_lens + i);
     const int T = clamp_len(T0, a.stride, a.B);
-    my_nc += (T + kChunk - 1) / kChunk;
+    my_nc += (T + a.CT - 1) / a.CT;
     if ((i % gridDim.x) == blockIdx.x) {
       if (T != T0) set_error(a.err, PA_DEVERR_SEQ_LEN);
       if (kMode != kModeGather && T == 0) {
@@ -551,16 +626,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   long long total_nc;
   const long long my_excl = block_scan_incl(my_nc, scan_tmp, total_nc) - my_nc;
-  const long long U = total_nc * a.Hkv;
+  const long long U = total_nc * a.NGR;
   const long long cpc = (U + gridDim.x - 1) / gridDim.x;
   const long long start = (long long)blockIdx.x * cpc;
   const long long end = min(U, start + cpc);
   const int n_chunks = (start < end) ? (int)(end - start) : 0;
-  if (n_chunks > 0 && my_nc > 0 && start >= my_excl * a.Hkv && start < (my_excl + my_nc) * a.Hkv) {
-    long long off = my_excl * a.Hkv;
+  if (n_chunks > 0 && my_nc > 0 && start >= my_excl * a.NGR && start < (my_excl + my_nc) * a.NGR) {
+    long long off = my_excl * a.NGR;
     for (int i = run0; i < run1; ++i) {
-      const int nc = (clamp_len(__ldg(a.seq_lens + i), a.stride, a.B) + kChunk - 1) / kChunk;
-      const long long span = (long long)nc * a.Hkv;
+      const int nc = (clamp_len(__ldg(a.seq_lens + i), a.stride, a.B) + a.CT - 1) / a.CT;
+      const long long span = (long long)nc * a.NGR;
       if (nc > 0 && start < off + span) {
         const long long rem = start - off;
         ctrl[0] = i;
@@ -588,12 +663,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   Walk w0;
   w0.i = ctrl[0];
-  w0.h = ctrl[1];
+  w0.g = ctrl[1];
   w0.c = ctrl[2];
   walk_load_seq(w0, a);
 
-  const int qbytes = (kMode == kModeGather) ? 0 : a.G * D * 2;
-  const uint32_t box_bytes = (uint32_t)(a.R * D * 2);
+  const int qbytes = a.q_bytes;
+  const uint32_t box_bytes = 1u << a.sub_log2;
 
   if (warp == kProducerWarp) {
     // ======================= producer =======================
@@ -602,14 +677,40 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto load_entry = [&](const Walk& ww) -> int {
       int ent = -1;
       if (lane < a.nsb) {
-        const int tok0 = ww.c * kChunk + lane * a.R;
+        const int tok0 = ww.c * a.CT + lane * a.R;
         if (tok0 < ww.T) ent = __ldg(a.bt + (size_t)ww.i * a.stride + (tok0 >> a.log2B));
       }
       return ent;
     };
     int ent = load_entry(w);
     int issued = 0;
+    uint32_t seg = 0;
     for (int n = 0; n < n_chunks; ++n) {
+      const bool seg_start = (n == 0) || (w.c == 0);
+      if (kMode != kModeGather && seg_start) {
+        // this segment's query rows, into query buffer seg % kQBufs once the
+        // consumers have taken the rows of segment seg - kQBufs out of it
+        const int qb = (int)(seg % kQBufs);
+        bool waited = true;
+        if (seg >= kQBufs)
+          waited = mbar_wait_bounded(bar_qempty + 8 * qb, ((seg / kQBufs) - 1) & 1u, abort_flag);
+        const bool timed_out = __any_sync(0xffffffffu, !waited);
+        if (__any_sync(0xffffffffu, timed_out || *abort_flag != 0)) {
+          if (lane == 0) {
+            if (timed_out) set_error(a.err, PA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t qdst = base + a.q_off + (uint32_t)qb * a.q_stride;
+          const uint16_t* qsrc = a.q + ((size_t)w.i * a.Hq + (size_t)w.g * a.HG * a.G) * D;
+          mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)qbytes);
+          bulk_load(qdst, qsrc, (uint32_t)qbytes, bar_qfull + 8 * qb);
+        }
+        __syncwarp();
+        ++seg;
+      }
       const int st = n % S;
       const uint32_t round = (uint32_t)(n / S);
       const bool waited = mbar_wait_bounded(bar_empty + 8 * st, (round & 1u) ^ 1u, abort_flag);
@@ -621,35 +722,34 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         break;
       }
-      const int valid_tok = min(kChunk, w.T - w.c * kChunk);
+      const int valid_tok = min(a.CT, w.T - w.c * a.CT);
       const int nvsub = (valid_tok + a.R - 1) >> a.log2R;
       const bool in_sub = lane < nvsub;
       const bool ok = in_sub && ent >= 0 && (long long)ent < a.num_blocks;
       if (in_sub && !ok) set_error(a.err, PA_DEVERR_BLOCK_ID);
       const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-      const bool seg_start = (n == 0) || (w.c == 0);
       const uint32_t sbase = base + (uint32_t)st * a.stage_bytes;
       if (lane == 0) {
-        const uint32_t tx =
-            (uint32_t)__popc(okmask) * box_bytes * 2u + (seg_start ? (uint32_t)qbytes : 0u);
+        const uint32_t tx = (uint32_t)__popc(okmask) * box_bytes * 2u;
         mbar_arrive_expect_tx(bar_full + 8 * st, tx);
       }
       __syncwarp();
       if (ok) {
-        const int row_off = (w.c * kChunk + lane * a.R) & (a.B - 1);
+        const int row_off = (w.c * a.CT + lane * a.R) & (a.B - 1);
         const uint32_t dk = sbase + (uint32_t)lane * box_bytes;
+        const int h0 = w.g * a.HG;
         if (a.split_rows) {
-          tma_load_5d(dk, &tmk, bar_full + 8 * st, 0, row_off, 0, w.h, ent, pol);
-          tma_load_5d(dk + a.kv_bytes, &tmv, bar_full + 8 * st, 0, row_off, 0, w.h, ent, pol);
+          tma_load_5d(dk, &tmk, bar_full + 8 * st, 0, row_off, 0, h0, ent, pol);
+          tma_load_5d(dk + a.kv_bytes, &tmv, bar_full + 8 * st, 0, row_off, 0, h0, ent, pol);
         } else {
-          tma_load_5d(dk, &tmk, bar_full + 8 * st, 0, 0, w.h, row_off, ent, pol);
-          tma_load_5d(dk + a.kv_bytes, &tmv, bar_full + 8 * st, 0, 0, w.h, row_off, ent, pol);
+          tma_load_5d(dk, &tmk, bar_full + 8 * st, 0, 0, h0, row_off, ent, pol);
+          tma_load_5d(dk + a.kv_bytes, &tmv, bar_full + 8 * st, 0, 0, h0, row_off, ent, pol);
         }
       }
-      if (kMode != kModeGather && lane == 0 && seg_start) {
-        const uint16_t* qsrc = a.q + ((size_t)w.i * a.Hq + (size_t)w.h * a.G) * D;
-        bulk_load(sbase + 2 * a.kv_bytes, qsrc, (uint32_t)qbytes, bar_full + 8 * st);
-      }
+      // at a sequence's first chunk, pull the next sequence's block-table row
+      // towards L1 so that its first entries do not stall the next segment
+      if (w.c == 0 && w.g == 0 && lane < 2 && w.i + 1 < a.num_seqs && lane * 32 < a.stride)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.bt + (size_t)(w.i + 1) * a.stride + lane * 32));
       ++issued;
       walk_advance(w, a);
       if (n + 1 < n_chunks) ent = load_entry(w);
@@ -657,9 +757,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     // drain: make sure no TMA write is still in flight into this CTA's shared
     // memory when it exits (only matters after an abort)
     if (__any_sync(0xffffffffu, *abort_flag != 0)) {
-      for (int k = max(0, issued - S); k < issued; ++k) {
+      for (int k = max(0, issued - S); k < issued; ++k)
         mbar_wait_bounded(bar_full + 8 * (k % S), (uint32_t)(k / S) & 1u, nullptr);
-      }
+      for (uint32_t k = (seg > kQBufs ? seg - kQBufs : 0); k < seg; ++k)
+        mbar_wait_bounded(bar_qfull + 8 * (k % kQBufs), (k / kQBufs) & 1u, nullptr);
     }
     return;
   }
@@ -670,13 +771,37 @@ __global__ void __launch_bounds__(kThreads, 2)
   Consumer cs;
   float* const mbuf = reinterpret_cast<float*>(gbase + a.merge_off);
   const int slot_floats = 32 + a.G * D;
+  const int hl = warp / a.TPH;                 // this warp's head within the group
+  const int tile0 = (warp % a.TPH) * kTile;    // and its 16 tokens of every chunk
+  const uint32_t head_off = (uint32_t)hl << a.head_log2;
+  const int rows = a.HG * a.G;
   Walk w = w0;
   int seg_c0 = w.c;
   bool first_seg = true;
+  uint32_t seg = 0;
   const float sl2 = a.scale_log2;
   for (int n = 0; n < n_chunks; ++n) {
     const int st = n % S;
     const uint32_t round = (uint32_t)(n / S);
+    const bool seg_start = (n == 0) || (w.c == 0);
+    if (seg_start) {
+      seg_c0 = w.c;
+      if constexpr (kMode != kModeGather) {
+        const int qb = (int)(seg % kQBufs);
+        if (!*abort_flag) {
+          if (!mbar_wait_bounded(bar_qfull + 8 * qb, (seg / kQBufs) & 1u, abort_flag) &&
+              lane == 0) {
+            set_error(a.err, PA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+        }
+        if (!__any_sync(0xffffffffu, *abort_flag != 0))
+          cs.begin(base + a.q_off + (uint32_t)qb * a.q_stride + (uint32_t)(hl * a.G * D * 2), a.G);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_qempty + 8 * qb);
+        ++seg;
+      }
+    }
     if (!*abort_flag) {
       if (!mbar_wait_bounded(bar_full + 8 * st, round & 1u, abort_flag)) {
         if (lane == 0) {
@@ -687,27 +812,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const bool live = !__any_sync(0xffffffffu, *abort_flag != 0);
     const uint32_t sbase = base + (uint32_t)st * a.stage_bytes;
-    const uint32_t kpart = sbase, vpart = sbase + a.kv_bytes, qslot = sbase + 2 * a.kv_bytes;
-    const bool seg_start = (n == 0) || (w.c == 0);
-    if (seg_start) {
-      seg_c0 = w.c;
-      if constexpr (kMode != kModeGather) {
-        if (live) cs.begin(qslot, a.G);
-      }
-    }
-    const int valid_tok = min(kChunk, w.T - w.c * kChunk);
-    const int tile0 = warp * kTile;
+    const uint32_t kpart = sbase + head_off, vpart = sbase + a.kv_bytes + head_off;
+    const int valid_tok = min(a.CT, w.T - w.c * a.CT);
     const int nv = max(0, min(kTile, valid_tok - tile0));
     if (live && nv > 0) {
       if constexpr (kMode == kModeGather) {
-        gather_tile<D, kSwz>(a, kpart, vpart, tile0, nv, w.i, w.h, w.c);
+        gather_tile<D, kSwz>(a, kpart, vpart, tile0, nv, w.i, w.g * a.HG + hl, w.c);
       } else {
-        cs.tile(kpart, vpart, tile0, nv, a.log2R, a.hi_log2, a.r_log2, sl2);
+        cs.tile(kpart, vpart, tile0, nv, a, sl2);
       }
     }
-    // this stage may be refilled by TMA once every consumer warp is done; the
-    // rows a warp zeroed must be ordered before that async-proxy write
-    if (kMode == kModeMma && nv > 0 && nv < kTile) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * st);
 
@@ -715,19 +829,28 @@ __global__ void __launch_bounds__(kThreads, 2)
     if constexpr (kMode != kModeGather) {
       if (seg_end) {
         const bool full = (seg_c0 == 0) && (w.c == w.nc - 1);
-        cs.store(mbuf + warp * slot_floats, a.G);
-        asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
-        merge_and_write<D, kBF16>(a, mbuf, w.i, w.h, full, first_seg ? 0 : 1);
+        const int slot_idx = first_seg ? 0 : 1;
+        if (a.TPH == 1) {
+          // this warp holds the whole head: write it out directly
+          uint16_t* out_rows =
+              a.out + ((size_t)w.i * a.Hq + (size_t)(w.g * a.HG + hl) * a.G) * D;
+          float* rec = a.ws_rec + ((size_t)blockIdx.x * 2 + slot_idx) * rec_floats(rows, D);
+          cs.write_direct(out_rows, rec, hl * a.G, rows, full, a.G);
+        } else {
+          cs.store(mbuf + warp * slot_floats, a.G);
+          asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
+          merge_and_write<D, kBF16>(a, mbuf, w.i, w.g, full, slot_idx);
+          asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
+        }
         if (first_seg && seg_c0 > 0 && w.c == w.nc - 1 && tid == 0) {
-          // this CTA finishes a (sequence, head) begun by earlier CTAs: the
-          // reduce kernel merges its pieces
+          // this CTA finishes a (sequence, head group) begun by earlier CTAs:
+          // the reduce kernel merges its pieces
           int* meta = a.ws_meta + (size_t)blockIdx.x * 8;
           meta[1] = w.i;
-          meta[2] = w.h;
+          meta[2] = w.g;
           meta[3] = (int)(start - seg_c0);
           meta[0] = 1;
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
         first_seg = false;
       }
     }
@@ -736,46 +859,79 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
-// Merge of split contexts: one block per decode CTA; the CTA that finished a
-// split (sequence, head) merges the partial states of every CTA that held a
-// piece of it.  out = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k.
+// Merge of split contexts.  Block b works for decode CTA b / slices on the
+// rows [slice * RPB, slice * RPB + RPB) of the (sequence, head group) that
+// CTA finished, when earlier CTAs held pieces of it:
+//   out = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k.
+// First the per-row weights (shared memory), then the weighted sum over the
+// pieces, four head_dim columns per thread, one pass.
 // ---------------------------------------------------------------------------
+constexpr int kReduceThreads = 256;
+constexpr int kReduceMaxPieces = 32;   // pieces whose weights are kept in shared memory
+
+template <int D>
+__host__ __device__ constexpr int reduce_rows_per_block() { return kReduceThreads / (D / 4); }
+
 template <int D, bool kBF16>
-__global__ void __launch_bounds__(128) split_reduce_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const DecodeArgs a) {
+  constexpr int RPB = reduce_rows_per_block<D>();
+  __shared__ float s_w[kReduceMaxPieces][RPB];
+  __shared__ float s_mx[RPB], s_inv[RPB];
   // wait until the decode grid has finished and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int* meta = a.ws_meta + (size_t)blockIdx.x * 8;
+  const int rows = a.HG * a.G;
+  const int slices = (rows + RPB - 1) / RPB;
+  const int last = blockIdx.x / slices;
+  const int r0 = (blockIdx.x % slices) * RPB;
+  const int* meta = a.ws_meta + (size_t)last * 8;
   if (meta[0] == 0) return;
-  const int i = meta[1], h = meta[2];
+  const int i = meta[1], grp = meta[2];
   const long long gstart = meta[3];
   const long long cpc = meta[4];
-  const int G = a.G;
-  const int last = blockIdx.x;
   const int first = (int)(gstart / cpc);
-  const size_t rec_floats = (size_t)G * (D + 2);
-  for (int e = threadIdx.x; e < G * (D / 2); e += blockDim.x) {
-    const int g = e / (D / 2);
-    const int d = 2 * (e % (D / 2));
+  const size_t rf = rec_floats(rows, D);
+  const size_t ml = (size_t)rows * D;   // m[] then l[] follow o[][]
+  auto rec_of = [&](int k) -> const float* {
+    const int slot = (k == first && gstart != (long long)first * cpc) ? 1 : 0;
+    return a.ws_rec + ((size_t)k * 2 + slot) * rf;
+  };
+  // per row: m* = max_k m_k, L = sum_k 2^(m_k - m*) l_k, and the weights
+  if (threadIdx.x < RPB && r0 + threadIdx.x < rows) {
+    const int r = r0 + threadIdx.x;
     float mx = -INFINITY;
+    for (int k = first; k <= last; ++k) mx = fmaxf(mx, rec_of(k)[ml + r]);
+    float L = 0.f;
     for (int k = first; k <= last; ++k) {
-      const int slot = (k == first && gstart != (long long)first * cpc) ? 1 : 0;
-      const float* rec = a.ws_rec + ((size_t)k * 2 + slot) * rec_floats;
-      mx = fmaxf(mx, rec[g]);
+      const float* rec = rec_of(k);
+      const float wt = exp2f(rec[ml + r] - mx);
+      if (k - first < kReduceMaxPieces) s_w[k - first][threadIdx.x] = wt;
+      L = fmaf(wt, rec[ml + rows + r], L);
     }
-    float L = 0.f, o0 = 0.f, o1 = 0.f;
-    for (int k = first; k <= last; ++k) {
-      const int slot = (k == first && gstart != (long long)first * cpc) ? 1 : 0;
-      const float* rec = a.ws_rec + ((size_t)k * 2 + slot) * rec_floats;
-      const float wt = exp2f(rec[g] - mx);
-      L = fmaf(wt, rec[G + g], L);
-      const float2 ov = *reinterpret_cast<const float2*>(rec + 2 * G + g * D + d);
-      o0 = fmaf(wt, ov.x, o0);
-      o1 = fmaf(wt, ov.y, o1);
-    }
-    const float inv = 1.f / L;
-    uint16_t* dst = a.out + ((size_t)i * a.Hq + (size_t)h * G + g) * D + d;
-    *reinterpret_cast<uint32_t*>(dst) = pack2<kBF16>(o0 * inv, o1 * inv);
+    s_mx[threadIdx.x] = mx;
+    s_inv[threadIdx.x] = 1.f / L;
   }
+  __syncthreads();
+  const int rr = threadIdx.x / (D / 4);
+  const int r = r0 + rr;
+  if (r >= rows) return;
+  const int d = 4 * (threadIdx.x % (D / 4));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = first; k <= last; ++k) {
+    const float* rec = rec_of(k);
+    const float wt = (k - first < kReduceMaxPieces) ? s_w[k - first][rr]
+                                                   : exp2f(rec[ml + r] - s_mx[rr]);
+    const float4 ov = *reinterpret_cast<const float4*>(rec + (size_t)r * D + d);
+    acc.x = fmaf(wt, ov.x, acc.x);
+    acc.y = fmaf(wt, ov.y, acc.y);
+    acc.z = fmaf(wt, ov.z, acc.z);
+    acc.w = fmaf(wt, ov.w, acc.w);
+  }
+  const float inv = s_inv[rr];
+  uint16_t* dst = a.out + ((size_t)i * a.Hq + (size_t)grp * rows + r) * D + d;
+  uint2 pk;
+  pk.x = pack2<kBF16>(acc.x * inv, acc.y * inv);
+  pk.y = pack2<kBF16>(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(dst) = pk;
 }
 
 }  // namespace pa

@@ -15,8 +15,9 @@ struct DecodePlan {
   bool hi;           // group size > 8: query heads fill both MMA row halves
   bool split_rows;   // rows of a box stored as two [R][64] planes
   int D, G, B, R, nsb;
+  int HG, NGR, TPH, CT;   // heads per group, groups, tiles per head, tokens per chunk
   int stages;
-  int kv_bytes, stage_bytes, merge_off, ctrl_off, smem_bytes;
+  int kv_bytes, stage_bytes, q_off, q_bytes, q_stride, merge_off, ctrl_off, smem_bytes;
   int smem_optin;    // the device's per-block shared-memory maximum
   int grid;
   size_t ws_meta_bytes, ws_rec_bytes;

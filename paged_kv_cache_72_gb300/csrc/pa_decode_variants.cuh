@@ -77,8 +77,9 @@ int launch_impl(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& t
   // grid: it is scheduled while the decode grid drains and waits on the
   // grid-dependency barrier before it reads the partial states
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(128);
+  const int rpb = reduce_rows_per_block<D>();
+  cfg.gridDim = dim3(p.grid * ((p.HG * p.G + rpb - 1) / rpb));
+  cfg.blockDim = dim3(kReduceThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
