@@ -196,14 +196,16 @@ class Step:
         self.out = torch.empty_like(self.q)
         nbytes = pa.pa_decode_workspace_size(wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
                                              wl.block_size, wl.dtype)
-        self.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+        self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.ev0 = torch.cuda.Event(enable_timing=True)
         self.ev1 = torch.cuda.Event(enable_timing=True)
         self.decode_ms = []
 
     def launches_per_step(self):
-        return (1 if self.pairs.numel() else 0) + 2 + 2
+        # copy-on-write (if any), slot mapping, cache write, decode (the split
+        # merge runs inside the decode grid when it is cooperative)
+        return (1 if self.pairs.numel() else 0) + 2 + 1
 
     def write_phase(self):
         pa, wl = self.pa, self.wl
@@ -224,16 +226,19 @@ class Step:
         self.decode_phase()
 
     def capture(self):
-        """CUDA graphs of the two phases (the calls are the same C-ABI calls;
-        a graph removes the per-call host cost from the GPU timeline)."""
+        """CUDA graphs of the step and of its decode phase alone (the calls are
+        the same C-ABI calls; a graph removes the per-call host cost from the
+        GPU timeline, and inside the step graph each kernel may start while
+        its predecessor drains)."""
         torch = self.torch
-        self.g_write = torch.cuda.CUDAGraph()
+        self.g_step = torch.cuda.CUDAGraph()
         self.g_decode = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            with torch.cuda.graph(self.g_write, stream=s):
+            with torch.cuda.graph(self.g_step, stream=s):
                 self.write_phase()
+                self.decode_phase()
             with torch.cuda.graph(self.g_decode, stream=s):
                 self.decode_phase()
         torch.cuda.current_stream().wait_stream(s)
@@ -259,7 +264,7 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError("kernel reported error bits 0x%x" % flags)
     st.capture()
     for _ in range(args.warmup):
-        st.g_write.replay()
+        st.g_step.replay()
         st.g_decode.replay()
     torch.cuda.synchronize()
 
@@ -267,24 +272,27 @@ def run_gpu(args, rank, world, local_rank):
     clocks.start()
     _barrier(world)
     torch.cuda.synchronize()
+    # timed region: K steps (one graph each), then K decode phases alone for
+    # the decode kernels' own duration; L2 flushed before each, untimed
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for k in range(args.steps):
-        l2_flush(flush, k)                 # outside the timed events
-        e = ev[k]
-        e[0].record()
-        st.g_write.replay()
-        e[1].record()
+        l2_flush(flush, k)
+        ev[k][0].record()
+        st.g_step.replay()
+        ev[k][1].record()
+    for k in range(args.steps):
+        l2_flush(flush, k)
+        ev[k][2].record()
         st.g_decode.replay()
-        e[2].record()
-        e[3].record()
+        ev[k][3].record()
     torch.cuda.synchronize()
     _barrier(world)
     clk = clocks.stop()
     flags = pa.pa_get_error(st.err)
     if flags:
         raise RuntimeError("kernel reported error bits 0x%x" % flags)
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    decode_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    decode_ms = [e[2].elapsed_time(e[3]) for e in ev]
 
     ms = statistics.mean(step_ms)
     dms = statistics.mean(decode_ms)

@@ -140,11 +140,18 @@ int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t 
  *              written this step; 0 gives a zero output row
  *   out        [num_seqs][num_q_heads][head_dim], dtype; must not alias q
  *   scale      multiplies q.k (e.g. 1/sqrt(head_dim))
- *   workspace  device buffer of at least pa_decode_workspace_size() bytes
+ *   workspace  device buffer of at least pa_decode_workspace_size() bytes,
+ *              zero-filled before its first use; every call that completes
+ *              without a device error leaves it ready for the next call (zero it
+ *              again after a PA_DEVERR_TIMEOUT).  Calls sharing one workspace
+ *              must not overlap on the GPU.
  * Query head hq reads KV head hq / G (contiguous query groups).  Accumulation
  * is fp32; the output is rounded once to dtype.  The result does not depend on
- * where the blocks sit in the pool.  Each sequence's context is split across
- * thread blocks in 64-token chunks and merged by a second kernel.
+ * where the blocks sit in the pool.  The work (chunks of one block's worth of
+ * tokens of up to 8 KV heads) is split evenly over a persistent grid; a context
+ * split between thread blocks is merged by the block holding its last piece
+ * (cooperative launch), or by a second kernel when the grid is larger than
+ * the GPU can hold at once.
  * flags: PA_DECODE_AUTO, PA_DECODE_SIMT or PA_DECODE_MMA; num_ctas: 0 = default.
  */
 int pa_decode(const void* q, const void* k_cache, const void* v_cache,

@@ -18,6 +18,8 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ bt, int stride, 
                                     const int32_t* __restrict__ tok_pos, long long n, int log2B,
                                     long long num_blocks, int64_t* __restrict__ slots,
                                     int32_t* err) {
+  grid_dep_wait();
+  grid_dep_launch();
   for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < n;
        k += (long long)gridDim.x * blockDim.x) {
     const int i = tok_seq[k];
@@ -43,6 +45,8 @@ __global__ void cache_write_kernel(const uint4* __restrict__ k, const uint4* __r
                                    const int64_t* __restrict__ slots, int vecs_per_row,
                                    long long num_slots, uint4* __restrict__ kc,
                                    uint4* __restrict__ vc, int32_t* err) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long tok = blockIdx.x;
   const long long s = slots[tok];
   if (s < 0) return;
@@ -67,6 +71,8 @@ __global__ void cache_write_kernel(const uint4* __restrict__ k, const uint4* __r
 __global__ void copy_blocks_kernel(const int32_t* __restrict__ pairs, int num_pairs,
                                    long long num_blocks, int vecs_per_block,
                                    uint4* __restrict__ kc, uint4* __restrict__ vc, int32_t* err) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int p = blockIdx.x;
   const int which = blockIdx.y;  // 0 = K, 1 = V
   const int src = pairs[2 * p], dst = pairs[2 * p + 1];
@@ -116,10 +122,12 @@ int pa_slot_mapping(const int32_t* block_tables, int32_t table_stride, int32_t n
   long long blocks = (num_tokens + threads - 1) / threads;
   if (blocks > (long long)di.sm_count * 16) blocks = (long long)di.sm_count * 16;
   clear_stale_error();
-  slot_mapping_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      block_tables, table_stride, num_seqs, token_seq, token_pos, num_tokens, ilog2(block_size),
-      num_blocks, slot_mapping, err_word);
-  return launch_status(cudaGetLastError());
+  return launch_status(launch_pdl(slot_mapping_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                                  static_cast<cudaStream_t>(stream), false, block_tables,
+                                  (int)table_stride, (int)num_seqs, token_seq, token_pos,
+                                  (long long)num_tokens, ilog2(block_size), (long long)num_blocks,
+                                  slot_mapping, err_word),
+                       "slot mapping launch");
 }
 
 int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
@@ -136,11 +144,13 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, in
   const int vecs = num_kv_heads * head_dim * 2 / 16;
   const int threads = vecs >= 256 ? 256 : (vecs >= 128 ? 128 : 64);
   clear_stale_error();
-  cache_write_kernel<<<(unsigned)num_tokens, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, vecs,
-      num_blocks * (long long)block_size, static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), err_word);
-  return launch_status(cudaGetLastError());
+  return launch_status(launch_pdl(cache_write_kernel, dim3((unsigned)num_tokens), dim3(threads), 0,
+                                  static_cast<cudaStream_t>(stream), false,
+                                  static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                                  slot_mapping, vecs, num_blocks * (long long)block_size,
+                                  static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                  err_word),
+                       "cache write launch");
 }
 
 int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cache, void* v_cache,
@@ -156,10 +166,12 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
   if (vecs > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   dim3 grid((unsigned)num_pairs, 2);
   clear_stale_error();
-  copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      src_dst_pairs, num_pairs, num_blocks, (int)vecs, static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), err_word);
-  return launch_status(cudaGetLastError());
+  return launch_status(launch_pdl(copy_blocks_kernel, grid, dim3(256), 0,
+                                  static_cast<cudaStream_t>(stream), false, src_dst_pairs,
+                                  (int)num_pairs, (long long)num_blocks, (int)vecs,
+                                  static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                  err_word),
+                       "block copy launch");
 }
 
 }  // extern "C"

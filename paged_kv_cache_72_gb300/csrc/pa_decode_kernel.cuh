@@ -56,6 +56,8 @@ struct DecodeArgs {
   const int32_t* seq_lens;   // [N]
   float* ws_rec;             // [grid][2] records of rec_floats(HG*G, D): o[][D], m[], l[]
   int* ws_meta;              // [grid][8]: needs merge, i, head group, segment start, cpc
+  uint32_t* ws_flags;        // [grid][2]: record published (1) / consumed (0); zero between calls
+  int fused;                 // 1: the CTA holding a context's last piece merges it (cooperative grid)
   int32_t* err;
   const int64_t* out_off;    // gather: first output row of each sequence
   uint16_t* k_out;           // gather outputs [rows][H_kv][D]
@@ -562,6 +564,85 @@ __device__ __forceinline__ void gather_tile(const DecodeArgs& a, uint32_t kpart,
 }
 
 // ---------------------------------------------------------------------------
+// In-kernel merge of a split context (cooperative grid): the CTA that holds a
+// (sequence, head group)'s last piece waits for the earlier CTAs' published
+// records, takes them (resetting their flags for the next call) and writes
+// out = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k.  Its own piece is its
+// record in slot 0.  s_row: 130 floats of shared memory.
+// ---------------------------------------------------------------------------
+template <int D, bool kBF16>
+__device__ __forceinline__ void merge_split_in_cta(const DecodeArgs& a, int i, int grp,
+                                                   long long gstart, long long cpc,
+                                                   volatile int* abort_flag, float* s_row) {
+  const int tid = threadIdx.x;   // consumer threads 0 .. kCWarps * 32 - 1
+  const int nthr = kCWarps * 32;
+  const int last = blockIdx.x;
+  const int first = (int)(gstart / cpc);
+  const int rows = a.HG * a.G;
+  const size_t rf = rec_floats(rows, D);
+  const size_t ml = (size_t)rows * D;
+  auto slot_of = [&](int k) -> int {
+    return (k == first && gstart != (long long)first * cpc) ? 1 : 0;
+  };
+  volatile float* const s_ok = s_row + 128;
+  if (tid == 0) {
+    bool ok = !*abort_flag;
+    for (int k = first; k < last && ok; ++k) {
+      volatile uint32_t* f = a.ws_flags + (size_t)k * 2 + slot_of(k);
+      const long long t0 = clock64();
+      while (*f == 0u) {
+        if (*abort_flag || clock64() - t0 > kWaitLimitCycles) { ok = false; break; }
+      }
+      if (ok) *f = 0u;   // taken: clear for the next call
+    }
+    if (!ok) {
+      set_error(a.err, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    *s_ok = ok ? 1.f : 0.f;
+    __threadfence();
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+  if (*s_ok == 0.f) return;   // the same decision in every consumer thread
+  auto rec_of = [&](int k) -> const float* {
+    return a.ws_rec + ((size_t)k * 2 + slot_of(k)) * rf;
+  };
+  for (int r = tid; r < rows; r += nthr) {
+    float mx = -INFINITY;
+    for (int k = first; k <= last; ++k) mx = fmaxf(mx, __ldcg(rec_of(k) + ml + r));
+    float L = 0.f;
+    for (int k = first; k <= last; ++k) {
+      const float* rec = rec_of(k);
+      L = fmaf(exp2f(__ldcg(rec + ml + r) - mx), __ldcg(rec + ml + rows + r), L);
+    }
+    s_row[r] = mx;
+    s_row[64 + r] = 1.f / L;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+  for (int e = tid; e < rows * (D / 4); e += nthr) {
+    const int r = e / (D / 4);
+    const int d = 4 * (e % (D / 4));
+    const float mx = s_row[r];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = first; k <= last; ++k) {
+      const float* rec = rec_of(k);
+      const float wt = exp2f(__ldcg(rec + ml + r) - mx);
+      const float4 ov = __ldcg(reinterpret_cast<const float4*>(rec + (size_t)r * D + d));
+      acc.x = fmaf(wt, ov.x, acc.x);
+      acc.y = fmaf(wt, ov.y, acc.y);
+      acc.z = fmaf(wt, ov.z, acc.z);
+      acc.w = fmaf(wt, ov.w, acc.w);
+    }
+    const float inv = s_row[64 + r];
+    uint16_t* dst = a.out + ((size_t)i * a.Hq + (size_t)grp * rows + r) * D + d;
+    uint2 pk;
+    pk.x = pack2<kBF16>(acc.x * inv, acc.y * inv);
+    pk.y = pack2<kBF16>(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16, int kMode, bool kSwz, bool kHi>
@@ -602,6 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
+  // inputs may come from the previous kernel in the stream
+  grid_dep_wait();
 
   // ---- find this CTA's range of chunks -------------------------------------
   // The work is the list of chunks over (sequence, head group, CT tokens), in
@@ -652,9 +735,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     meta[4] = (int)cpc;
   }
   __syncthreads();
-  // let the merge kernel (a programmatic dependent launch) get scheduled; it
-  // still waits for this whole grid before reading anything
-  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // let the next kernel get scheduled; it still waits for this whole grid
+  // before reading anything
+  if (tid == 0) grid_dep_launch();
   if (n_chunks == 0) return;
   if (ctrl[0] < 0) {   // cannot happen for a consistent scan; never walk blind
     if (tid == 0) set_error(a.err, PA_DEVERR_SEQ_LEN);
@@ -777,8 +860,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows = a.HG * a.G;
   Walk w = w0;
   int seg_c0 = w.c;
+  const int seg_c0_first = w.c;
   bool first_seg = true;
   uint32_t seg = 0;
+  int merge_i = -1, merge_g = 0;
   const float sl2 = a.scale_log2;
   for (int n = 0; n < n_chunks; ++n) {
     const int st = n % S;
@@ -842,19 +927,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           merge_and_write<D, kBF16>(a, mbuf, w.i, w.g, full, slot_idx);
           asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
         }
-        if (first_seg && seg_c0 > 0 && w.c == w.nc - 1 && tid == 0) {
-          // this CTA finishes a (sequence, head group) begun by earlier CTAs:
-          // the reduce kernel merges its pieces
-          int* meta = a.ws_meta + (size_t)blockIdx.x * 8;
-          meta[1] = w.i;
-          meta[2] = w.g;
-          meta[3] = (int)(start - seg_c0);
-          meta[0] = 1;
+        const bool merger = first_seg && seg_c0 > 0 && w.c == w.nc - 1;
+        if (merger) {
+          // this CTA finishes a (sequence, head group) begun by earlier CTAs
+          merge_i = w.i;
+          merge_g = w.g;
+          if (tid == 0) {
+            int* meta = a.ws_meta + (size_t)blockIdx.x * 8;
+            meta[1] = w.i;
+            meta[2] = w.g;
+            meta[3] = (int)(start - seg_c0);
+            meta[0] = a.fused ? 0 : 1;   // without fusion the reduce kernel merges it
+          }
+        } else if (!full && a.fused) {
+          // a piece some later CTA merges: publish the record once complete
+          asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
+          if (tid == 0) {
+            __threadfence();
+            *reinterpret_cast<volatile uint32_t*>(a.ws_flags + (size_t)blockIdx.x * 2 + slot_idx) = 1u;
+          }
         }
         first_seg = false;
       }
     }
     walk_advance(w, a);
+  }
+  if constexpr (kMode != kModeGather) {
+    if (a.fused && merge_i >= 0)
+      merge_split_in_cta<D, kBF16>(a, merge_i, merge_g, start - seg_c0_first, cpc, abort_flag,
+                                   reinterpret_cast<float*>(gbase + a.ctrl_off + 16 * S +
+                                                            16 * kQBufs + 128 + 32));
   }
 }
 
@@ -878,7 +980,8 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Deco
   __shared__ float s_w[kReduceMaxPieces][RPB];
   __shared__ float s_mx[RPB], s_inv[RPB];
   // wait until the decode grid has finished and its writes are visible
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  grid_dep_wait();
+  grid_dep_launch();
   const int rows = a.HG * a.G;
   const int slices = (rows + RPB - 1) / RPB;
   const int last = blockIdx.x / slices;

@@ -20,7 +20,8 @@ struct DecodePlan {
   int kv_bytes, stage_bytes, q_off, q_bytes, q_stride, merge_off, ctrl_off, smem_bytes;
   int smem_optin;    // the device's per-block shared-memory maximum
   int grid;
-  size_t ws_meta_bytes, ws_rec_bytes;
+  bool fused;        // split contexts merged inside the (cooperative) decode grid
+  size_t ws_meta_bytes, ws_flag_bytes, ws_rec_bytes;
 };
 
 // Per-variant occupancy (CTAs per SM) for a given dynamic shared-memory size.

@@ -68,27 +68,26 @@ template <int D>
 int launch_impl(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
                 const DecodeArgs& a, cudaStream_t s) {
   clear_stale_error();
+  // fused: every CTA must be resident (cooperative launch), since the CTA
+  // holding a context's last piece waits for the earlier pieces' records
   int rc = with_variant<D>(p, [&](auto kern) -> int {
-    kern<<<p.grid, kThreads, p.smem_bytes, s>>>(tk, tv, a);
-    return launch_status(cudaGetLastError(), "decode kernel launch");
+    cudaError_t e = launch_pdl(kern, dim3(p.grid), dim3(kThreads), (size_t)p.smem_bytes, s,
+                               p.fused, tk, tv, a);
+    if (e != cudaSuccess && p.fused) {
+      // a cooperative grid that may not overlap its predecessor
+      clear_stale_error();
+      e = launch_ex(kern, dim3(p.grid), dim3(kThreads), (size_t)p.smem_bytes, s, true, false, tk,
+                    tv, a);
+    }
+    return launch_status(e, "decode kernel launch");
   });
-  if (rc != PA_OK || p.mode == kModeGather || p.grid < 2) return rc;
-  // the merge kernel is launched as a programmatic dependent of the decode
-  // grid: it is scheduled while the decode grid drains and waits on the
-  // grid-dependency barrier before it reads the partial states
-  cudaLaunchConfig_t cfg{};
+  if (rc != PA_OK || p.mode == kModeGather || p.grid < 2 || p.fused) return rc;
   const int rpb = reduce_rows_per_block<D>();
-  cfg.gridDim = dim3(p.grid * ((p.HG * p.G + rpb - 1) / rpb));
-  cfg.blockDim = dim3(kReduceThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = p.bf16 ? cudaLaunchKernelEx(&cfg, split_reduce_kernel<D, true>, a)
-                         : cudaLaunchKernelEx(&cfg, split_reduce_kernel<D, false>, a);
+  const dim3 grid(p.grid * ((p.HG * p.G + rpb - 1) / rpb));
+  cudaError_t e = p.bf16 ? launch_pdl(split_reduce_kernel<D, true>, grid, dim3(kReduceThreads), 0,
+                                      s, false, a)
+                         : launch_pdl(split_reduce_kernel<D, false>, grid,
+                                      dim3(kReduceThreads), 0, s, false, a);
   return launch_status(e, "merge kernel launch");
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -15,6 +17,7 @@ struct DeviceInfo {
   int sm_count;
   int smem_per_sm;      // bytes of shared memory per SM
   int smem_per_block;   // opt-in maximum per block
+  int coop;             // cooperative launches supported
 };
 int current_device_info(DeviceInfo* info);
 
@@ -45,6 +48,40 @@ inline int launch_status(cudaError_t e, const char* where = "kernel launch") {
   if (e == cudaSuccess) return PA_OK;
   note_cuda_error((int)e, where);
   return PA_ERR_CUDA;
+}
+
+// Launches `kern` with programmatic stream serialization allowed (the kernel
+// calls grid_dep_wait before reading inputs) and, if asked, as a cooperative
+// grid.  Returns the launch status.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, bool cooperative, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, bool cooperative, Args&&... args) {
+  return launch_ex(kern, grid, block, smem, s, cooperative, true, std::forward<Args>(args)...);
 }
 
 // Clears an error left by an earlier, already reported runtime call so that

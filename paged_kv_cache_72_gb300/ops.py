@@ -141,7 +141,8 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
         out = torch.empty_like(q)
     if workspace is None:
         nbytes = pa_decode_workspace_size(Hq, H, D, B, _dtype_code(q), flags, num_ctas)
-        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+        # zero-filled once; the decode leaves it ready for the next call
+        workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     _check(L.pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                        block_tables.shape[1], _ptr(seq_lens), N, Hq, H, D, B, nb,
                        _dtype_code(q), float(scale), _ptr(out), _ptr(workspace),
