@@ -2,7 +2,7 @@
 
 A step is one pass of the hot path over one batch: copy-on-write block copies
 (shared-prefix workload only), slot mapping, cache write of the step's new
-K/V, and paged decode attention (partition kernel + split reduce).  The
+K/V, and paged decode attention (one kernel; split contexts merged in-grid).  The
 default workload is the Llama-3-8B GQA decode layer (256 sequences, lognormal
 lengths with mean about 400, 32 q heads / 8 KV heads, head_dim 128, bf16,
 16-token blocks, 40,000-block pool).
@@ -203,8 +203,8 @@ class Step:
         self.decode_ms = []
 
     def launches_per_step(self):
-        # copy-on-write (if any), slot mapping, cache write, decode (the split
-        # merge runs inside the decode grid when it is cooperative)
+        # copy-on-write (if any), slot mapping, cache write, decode (split
+        # contexts are merged inside the decode grid)
         return (1 if self.pairs.numel() else 0) + 2 + 1
 
     def write_phase(self):
@@ -338,7 +338,7 @@ def run_gpu(args, rank, world, local_rank):
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s",
-            "kernel": "pa_decode: paged_decode_kernel + split_reduce_kernel",
+            "kernel": "pa_decode: paged_decode_kernel",
             "algorithmic_bytes_per_launch": nbytes["decode"],
             "frac_of_datasheet_7.9TBps": round(achieved / DATASHEET_HBM_GBS, 4),
         },

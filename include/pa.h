@@ -119,10 +119,15 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
 
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
- * this shape on the current device (partial softmax states of contexts split
- * across thread blocks, plus per-block bookkeeping).  num_ctas = 0 selects
- * the default grid (a multiple of the SM count); flags as for pa_decode.
+ * this shape on the current device: a fixed region of PA_DECODE_MAX_CTAS
+ * 32-bit piece counters, then the partial softmax states of contexts split
+ * across thread blocks (two per block of the grid).  Because the counters sit
+ * at the same place whatever the shape or grid, one workspace sized for the
+ * largest call serves calls of any shape and num_ctas.  num_ctas = 0 selects
+ * the default grid (a multiple of the SM count); larger than
+ * PA_DECODE_MAX_CTAS returns PA_ERR_INVALID_ARG; flags as for pa_decode.
  */
+#define PA_DECODE_MAX_CTAS 16384
 int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                              int32_t block_size, int32_t dtype, int32_t flags, int32_t num_ctas,
                              size_t* bytes);
@@ -141,17 +146,17 @@ int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t 
  *   out        [num_seqs][num_q_heads][head_dim], dtype; must not alias q
  *   scale      multiplies q.k (e.g. 1/sqrt(head_dim))
  *   workspace  device buffer of at least pa_decode_workspace_size() bytes,
- *              zero-filled before its first use; every call that completes
- *              without a device error leaves it ready for the next call (zero it
- *              again after a PA_DEVERR_TIMEOUT).  Calls sharing one workspace
- *              must not overlap on the GPU.
+ *              zero-filled before its first use; every call that runs to its
+ *              end (device errors included) leaves it zero-ready for the next
+ *              call.  Calls sharing one workspace must not overlap on the GPU.
  * Query head hq reads KV head hq / G (contiguous query groups).  Accumulation
  * is fp32; the output is rounded once to dtype.  The result does not depend on
  * where the blocks sit in the pool.  The work (chunks of one block's worth of
- * tokens of up to 8 KV heads) is split evenly over a persistent grid; a context
- * split between thread blocks is merged by the block holding its last piece
- * (cooperative launch), or by a second kernel when the grid is larger than
- * the GPU can hold at once.
+ * tokens of up to 8 KV heads) is split evenly over a persistent grid; each
+ * piece of a context split between thread blocks leaves its partial softmax
+ * state in the workspace and counts itself, and the block whose piece
+ * completes the count merges them (one kernel launch, no block waits for
+ * another, any num_ctas).
  * flags: PA_DECODE_AUTO, PA_DECODE_SIMT or PA_DECODE_MMA; num_ctas: 0 = default.
  */
 int pa_decode(const void* q, const void* k_cache, const void* v_cache,

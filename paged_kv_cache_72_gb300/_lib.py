@@ -26,6 +26,7 @@ PA_DECODE_AUTO = 0
 PA_DECODE_SIMT = 1
 PA_DECODE_MMA = 2
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
+PA_DECODE_MAX_CTAS = 16384
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32

@@ -26,7 +26,6 @@ int current_device_info(DeviceInfo* info) {
     cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (!e) e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     if (!e) e = cudaDeviceGetAttribute(&d.smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (!e) e = cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev);
     if (e) return launch_status(e, "cudaDeviceGetAttribute");
     g_info[dev] = d;
     g_have[dev] = true;

@@ -123,7 +123,7 @@ int pa_slot_mapping(const int32_t* block_tables, int32_t table_stride, int32_t n
   if (blocks > (long long)di.sm_count * 16) blocks = (long long)di.sm_count * 16;
   clear_stale_error();
   return launch_status(launch_pdl(slot_mapping_kernel, dim3((unsigned)blocks), dim3(threads), 0,
-                                  static_cast<cudaStream_t>(stream), false, block_tables,
+                                  static_cast<cudaStream_t>(stream), block_tables,
                                   (int)table_stride, (int)num_seqs, token_seq, token_pos,
                                   (long long)num_tokens, ilog2(block_size), (long long)num_blocks,
                                   slot_mapping, err_word),
@@ -145,7 +145,7 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, in
   const int threads = vecs >= 256 ? 256 : (vecs >= 128 ? 128 : 64);
   clear_stale_error();
   return launch_status(launch_pdl(cache_write_kernel, dim3((unsigned)num_tokens), dim3(threads), 0,
-                                  static_cast<cudaStream_t>(stream), false,
+                                  static_cast<cudaStream_t>(stream),
                                   static_cast<const uint4*>(k), static_cast<const uint4*>(v),
                                   slot_mapping, vecs, num_blocks * (long long)block_size,
                                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
@@ -167,7 +167,7 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
   dim3 grid((unsigned)num_pairs, 2);
   clear_stale_error();
   return launch_status(launch_pdl(copy_blocks_kernel, grid, dim3(256), 0,
-                                  static_cast<cudaStream_t>(stream), false, src_dst_pairs,
+                                  static_cast<cudaStream_t>(stream), src_dst_pairs,
                                   (int)num_pairs, (long long)num_blocks, (int)vecs,
                                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                   err_word),

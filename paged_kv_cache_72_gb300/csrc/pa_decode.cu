@@ -14,13 +14,16 @@ namespace {
 
 constexpr int kMaxStages = 8;
 
-// mbarriers (16 B per stage, 16 B per query buffer), scan scratch (128 B),
-// control words (32 B), merge row scratch (130 floats, rounded)
-int ctrl_bytes(int stages) { return 16 * stages + 16 * kQBufs + 128 + 32 + 528; }
+// mbarriers (16 B per stage, 16 B per query buffer), scan scratch, control
+// words, merge row scratch
+int ctrl_bytes(int stages) {
+  return 16 * stages + 16 * kQBufs + kScanBytes + kCtrlBytes + kRowScratchBytes;
+}
 
 int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas, bool gather,
               DecodePlan* p) {
-  if (Hq <= 0 || Hkv <= 0 || num_ctas < 0) return PA_ERR_INVALID_ARG;
+  if (Hq <= 0 || Hkv <= 0 || num_ctas < 0 || num_ctas > PA_DECODE_MAX_CTAS)
+    return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
   if (!is_pow2(B) || B < 2 || B > 256) return PA_ERR_UNSUPPORTED;
@@ -86,10 +89,10 @@ int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas,
   if (rc != PA_OK) return rc;
   if (per_sm < 1) return PA_ERR_UNSUPPORTED;
   q.grid = num_ctas > 0 ? num_ctas : di.sm_count * per_sm;
-  // merging split contexts inside the grid needs every CTA resident at once
-  q.fused = !gather && di.coop && q.grid <= di.sm_count * per_sm;
-  q.ws_meta_bytes = gather ? 0 : (((size_t)q.grid * 8 * sizeof(int) + 255) / 256) * 256;
-  q.ws_flag_bytes = gather ? 0 : (((size_t)q.grid * 2 * sizeof(uint32_t) + 255) / 256) * 256;
+  if (q.grid > PA_DECODE_MAX_CTAS) return PA_ERR_INVALID_ARG;
+  // the counters' place must not depend on the grid: a call with a small grid
+  // would otherwise leave records where a larger grid expects zero counters
+  q.ws_count_bytes = gather ? 0 : (size_t)PA_DECODE_MAX_CTAS * sizeof(uint32_t);
   q.ws_rec_bytes = gather ? 0 : (size_t)q.grid * 2 * rec_floats(q.HG * G, D) * sizeof(float);
   *p = q;
   return PA_OK;
@@ -286,7 +289,7 @@ int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t 
   if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
                            false, &p))
     return rc;
-  *bytes = p.ws_meta_bytes + p.ws_flag_bytes + p.ws_rec_bytes;
+  *bytes = p.ws_count_bytes + p.ws_rec_bytes;
   return PA_OK;
 }
 
@@ -308,7 +311,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(workspace))
     return PA_ERR_INVALID_ARG;
-  if (workspace_bytes < p.ws_meta_bytes + p.ws_flag_bytes + p.ws_rec_bytes) return PA_ERR_WORKSPACE;
+  if (workspace_bytes < p.ws_count_bytes + p.ws_rec_bytes) return PA_ERR_WORKSPACE;
   CUtensorMap tk, tv;
   if (int rc = encode_maps(&tk, &tv, k_cache, v_cache, &p, num_kv_heads, num_blocks)) return rc;
   DecodeArgs a{};
@@ -316,11 +319,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   a.out = static_cast<uint16_t*>(out);
   a.bt = block_tables;
   a.seq_lens = seq_lens;
-  a.ws_meta = static_cast<int*>(workspace);
-  a.ws_flags = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + p.ws_meta_bytes);
-  a.ws_rec = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ws_meta_bytes +
-                                      p.ws_flag_bytes);
-  a.fused = p.fused ? 1 : 0;
+  a.ws_count = static_cast<uint32_t*>(workspace);
+  a.ws_rec = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ws_count_bytes);
   a.err = err_word;
   a.num_blocks = num_blocks;
   a.num_seqs = num_seqs;

@@ -15,7 +15,9 @@
 //  * The work is the list of chunks (sequence, head group, CT tokens), cut into
 //    equal contiguous ranges, one per CTA (grid = the SM count).  Every CTA
 //    scans seq_lens once to find its range; a context may be split across
-//    CTAs, whose partial softmax states (m, l, o) a second kernel merges.  The
+//    CTAs.  Each piece leaves its partial softmax state (m, l, o) in the
+//    workspace and counts itself on the context's counter; the piece that
+//    completes the count merges them, so no CTA ever waits for another.  The
 //    split depends only on seq_lens, so the result does not depend on where the
 //    blocks sit.
 //  * One producer warp reads the block table one chunk ahead and streams each
@@ -46,6 +48,14 @@ constexpr int kCWarps = 8;         // consumer warps; stage = kCWarps * 16 token
 constexpr int kProducerWarp = kCWarps;
 constexpr int kThreads = (kCWarps + 1) * 32;
 constexpr int kQBufs = 2;          // query-row buffers in flight
+// Shared-memory control area after the mbarriers: scan scratch, control words
+// (walk start, abort flag, merges this CTA owes), merge row scratch.
+constexpr int kScanBytes = 128;
+constexpr int kCtrlBytes = 64;
+constexpr int kRowScratchBytes = 512;
+constexpr int kCtrlMerges = 5;     // ctrl[5] = pending merges, then 4 ints per merge
+// counter bit set by a piece whose CTA gave up: the context is left unmerged
+constexpr uint32_t kPieceAborted = 0x80000000u;
 
 enum Mode : int { kModeSimt = 0, kModeMma = 1, kModeGather = 2 };
 
@@ -55,9 +65,9 @@ struct DecodeArgs {
   const int32_t* bt;         // [N][stride]
   const int32_t* seq_lens;   // [N]
   float* ws_rec;             // [grid][2] records of rec_floats(HG*G, D): o[][D], m[], l[]
-  int* ws_meta;              // [grid][8]: needs merge, i, head group, segment start, cpc
-  uint32_t* ws_flags;        // [grid][2]: record published (1) / consumed (0); zero between calls
-  int fused;                 // 1: the CTA holding a context's last piece merges it (cooperative grid)
+  uint32_t* ws_count;        // [PA_DECODE_MAX_CTAS]: pieces of the split context ending in
+                             // CTA k that have arrived; zero between calls (the last
+                             // arriver resets it)
   int32_t* err;
   const int64_t* out_off;    // gather: first output row of each sequence
   uint16_t* k_out;           // gather outputs [rows][H_kv][D]
@@ -564,59 +574,58 @@ __device__ __forceinline__ void gather_tile(const DecodeArgs& a, uint32_t kpart,
 }
 
 // ---------------------------------------------------------------------------
-// In-kernel merge of a split context (cooperative grid): the CTA that holds a
-// (sequence, head group)'s last piece waits for the earlier CTAs' published
-// records, takes them (resetting their flags for the next call) and writes
-// out = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k.  Its own piece is its
-// record in slot 0.  s_row: 130 floats of shared memory.
+// Merge of a context split across CTAs, run by the CTA whose piece arrived
+// last.  The context's chunks start at global chunk index g0 and number nc,
+// so its pieces sit in CTAs first = g0 / cpc .. last = (g0 + nc - 1) / cpc,
+// each in record slot 0 except the first CTA's when the context began after
+// that CTA's own first chunk (then it is that CTA's second segment, slot 1):
+//   out = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k.
+// Pass 1: tpr threads per row fold the pieces' (m, l) pairs online and
+// combine by shuffles; pass 2: four head_dim columns per thread, weights
+// 2^(m_k - m*) recomputed next to each o_k load.  s_row: 128 floats of shared
+// memory.  Consumer threads only; the records come from other CTAs, so they
+// are read from L2 (ld.global.cg).
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16>
-__device__ __forceinline__ void merge_split_in_cta(const DecodeArgs& a, int i, int grp,
-                                                   long long gstart, long long cpc,
-                                                   volatile int* abort_flag, float* s_row) {
+__device__ __forceinline__ void merge_split(const DecodeArgs& a, int i, int grp, long long g0,
+                                            int nc, long long cpc, float* s_row) {
   const int tid = threadIdx.x;   // consumer threads 0 .. kCWarps * 32 - 1
   const int nthr = kCWarps * 32;
-  const int last = blockIdx.x;
-  const int first = (int)(gstart / cpc);
+  const int first = (int)(g0 / cpc);
+  const int last = (int)((g0 + nc - 1) / cpc);
   const int rows = a.HG * a.G;
   const size_t rf = rec_floats(rows, D);
-  const size_t ml = (size_t)rows * D;
-  auto slot_of = [&](int k) -> int {
-    return (k == first && gstart != (long long)first * cpc) ? 1 : 0;
-  };
-  volatile float* const s_ok = s_row + 128;
-  if (tid == 0) {
-    bool ok = !*abort_flag;
-    for (int k = first; k < last && ok; ++k) {
-      volatile uint32_t* f = a.ws_flags + (size_t)k * 2 + slot_of(k);
-      const long long t0 = clock64();
-      while (*f == 0u) {
-        if (*abort_flag || clock64() - t0 > kWaitLimitCycles) { ok = false; break; }
-      }
-      if (ok) *f = 0u;   // taken: clear for the next call
-    }
-    if (!ok) {
-      set_error(a.err, PA_DEVERR_TIMEOUT);
-      *abort_flag = 1;
-    }
-    *s_ok = ok ? 1.f : 0.f;
-    __threadfence();
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
-  if (*s_ok == 0.f) return;   // the same decision in every consumer thread
+  const size_t ml = (size_t)rows * D;   // m[] then l[] follow o[][]
   auto rec_of = [&](int k) -> const float* {
-    return a.ws_rec + ((size_t)k * 2 + slot_of(k)) * rf;
+    const int slot = (k == first && g0 != (long long)first * cpc) ? 1 : 0;
+    return a.ws_rec + ((size_t)k * 2 + slot) * rf;
   };
-  for (int r = tid; r < rows; r += nthr) {
-    float mx = -INFINITY;
-    for (int k = first; k <= last; ++k) mx = fmaxf(mx, __ldcg(rec_of(k) + ml + r));
-    float L = 0.f;
-    for (int k = first; k <= last; ++k) {
-      const float* rec = rec_of(k);
-      L = fmaf(exp2f(__ldcg(rec + ml + r) - mx), __ldcg(rec + ml + rows + r), L);
+  int tpr = 32;   // threads per row: a power of two, tpr * rows <= nthr
+  while (tpr * rows > nthr) tpr >>= 1;
+  if (tid < ((tpr * rows + 31) & ~31)) {   // whole warps, so that shuffles see every lane
+    const int r = tid / tpr, j = tid % tpr;
+    float m = -INFINITY, l = 0.f;
+    if (r < rows) {
+      for (int k = first + j; k <= last; k += tpr) {
+        const float* rec = rec_of(k);
+        const float mk = __ldcg(rec + ml + r), lk = __ldcg(rec + ml + rows + r);
+        const float mn = fmaxf(m, mk);
+        l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + lk * exp2f(mk - mn);
+        m = mn;
+      }
     }
-    s_row[r] = mx;
-    s_row[64 + r] = 1.f / L;
+    for (int o = 1; o < tpr; o <<= 1) {
+      const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+      const float lo = __shfl_xor_sync(0xffffffffu, l, o);
+      const float mn = fmaxf(m, mo);
+      if (mn != -INFINITY)
+        l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + (mo == -INFINITY ? 0.f : lo * exp2f(mo - mn));
+      m = mn;
+    }
+    if (r < rows && j == 0) {
+      s_row[r] = m;
+      s_row[64 + r] = 1.f / l;
+    }
   }
   asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
   for (int e = tid; e < rows * (D / 4); e += nthr) {
@@ -640,6 +649,7 @@ __device__ __forceinline__ void merge_split_in_cta(const DecodeArgs& a, int i, i
     pk.y = pack2<kBF16>(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2*>(dst) = pk;
   }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");   // s_row is reused by the next merge
 }
 
 // ---------------------------------------------------------------------------
@@ -663,8 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_qempty = bar_qfull + 8 * kQBufs;
   const int ctrl_words = a.ctrl_off + 16 * S + 16 * kQBufs;
   long long* const scan_tmp = reinterpret_cast<long long*>(gbase + ctrl_words);
-  int* const ctrl = reinterpret_cast<int*>(gbase + ctrl_words + 8 * 16);
+  int* const ctrl = reinterpret_cast<int*>(gbase + ctrl_words + kScanBytes);
   volatile int* const abort_flag = ctrl + 4;
+  float* const s_row = reinterpret_cast<float*>(gbase + ctrl_words + kScanBytes + kCtrlBytes);
 
   if (tid == 0) {
     ctrl[0] = -1;
@@ -677,11 +688,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_qempty + 8 * s, kCWarps);
     }
     *abort_flag = 0;
+    ctrl[kCtrlMerges] = 0;
     fence_barrier_init();
   }
   if (warp == kProducerWarp && lane == 0) {
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
+  }
+  // Warm L2 with the small inputs (lengths, block tables, queries) while the
+  // previous kernel in the stream drains: a prefetch returns no data, so it
+  // is harmless even if that kernel is still writing them.
+  {
+    const size_t step = (size_t)gridDim.x * blockDim.x * 128;
+    const size_t t0 = ((size_t)blockIdx.x * blockDim.x + tid) * 128;
+    const char* sl = reinterpret_cast<const char*>(a.seq_lens);
+    const char* bt = reinterpret_cast<const char*>(a.bt);
+    const size_t sl_bytes = (size_t)a.num_seqs * 4, bt_bytes = sl_bytes * a.stride;
+    for (size_t o = t0; o < sl_bytes; o += step) prefetch_l2(sl + o);
+    for (size_t o = t0; o < bt_bytes; o += step) prefetch_l2(bt + o);
+    if (kMode != kModeGather) {
+      const char* qp = reinterpret_cast<const char*>(a.q);
+      const size_t q_bytes = (size_t)a.num_seqs * a.Hq * D * 2;
+      for (size_t o = t0; o < q_bytes; o += step) prefetch_l2(qp + o);
+    }
   }
   // inputs may come from the previous kernel in the stream
   grid_dep_wait();
@@ -728,11 +757,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       off += span;
     }
-  }
-  if (kMode != kModeGather && tid == 0) {
-    int* meta = a.ws_meta + (size_t)blockIdx.x * 8;
-    meta[0] = 0;
-    meta[4] = (int)cpc;
   }
   __syncthreads();
   // let the next kernel get scheduled; it still waits for this whole grid
@@ -860,10 +884,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows = a.HG * a.G;
   Walk w = w0;
   int seg_c0 = w.c;
-  const int seg_c0_first = w.c;
   bool first_seg = true;
   uint32_t seg = 0;
-  int merge_i = -1, merge_g = 0;
   const float sl2 = a.scale_log2;
   for (int n = 0; n < n_chunks; ++n) {
     const int st = n % S;
@@ -927,24 +949,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           merge_and_write<D, kBF16>(a, mbuf, w.i, w.g, full, slot_idx);
           asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
         }
-        const bool merger = first_seg && seg_c0 > 0 && w.c == w.nc - 1;
-        if (merger) {
-          // this CTA finishes a (sequence, head group) begun by earlier CTAs
-          merge_i = w.i;
-          merge_g = w.g;
-          if (tid == 0) {
-            int* meta = a.ws_meta + (size_t)blockIdx.x * 8;
-            meta[1] = w.i;
-            meta[2] = w.g;
-            meta[3] = (int)(start - seg_c0);
-            meta[0] = a.fused ? 0 : 1;   // without fusion the reduce kernel merges it
-          }
-        } else if (!full && a.fused) {
-          // a piece some later CTA merges: publish the record once complete
+        if (!full) {
+          // a piece of a context split across CTAs: once its record is
+          // complete, count it on the counter of the context's last CTA; the
+          // piece that completes the count owes the merge
           asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
           if (tid == 0) {
-            __threadfence();
-            *reinterpret_cast<volatile uint32_t*>(a.ws_flags + (size_t)blockIdx.x * 2 + slot_idx) = 1u;
+            const long long g0 = start + n - w.c;   // global index of the context's chunk 0
+            const int first = (int)(g0 / cpc), last = (int)((g0 + w.nc - 1) / cpc);
+            uint32_t* cnt = a.ws_count + last;
+            __threadfence();   // release this CTA's record
+            if (*abort_flag) atomicOr(cnt, kPieceAborted);
+            const uint32_t now = atomicAdd(cnt, 1u) + 1u;
+            if ((now & ~kPieceAborted) == (uint32_t)(last - first + 1)) {
+              *cnt = 0u;         // every piece is in: ready for the next call
+              __threadfence();   // acquire the other pieces' records
+              if (!(now & kPieceAborted)) {
+                int* pm = ctrl + kCtrlMerges;
+                const int k = pm[0]++;
+                pm[1 + 4 * k] = w.i;
+                pm[2 + 4 * k] = w.g;
+                pm[3 + 4 * k] = (int)(g0 - start);
+                pm[4 + 4 * k] = w.nc;
+              }
+            }
           }
         }
         first_seg = false;
@@ -953,88 +981,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     walk_advance(w, a);
   }
   if constexpr (kMode != kModeGather) {
-    if (a.fused && merge_i >= 0)
-      merge_split_in_cta<D, kBF16>(a, merge_i, merge_g, start - seg_c0_first, cpc, abort_flag,
-                                   reinterpret_cast<float*>(gbase + a.ctrl_off + 16 * S +
-                                                            16 * kQBufs + 128 + 32));
+    // the merges this CTA owes (at most two: its first and its last segment
+    // are the only ones that can be pieces); a CTA that gave up merges nothing.
+    // Thread 0 decides for all, so that every thread takes the same barriers.
+    if (tid == 0 && *abort_flag) ctrl[kCtrlMerges] = 0;
+    asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
+    const int* pm = ctrl + kCtrlMerges;
+    const int owed = pm[0];
+    for (int k = 0; k < owed; ++k)
+      merge_split<D, kBF16>(a, pm[1 + 4 * k], pm[2 + 4 * k], start + pm[3 + 4 * k],
+                            pm[4 + 4 * k], cpc, s_row);
   }
-}
-
-// ---------------------------------------------------------------------------
-// Merge of split contexts.  Block b works for decode CTA b / slices on the
-// rows [slice * RPB, slice * RPB + RPB) of the (sequence, head group) that
-// CTA finished, when earlier CTAs held pieces of it:
-//   out = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k.
-// First the per-row weights (shared memory), then the weighted sum over the
-// pieces, four head_dim columns per thread, one pass.
-// ---------------------------------------------------------------------------
-constexpr int kReduceThreads = 256;
-constexpr int kReduceMaxPieces = 32;   // pieces whose weights are kept in shared memory
-
-template <int D>
-__host__ __device__ constexpr int reduce_rows_per_block() { return kReduceThreads / (D / 4); }
-
-template <int D, bool kBF16>
-__global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const DecodeArgs a) {
-  constexpr int RPB = reduce_rows_per_block<D>();
-  __shared__ float s_w[kReduceMaxPieces][RPB];
-  __shared__ float s_mx[RPB], s_inv[RPB];
-  // wait until the decode grid has finished and its writes are visible
-  grid_dep_wait();
-  grid_dep_launch();
-  const int rows = a.HG * a.G;
-  const int slices = (rows + RPB - 1) / RPB;
-  const int last = blockIdx.x / slices;
-  const int r0 = (blockIdx.x % slices) * RPB;
-  const int* meta = a.ws_meta + (size_t)last * 8;
-  if (meta[0] == 0) return;
-  const int i = meta[1], grp = meta[2];
-  const long long gstart = meta[3];
-  const long long cpc = meta[4];
-  const int first = (int)(gstart / cpc);
-  const size_t rf = rec_floats(rows, D);
-  const size_t ml = (size_t)rows * D;   // m[] then l[] follow o[][]
-  auto rec_of = [&](int k) -> const float* {
-    const int slot = (k == first && gstart != (long long)first * cpc) ? 1 : 0;
-    return a.ws_rec + ((size_t)k * 2 + slot) * rf;
-  };
-  // per row: m* = max_k m_k, L = sum_k 2^(m_k - m*) l_k, and the weights
-  if (threadIdx.x < RPB && r0 + threadIdx.x < rows) {
-    const int r = r0 + threadIdx.x;
-    float mx = -INFINITY;
-    for (int k = first; k <= last; ++k) mx = fmaxf(mx, rec_of(k)[ml + r]);
-    float L = 0.f;
-    for (int k = first; k <= last; ++k) {
-      const float* rec = rec_of(k);
-      const float wt = exp2f(rec[ml + r] - mx);
-      if (k - first < kReduceMaxPieces) s_w[k - first][threadIdx.x] = wt;
-      L = fmaf(wt, rec[ml + rows + r], L);
-    }
-    s_mx[threadIdx.x] = mx;
-    s_inv[threadIdx.x] = 1.f / L;
-  }
-  __syncthreads();
-  const int rr = threadIdx.x / (D / 4);
-  const int r = r0 + rr;
-  if (r >= rows) return;
-  const int d = 4 * (threadIdx.x % (D / 4));
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = first; k <= last; ++k) {
-    const float* rec = rec_of(k);
-    const float wt = (k - first < kReduceMaxPieces) ? s_w[k - first][rr]
-                                                   : exp2f(rec[ml + r] - s_mx[rr]);
-    const float4 ov = *reinterpret_cast<const float4*>(rec + (size_t)r * D + d);
-    acc.x = fmaf(wt, ov.x, acc.x);
-    acc.y = fmaf(wt, ov.y, acc.y);
-    acc.z = fmaf(wt, ov.z, acc.z);
-    acc.w = fmaf(wt, ov.w, acc.w);
-  }
-  const float inv = s_inv[rr];
-  uint16_t* dst = a.out + ((size_t)i * a.Hq + (size_t)grp * rows + r) * D + d;
-  uint2 pk;
-  pk.x = pack2<kBF16>(acc.x * inv, acc.y * inv);
-  pk.y = pack2<kBF16>(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(dst) = pk;
 }
 
 }  // namespace pa

@@ -20,14 +20,13 @@ struct DecodePlan {
   int kv_bytes, stage_bytes, q_off, q_bytes, q_stride, merge_off, ctrl_off, smem_bytes;
   int smem_optin;    // the device's per-block shared-memory maximum
   int grid;
-  bool fused;        // split contexts merged inside the (cooperative) decode grid
-  size_t ws_meta_bytes, ws_flag_bytes, ws_rec_bytes;
+  size_t ws_count_bytes, ws_rec_bytes;   // workspace: per-CTA piece counters, then records
 };
 
 // Per-variant occupancy (CTAs per SM) for a given dynamic shared-memory size.
 int decode_ctas_per_sm(const DecodePlan& p, int* ctas);
 
-// Launches the decode (or gather) kernel and, for decode, the split reduce.
+// Launches the decode (or gather) kernel.
 int decode_launch(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
                   const DecodeArgs& a, cudaStream_t s);
 

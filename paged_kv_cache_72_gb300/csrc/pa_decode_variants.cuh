@@ -68,27 +68,12 @@ template <int D>
 int launch_impl(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
                 const DecodeArgs& a, cudaStream_t s) {
   clear_stale_error();
-  // fused: every CTA must be resident (cooperative launch), since the CTA
-  // holding a context's last piece waits for the earlier pieces' records
-  int rc = with_variant<D>(p, [&](auto kern) -> int {
-    cudaError_t e = launch_pdl(kern, dim3(p.grid), dim3(kThreads), (size_t)p.smem_bytes, s,
-                               p.fused, tk, tv, a);
-    if (e != cudaSuccess && p.fused) {
-      // a cooperative grid that may not overlap its predecessor
-      clear_stale_error();
-      e = launch_ex(kern, dim3(p.grid), dim3(kThreads), (size_t)p.smem_bytes, s, true, false, tk,
-                    tv, a);
-    }
+  // no CTA waits for another, so any grid size runs as an ordinary launch
+  return with_variant<D>(p, [&](auto kern) -> int {
+    const cudaError_t e =
+        launch_pdl(kern, dim3(p.grid), dim3(kThreads), (size_t)p.smem_bytes, s, tk, tv, a);
     return launch_status(e, "decode kernel launch");
   });
-  if (rc != PA_OK || p.mode == kModeGather || p.grid < 2 || p.fused) return rc;
-  const int rpb = reduce_rows_per_block<D>();
-  const dim3 grid(p.grid * ((p.HG * p.G + rpb - 1) / rpb));
-  cudaError_t e = p.bf16 ? launch_pdl(split_reduce_kernel<D, true>, grid, dim3(kReduceThreads), 0,
-                                      s, false, a)
-                         : launch_pdl(split_reduce_kernel<D, false>, grid,
-                                      dim3(kReduceThreads), 0, s, false, a);
-  return launch_status(e, "merge kernel launch");
 }
 
 }  // namespace pa

@@ -17,7 +17,6 @@ struct DeviceInfo {
   int sm_count;
   int smem_per_sm;      // bytes of shared memory per SM
   int smem_per_block;   // opt-in maximum per block
-  int coop;             // cooperative launches supported
 };
 int current_device_info(DeviceInfo* info);
 
@@ -50,38 +49,23 @@ inline int launch_status(cudaError_t e, const char* where = "kernel launch") {
   return PA_ERR_CUDA;
 }
 
-// Launches `kern` with programmatic stream serialization allowed (the kernel
-// calls grid_dep_wait before reading inputs) and, if asked, as a cooperative
-// grid.  Returns the launch status.
+// Launches `kern` with programmatic stream serialization allowed: the kernel
+// may start while its predecessor in the stream drains, and calls
+// grid_dep_wait before reading any input.  Returns the launch status.
 template <class... KArgs, class... Args>
-inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t s, bool cooperative, bool pdl, Args&&... args) {
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  int n = 0;
-  if (pdl) {
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-  }
-  if (cooperative) {
-    attr[n].id = cudaLaunchAttributeCooperative;
-    attr[n].val.cooperative = 1;
-    ++n;
-  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = n;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
-template <class... KArgs, class... Args>
-inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                              cudaStream_t s, bool cooperative, Args&&... args) {
-  return launch_ex(kern, grid, block, smem, s, cooperative, true, std::forward<Args>(args)...);
 }
 
 // Clears an error left by an earlier, already reported runtime call so that

@@ -24,6 +24,18 @@ def _declared():
     return out
 
 
+def test_binding_constants_match_the_header():
+    # every value #define in the header has the same value in the binding
+    text = open(HEADER).read()
+    found = 0
+    for name, val in re.findall(r"^#define[ \t]+(PA_\w+)[ \t]+(\S.*?)[ \t]*(?:/\*.*)?$", text, flags=re.M):
+        expr = val.replace("u", "")
+        assert hasattr(_lib, name), name
+        assert getattr(_lib, name) == eval(expr, {}), (name, val)
+        found += 1
+    assert found >= 19
+
+
 @pytest.fixture(scope="module")
 def lib():
     build()
@@ -61,6 +73,9 @@ def test_host_checks_need_no_device(lib):
     assert lib.pa_decode_workspace_size(6, 4, 128, 16, 0, 0, 0, ctypes.byref(n)) == 1
     assert lib.pa_decode_workspace_size(8, 8, 128, 16, 7, 0, 0, ctypes.byref(n)) == 2
     assert lib.pa_decode_workspace_size(8, 8, 128, 16, 0, 0, 0, None) == 1
+    # a grid beyond the fixed counter region is refused
+    assert lib.pa_decode_workspace_size(8, 8, 128, 16, 0, 0, _lib.PA_DECODE_MAX_CTAS + 1,
+                                        ctypes.byref(n)) == 1
     # empty batches are no-ops
     assert lib.pa_cache_write(None, None, None, 0, None, None, 10, 16, 8, 128, 0, None, None) == 0
     assert lib.pa_copy_blocks(None, 0, None, None, 10, 16, 8, 128, 0, None, None) == 0

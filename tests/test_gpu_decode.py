@@ -65,13 +65,41 @@ def test_parity_sweep(cuda_device, dtype, Hq, Hkv, D, B):
 
 @pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 50, 1000])
 def test_split_contexts_across_blocks(cuda_device, num_ctas):
-    # few blocks: long ranges spanning many sequences; many blocks: every
-    # context split into one-chunk pieces merged by the reduce kernel
+    # few blocks: long ranges spanning many sequences; many blocks (more than
+    # the GPU holds at once): contexts split into one-chunk pieces, each merged
+    # by whichever block's piece arrives last
     lens = [3000, 1, 64, 65, 900, 2048, 5, 4096]
     wl = W.random_workload(77, W.BF16, 16, 4, 128, 16, lens, kv_sigma=0.5)
     _parity(wl, num_ctas=num_ctas)
     wl1 = W.random_workload(78, W.F16, 4, 4, 128, 16, lens)
     _parity(wl1, num_ctas=num_ctas)
+
+
+def test_one_workspace_across_calls_that_split_differently(cuda_device):
+    # the split-merge counters live in the workspace and every call must leave
+    # them at zero: one workspace serves calls whose contexts split at other
+    # places (grid sizes from 1 to more than the GPU holds, other lengths)
+    lens = [3000, 1, 64, 65, 900, 2048, 5, 4096]
+    wl = W.random_workload(21, W.BF16, 16, 4, 128, 16, lens, kv_sigma=0.5)
+    st = GpuState(wl)
+    gpu_step(st, decode=False)
+    ref = OracleState(wl)
+    ref.step()
+    full = ref.decode()
+    short = np.array([1500, 1, 33, 65, 17, 2048, 5, 999], np.int32)
+    exp_short = oracle.paged_decode(wl.q, ref.k_cache, ref.v_cache, wl.dtype, wl.block_tables,
+                                    short, wl.scale)
+    sl_short = torch.from_numpy(short).cuda()
+    sizes = [0, 7, 1000, 3, 152, 50, 1, 0]
+    nbytes = max(pa.pa_decode_workspace_size(16, 4, 128, 16, torch.bfloat16, num_ctas=n)
+                 for n in sizes)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for k, n in enumerate(sizes):
+        sl, expected = (st.seq_lens, full) if k % 2 == 0 else (sl_short, exp_short)
+        out = pa.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, sl, wl.scale,
+                           workspace=ws, num_ctas=n, err=st.err)
+        assert_close(gpu_out_f64(out), expected, "call %d, ctas=%d" % (k, n))
+    assert pa.pa_get_error(st.err) == 0
 
 
 def test_placement_does_not_change_bits(cuda_device):
