@@ -71,6 +71,26 @@ def lib():
         L.or_paged_decode.restype = ctypes.c_int
         L.or_contiguous_decode.argtypes = [f64p, f64p, f64p, ctypes.c_int64, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_double, f64p]
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        L.or_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.or_e4m3_to_f64.restype = ctypes.c_double
+        L.or_e4m3_from_f32.argtypes = [ctypes.c_float]
+        L.or_e4m3_from_f32.restype = ctypes.c_uint8
+        L.or_e4m3_encode_array.argtypes = [f32p, ctypes.c_int64, u8p]
+        L.or_e4m3_decode_array.argtypes = [u8p, ctypes.c_int64, f64p]
+        L.or_cache_write_fp8.argtypes = [u8p, u8p, u16p, u16p, ctypes.c_int, i64p,
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                         ctypes.c_float]
+        L.or_gather_head_fp8.argtypes = [u8p, ctypes.c_double, i32p, ctypes.c_int64,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, f64p]
+        L.or_paged_decode_fp8.argtypes = [u16p, u8p, u8p, ctypes.c_int, ctypes.c_double,
+                                          ctypes.c_double, i32p, ctypes.c_int64, i32p, i32p,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_double, f64p,
+                                          ctypes.c_int]
+        L.or_paged_decode_fp8.restype = ctypes.c_int
         L.or_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -148,8 +168,14 @@ def cache_write(k_cache, v_cache, k, v, slots):
 
 
 def copy_blocks(k_cache, v_cache, pairs):
-    """In place: block dst <- block src for each (src, dst) pair, K and V."""
+    """In place: block dst <- block src for each (src, dst) pair, K and V.
+
+    Pools of 16-bit patterns, or of 8-bit codes (copied as byte pairs).
+    """
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    if k_cache.dtype == np.uint8:
+        k_cache = k_cache.view(np.uint16)
+        v_cache = v_cache.view(np.uint16)
     pr = _i32(pairs).reshape(-1, 2)
     blk = k_cache.shape[1] * k_cache.shape[2] * k_cache.shape[3]
     lib().or_copy_blocks(_p(k_cache, ctypes.c_uint16), _p(v_cache, ctypes.c_uint16),
@@ -240,6 +266,83 @@ def contiguous_decode(q, K, V, scale):
 
 def max_threads():
     return int(lib().or_max_threads())
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) KV cache   [P1 "How can one customize the tokenizer, cache
+# strategy, or scheduler strategy?" (kv_cache_dtype="fp8"); P3 "Quantization:
+# Reducing Weight & KV Precision" (--kv-cache-dtype fp8)].  Our reading: OCP
+# E4M3 codes with one scale per tensor; code = e4m3_rne_satfinite(x / scale)
+# with the division in binary32, value = e4m3(code) * scale.
+# --------------------------------------------------------------------------
+
+def e4m3_decode(codes):
+    """uint8 E4M3 codes -> exact fp64 values (NaN for S.1111.111)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().or_e4m3_decode_array(_p(c, ctypes.c_uint8), c.size, _p(out, ctypes.c_double))
+    return out
+
+
+def e4m3_encode(x):
+    """binary32 values -> E4M3 codes (round to nearest even, saturating)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().or_e4m3_encode_array(_p(x, ctypes.c_float), x.size, _p(out, ctypes.c_uint8))
+    return out
+
+
+def cache_write_fp8(k_cache, v_cache, k, v, src_dtype, slots, k_scale, v_scale):
+    """In place: pool rows at `slots` <- E4M3 codes of k / k_scale, v / v_scale.
+
+    k_cache, v_cache: uint8 [num_blocks, B, H_kv, D]; k, v: uint16 [n, H_kv, D]
+    in src_dtype; slot < 0 skipped.
+    """
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    k = _u16(k)
+    v = _u16(v)
+    s = np.ascontiguousarray(slots, dtype=np.int64)
+    row = k_cache.shape[2] * k_cache.shape[3]
+    lib().or_cache_write_fp8(_p(k_cache, ctypes.c_uint8), _p(v_cache, ctypes.c_uint8),
+                             _p(k, ctypes.c_uint16), _p(v, ctypes.c_uint16), int(src_dtype),
+                             _p(s, ctypes.c_int64), s.size, row, float(np.float32(k_scale)),
+                             float(np.float32(v_scale)))
+
+
+def gather_head_fp8(cache, scale, table_row, T, h):
+    """fp64 [T, D] of KV head h from an E4M3 pool, dequantized."""
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    nb, B, H, D = cache.shape
+    row = _i32(table_row)
+    out = np.empty((int(T), D), dtype=np.float64)
+    lib().or_gather_head_fp8(_p(cache, ctypes.c_uint8), float(scale), _p(row, ctypes.c_int32),
+                             int(T), B, H, D, int(h), _p(out, ctypes.c_double))
+    return out
+
+
+def paged_decode_fp8(q, k_cache, v_cache, q_dtype, k_scale, v_scale, block_tables, seq_lens,
+                     scale, seq_ids=None, threads=0):
+    """fp64 decode output [len(seq_ids), Hq, D] over E4M3 pools (uint8)."""
+    q = _u16(q)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    N, Hq, D = q.shape
+    nb, B, H_kv, D2 = k_cache.shape
+    assert D == D2 and Hq % H_kv == 0
+    bt = _i32(block_tables)
+    sl = _i32(seq_lens)
+    ids = _i32(np.arange(N) if seq_ids is None else seq_ids)
+    out = np.empty((ids.size, Hq, D), dtype=np.float64)
+    rc = lib().or_paged_decode_fp8(_p(q, ctypes.c_uint16), _p(k_cache, ctypes.c_uint8),
+                                   _p(v_cache, ctypes.c_uint8), int(q_dtype),
+                                   float(np.float32(k_scale)), float(np.float32(v_scale)),
+                                   _p(bt, ctypes.c_int32), bt.shape[1], _p(sl, ctypes.c_int32),
+                                   _p(ids, ctypes.c_int32), ids.size, Hq, H_kv, D, B,
+                                   float(scale), _p(out, ctypes.c_double), int(threads))
+    if rc != 0:
+        raise MemoryError("oracle decode could not allocate its gather buffers")
+    return out
 
 
 # --------------------------------------------------------------------------

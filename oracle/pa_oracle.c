@@ -286,6 +286,159 @@ void or_contiguous_decode(const double* q /*[Hq][D]*/, const double* K, const do
     free(s);
 }
 
+/* ---------------------------------------------------------------------------
+ * FP8 KV cache ("vLLM Framework and Inference Engine Design", section "How can
+ * one customize the tokenizer, cache strategy, or scheduler strategy?", the
+ * kv_cache_dtype="fp8" flag: half the KV memory of FP16; "vLLM anatomy",
+ * section "Quantization: Reducing Weight & KV Precision": --kv-cache-dtype fp8
+ * stores the KV cache in FP8).  The pages name neither the 8-bit format nor a
+ * scale convention.  Our reading: the OCP E4M3 format with one scale per
+ * tensor (one for K, one for V); a stored code c stands for e4m3(c) * scale,
+ * and a value x is stored as c = e4m3_rne_satfinite(float(x) / scale), the
+ * division done in IEEE binary32.
+ * ------------------------------------------------------------------------- */
+
+/* E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits, no
+ * infinities.  Exponent field 0: (-1)^s * 2^-6 * f/8 (subnormal); fields
+ * 1..15: (-1)^s * 2^(e-7) * (1 + f/8), except S.1111.111, which is NaN.  The
+ * largest finite magnitude is 1.75 * 2^8 = 448.  Exact in fp64. */
+double or_e4m3_to_f64(uint8_t c) {
+    int s = (c >> 7) & 1;
+    int e = (c >> 3) & 0xf;
+    int f = c & 7;
+    double v;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0) v = ldexp((double)f / 8.0, -6);
+    else v = ldexp(1.0 + (double)f / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Round half to even of a non-negative double. */
+static double or_rne(double q) {
+    double fl = floor(q);
+    double diff = q - fl;
+    if (diff > 0.5) return fl + 1.0;
+    if (diff < 0.5) return fl;
+    return fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;
+}
+
+/* binary32 -> E4M3 code, round to nearest (ties to even), magnitudes beyond
+ * the largest finite value saturate to +-448; NaN gives 0x7F. */
+uint8_t or_e4m3_from_f32(float x) {
+    if (isnan(x)) return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7e;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal spacing 2^-9; a result of 8 is the smallest normal, code 8 */
+        double m = or_rne(a / ldexp(1.0, -9));
+        return sign | (uint8_t)m;
+    }
+    int e2;
+    frexp(a, &e2);          /* a = fr * 2^e2, fr in [0.5, 1): a in [2^(e2-1), 2^e2) */
+    int e = e2 - 1;         /* a in [2^e, 2^(e+1)) */
+    double m = or_rne(a / ldexp(1.0, e - 3));   /* in [8, 16] */
+    if (m == 16.0) {
+        m = 8.0;
+        e += 1;
+    }
+    if (e + 7 > 15 || (e + 7 == 15 && m - 8.0 > 6.0)) return sign | 0x7e;
+    return sign | (uint8_t)(((e + 7) << 3) | (int)(m - 8.0));
+}
+
+void or_e4m3_encode_array(const float* src, int64_t n, uint8_t* dst) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = or_e4m3_from_f32(src[i]);
+}
+
+void or_e4m3_decode_array(const uint8_t* src, int64_t n, double* dst) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = or_e4m3_to_f64(src[i]);
+}
+
+/* Quantizing cache write: pool row at slot_mapping[n] <- codes of k[n], v[n]
+ * (16-bit rows of row_elems elements in src_dtype); slot < 0 is skipped. */
+void or_cache_write_fp8(uint8_t* k_cache, uint8_t* v_cache, const uint16_t* k,
+                        const uint16_t* v, int src_dtype, const int64_t* slots,
+                        int64_t n_tok, int64_t row_elems, float k_scale, float v_scale) {
+    for (int64_t n = 0; n < n_tok; ++n) {
+        int64_t s = slots[n];
+        if (s < 0) continue;
+        for (int64_t e = 0; e < row_elems; ++e) {
+            volatile float kx = (float)or_decode(k[n * row_elems + e], src_dtype);
+            volatile float vx = (float)or_decode(v[n * row_elems + e], src_dtype);
+            volatile float kq = kx / k_scale;
+            volatile float vq = vx / v_scale;
+            k_cache[s * row_elems + e] = or_e4m3_from_f32(kq);
+            v_cache[s * row_elems + e] = or_e4m3_from_f32(vq);
+        }
+    }
+}
+
+/* Gather of one KV head from an E4M3 pool: out[t][d] = e4m3(code) * scale. */
+void or_gather_head_fp8(const uint8_t* cache, double scale, const int32_t* table_row,
+                        int64_t T, int32_t B, int32_t H_kv, int32_t D, int32_t h,
+                        double* out) {
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = or_slot(table_row, t, B);
+        const uint8_t* row = cache + (slot * H_kv + h) * (int64_t)D;
+        for (int32_t d = 0; d < D; ++d) out[t * D + d] = or_e4m3_to_f64(row[d]) * scale;
+    }
+}
+
+/* Paged single-query decode over E4M3 pools: the same textbook attention as
+ * or_paged_decode on the dequantized K and V; q (and the output) stay in
+ * q_dtype (binary16 or bfloat16). */
+int or_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                        int q_dtype, double k_scale, double v_scale,
+                        const int32_t* block_tables, int64_t table_stride,
+                        const int32_t* seq_lens, const int32_t* seq_ids, int32_t n_ids,
+                        int32_t Hq, int32_t H_kv, int32_t D, int32_t B, double scale,
+                        double* out, int threads) {
+    int32_t G = Hq / H_kv;
+    int64_t n_work = (int64_t)n_ids * H_kv;
+    int failed = 0;
+#ifdef _OPENMP
+    if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+    for (int64_t w = 0; w < n_work; ++w) {
+        int32_t idx = (int32_t)(w / H_kv);
+        int32_t h = (int32_t)(w % H_kv);
+        int32_t i = seq_ids[idx];
+        int64_t T = seq_lens[i];
+        double* o = out + (int64_t)idx * Hq * D;
+        if (T <= 0) {
+            for (int32_t g = 0; g < G; ++g)
+                for (int32_t d = 0; d < D; ++d) o[(int64_t)(h * G + g) * D + d] = 0.0;
+            continue;
+        }
+        const int32_t* row = block_tables + (int64_t)i * table_stride;
+        double* K = (double*)malloc((size_t)(T * D) * sizeof(double));
+        double* V = (double*)malloc((size_t)(T * D) * sizeof(double));
+        double* s = (double*)malloc((size_t)T * sizeof(double));
+        double* qv = (double*)malloc((size_t)D * sizeof(double));
+        if (!K || !V || !s || !qv) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+            or_gather_head_fp8(k_cache, k_scale, row, T, B, H_kv, D, h, K);
+            or_gather_head_fp8(v_cache, v_scale, row, T, B, H_kv, D, h, V);
+            for (int32_t g = 0; g < G; ++g) {
+                int32_t hq = h * G + g;
+                const uint16_t* qrow = q + ((int64_t)i * Hq + hq) * D;
+                for (int32_t d = 0; d < D; ++d) qv[d] = or_decode(qrow[d], q_dtype);
+                or_attention_1q(qv, K, V, T, D, scale, o + (int64_t)hq * D, s);
+            }
+        }
+        free(K);
+        free(V);
+        free(s);
+        free(qv);
+    }
+    return failed ? -1 : 0;
+}
+
 int or_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -13,7 +13,8 @@ Inference Engine Design", "vLLM anatomy", "vLLM"), and ragged lengths.
 
 Conventions:
 * pools are uint16 bit patterns [num_blocks, block_size, num_kv_heads, head_dim]
-  holding binary16 (F16) or bfloat16 (BF16) values;
+  holding binary16 (F16) or bfloat16 (BF16) values, or, for an FP8 KV cache,
+  uint8 E4M3 codes of the same shape with one scale for K and one for V;
 * ``seq_lens`` count the tokens after the step's cache write: the step writes
   the K/V of position seq_lens[i] - 1 (and, for the shared-prefix workload, of
   the whole divergent suffix) and then decodes the query of the newest token;
@@ -29,7 +30,8 @@ from .blocks import BlockPool, Sequence
 
 F16 = 0
 BF16 = 1
-DTYPE_NAMES = {F16: "f16", BF16: "bf16"}
+FP8 = 2   # E4M3 KV cache (the pools only; q and the new K/V rows stay 16-bit)
+DTYPE_NAMES = {F16: "f16", BF16: "bf16", FP8: "e4m3"}
 
 
 # ---------------------------------------------------------------------------
@@ -82,6 +84,44 @@ def _normal_bits_into(out, sigma, dtype, seed, rows=None, chunk_rows=256, thread
             list(ex.map(work, range(n_chunks)))
 
 
+def random_e4m3_codes(rng, shape, exp_mean=12.5, exp_sd=1.2):
+    """Random E4M3 codes (no NaN codes) built bit field by bit field: a
+    random sign, an exponent field drawn around exp_mean (12.5: magnitudes
+    near 2^5.5, the bulk of a tensor quantized with scale amax / 448) and a
+    uniform 3-bit fraction."""
+    n = int(np.prod(shape))
+    sign = rng.integers(0, 2, n, dtype=np.uint8) << np.uint8(7)
+    e = np.clip(np.rint(rng.normal(exp_mean, exp_sd, n)), 0, 15).astype(np.uint8)
+    f = rng.integers(0, 8, n, dtype=np.uint8)
+    f[(e == 15) & (f == 7)] = 6   # S.1111.111 is NaN
+    return (sign | (e << np.uint8(3)) | f).reshape(shape)
+
+
+def _e4m3_codes_into(out, seed, rows, chunk_rows=256, threads=8):
+    """Fill rows of a uint8 pool with random_e4m3_codes, one generator per
+    chunk of rows spawned from ``seed``."""
+    n = len(rows)
+    n_chunks = max(1, -(-n // chunk_rows))
+    if not isinstance(seed, np.random.SeedSequence):
+        seed = np.random.SeedSequence(seed)
+    children = seed.spawn(n_chunks)
+    inner = out.shape[1:]
+
+    def work(c):
+        lo, hi = c * chunk_rows, min(n, (c + 1) * chunk_rows)
+        out[rows[lo:hi]] = random_e4m3_codes(np.random.default_rng(children[c]),
+                                             (hi - lo,) + inner)
+
+    if n_chunks == 1:
+        work(0)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(work, range(n_chunks)))
+
+
+E4M3_NAN = 0x7F
+
+
 @dataclass
 class Workload:
     name: str
@@ -104,6 +144,13 @@ class Workload:
     seed: int
     recipe: str
     shared_blocks: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))
+    kv_dtype: int = -1            # FP8 for an E4M3 pool; -1: the pools hold `dtype`
+    k_scale: float = 1.0          # E4M3 pools: value = e4m3(code) * scale
+    v_scale: float = 1.0
+
+    @property
+    def fp8(self):
+        return self.kv_dtype == FP8
 
     @property
     def num_seqs(self):
@@ -124,7 +171,7 @@ class Workload:
 
     @property
     def elem_bytes(self):
-        return 2
+        return 1 if self.fp8 else 2
 
 
 def _tables_from_lengths(lens, B, pool):
@@ -141,8 +188,9 @@ def _tables_from_lengths(lens, B, pool):
 
 
 def _garbage_fill(k_cache, v_cache, valid_mask, dtype):
-    k_cache[~valid_mask] = NAN_BITS[dtype]
-    v_cache[~valid_mask] = NAN_BITS[dtype]
+    nan = E4M3_NAN if k_cache.dtype == np.uint8 else NAN_BITS[dtype]
+    k_cache[~valid_mask] = nan
+    v_cache[~valid_mask] = nan
 
 
 def valid_slot_mask(wl):
@@ -160,11 +208,12 @@ def valid_slot_mask(wl):
 
 
 def decode_workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, seed, q_sigma=1.0,
-                    kv_sigma=1.0, garbage="random", recipe=""):
+                    kv_sigma=1.0, garbage="random", recipe="", fp8_scales=None):
     """One new token per sequence at position T_i - 1, then decode.
 
     Blocks are popped, sequence by sequence and block by block, from a free
-    list in the order of a seeded permutation of the pool."""
+    list in the order of a seeded permutation of the pool.  With
+    fp8_scales = (k_scale, v_scale) the pools hold random E4M3 codes."""
     lens = np.asarray(lens, dtype=np.int32)
     ss = np.random.SeedSequence(seed)
     s_perm, s_q, s_k, s_v, s_nk, s_nv = ss.spawn(6)
@@ -174,12 +223,18 @@ def decode_workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, seed, q_sigma
     N = lens.shape[0]
     q = np.empty((N, Hq, D), np.uint16)
     _normal_bits_into(q, q_sigma, dtype, s_q)
-    k_cache = np.zeros((num_blocks, B, H_kv, D), np.uint16)
-    v_cache = np.zeros((num_blocks, B, H_kv, D), np.uint16)
     used = bt[bt >= 0]
-    # values of the allocated blocks, in allocation order
-    _normal_bits_into(k_cache, kv_sigma, dtype, s_k, rows=used)
-    _normal_bits_into(v_cache, kv_sigma, dtype, s_v, rows=used)
+    if fp8_scales is None:
+        k_cache = np.zeros((num_blocks, B, H_kv, D), np.uint16)
+        v_cache = np.zeros((num_blocks, B, H_kv, D), np.uint16)
+        # values of the allocated blocks, in allocation order
+        _normal_bits_into(k_cache, kv_sigma, dtype, s_k, rows=used)
+        _normal_bits_into(v_cache, kv_sigma, dtype, s_v, rows=used)
+    else:
+        k_cache = np.zeros((num_blocks, B, H_kv, D), np.uint8)
+        v_cache = np.zeros((num_blocks, B, H_kv, D), np.uint8)
+        _e4m3_codes_into(k_cache, s_k, used)
+        _e4m3_codes_into(v_cache, s_v, used)
     new_seq = np.arange(N, dtype=np.int32)
     new_pos = (lens - 1).astype(np.int32)
     k_new = np.empty((N, H_kv, D), np.uint16)
@@ -188,6 +243,10 @@ def decode_workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, seed, q_sigma
     _normal_bits_into(v_new, kv_sigma, dtype, s_nv)
     wl = Workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, bt, q, k_cache, v_cache,
                   new_seq, new_pos, k_new, v_new, np.zeros((0, 2), np.int32), seed, recipe)
+    if fp8_scales is not None:
+        wl.kv_dtype = FP8
+        wl.k_scale = float(np.float32(fp8_scales[0]))
+        wl.v_scale = float(np.float32(fp8_scales[1]))
     if garbage == "nan":
         _garbage_fill(k_cache, v_cache, valid_slot_mask(wl), dtype)
     return wl
@@ -236,6 +295,24 @@ def llama3_8b(seed=3, num_seqs=256, garbage="random", num_blocks=40_000):
                            recipe="T ~ round(lognormal(ln400 - 0.632^2/2, 0.632)) clipped to "
                                   "[16,4096]; q ~ N(0,1), k,v ~ N(0,0.25) bf16; free list = "
                                   "seeded permutation of 40,000 blocks")
+
+
+# E4M3 scales of the FP8 workloads: K/V ~ N(0, 0.5^2) quantized with
+# scale amax / 448 would put sigma near 2^6 codes' magnitude; 2^-7 does that.
+FP8_SCALES = (2.0 ** -7, 2.0 ** -7)
+
+
+def llama3_8b_fp8(seed=3, num_seqs=256, garbage="random", num_blocks=40_000):
+    """The Llama-3-8B GQA layer with an FP8 (E4M3) KV cache: same lengths,
+    tables and queries as llama3-8b-gqa; random E4M3 codes in the pool,
+    k_scale = v_scale = 2^-7; the step's new K/V rows are bf16 and are
+    quantized by the write."""
+    lens = llama3_8b_lengths(seed, num_seqs)
+    return decode_workload("llama3-8b-gqa-fp8", BF16, 32, 8, 128, 16, num_blocks, lens, seed,
+                           q_sigma=1.0, kv_sigma=0.5, garbage=garbage, fp8_scales=FP8_SCALES,
+                           recipe="llama3-8b-gqa lengths and tables; pool = random E4M3 "
+                                  "codes (sign uniform, exponent field ~ round(N(12.5, "
+                                  "1.2)), fraction uniform); k_scale = v_scale = 2^-7")
 
 
 def long_context_70b(seed=5, num_seqs=32, lo=16_384, hi=32_768, garbage="random"):
@@ -309,7 +386,7 @@ def shared_prefix(seed=4, num_seqs=12, prefix=1800, suffix_hi=300, num_blocks=10
 
 
 def random_workload(seed, dtype, Hq, H_kv, D, B, lens, num_blocks=None, q_sigma=1.0,
-                    kv_sigma=1.0, garbage="random", spare_blocks=7):
+                    kv_sigma=1.0, garbage="random", spare_blocks=7, fp8_scales=None):
     """A parity-test case of any shape: blocks scattered through a pool with
     spare_blocks extra blocks."""
     lens = np.asarray(lens, np.int32)
@@ -318,7 +395,7 @@ def random_workload(seed, dtype, Hq, H_kv, D, B, lens, num_blocks=None, q_sigma=
         num_blocks = need + spare_blocks
     return decode_workload("random", dtype, Hq, H_kv, D, B, num_blocks, lens, seed,
                            q_sigma=q_sigma, kv_sigma=kv_sigma, garbage=garbage,
-                           recipe="parity case")
+                           recipe="parity case", fp8_scales=fp8_scales)
 
 
 CONFIGS = {
@@ -327,4 +404,5 @@ CONFIGS = {
     "llama3-8b-gqa": llama3_8b,
     "qwen2-0.5b-shared-prefix": shared_prefix,
     "70b-long-context": long_context_70b,
+    "llama3-8b-gqa-fp8": llama3_8b_fp8,
 }
