@@ -45,6 +45,8 @@ extern "C" {
 /* element types */
 #define PA_F16 0
 #define PA_BF16 1
+/* E4M3 KV-cache codes (pools only; see pa_cache_write_fp8 / pa_decode_fp8) */
+#define PA_FP8_E4M3 2
 
 /* status codes returned by the entry points */
 #define PA_OK 0
@@ -111,11 +113,34 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, in
  * Every pair copies all block_size * num_kv_heads * head_dim elements of K and
  * of V from src to dst.  Pairs are independent: dst blocks must be distinct and
  * no dst may also be a src.  A pair out of range, or one that breaks this rule,
- * sets PA_DEVERR_COPY_PAIR and is not copied.
+ * sets PA_DEVERR_COPY_PAIR and is not copied.  dtype PA_FP8_E4M3 copies pools
+ * of 1-byte codes.
  */
 int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cache, void* v_cache,
                    int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                    int32_t head_dim, int32_t dtype, int32_t* err_word, pa_stream stream);
+
+/*
+ * pa_cache_write_fp8 -- pa_cache_write into an E4M3 (FP8) KV cache.
+ * [P1] "How can one customize the tokenizer, cache strategy, or scheduler
+ * strategy?" (kv_cache_dtype="fp8": half the KV memory of FP16); [P3]
+ * "Quantization: Reducing Weight & KV Precision" (--kv-cache-dtype fp8).  The
+ * pages name neither the 8-bit format nor a scale; our reading is OCP E4M3
+ * with one scale per tensor:
+ *   code = e4m3(float32(x) / scale), rounded to nearest even, magnitudes
+ *   beyond 448 saturating to +-448; the code stands for e4m3(code) * scale.
+ *   k, v          [num_tokens][num_kv_heads][head_dim], contiguous, src_dtype
+ *                 (PA_F16 or PA_BF16), finite
+ *   k_cache, v_cache  uint8 [num_blocks][block_size][num_kv_heads][head_dim]
+ *   k_scale, v_scale  finite and > 0
+ * Slots as for pa_cache_write.  The division is IEEE binary32 and the codes
+ * are bit-exact.
+ */
+int pa_cache_write_fp8(const void* k, const void* v, int32_t src_dtype,
+                       const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                       void* v_cache, int64_t num_blocks, int32_t block_size,
+                       int32_t num_kv_heads, int32_t head_dim, float k_scale, float v_scale,
+                       int32_t* err_word, pa_stream stream);
 
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
@@ -126,6 +151,7 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
  * largest call serves calls of any shape and num_ctas.  num_ctas = 0 selects
  * the default grid (a multiple of the SM count); larger than
  * PA_DECODE_MAX_CTAS returns PA_ERR_INVALID_ARG; flags as for pa_decode.
+ * dtype PA_FP8_E4M3 sizes the workspace of pa_decode_fp8.
  */
 #define PA_DECODE_MAX_CTAS 16384
 int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -165,6 +191,30 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               int32_t block_size, int64_t num_blocks, int32_t dtype, float scale, void* out,
               void* workspace, size_t workspace_bytes, int32_t flags, int32_t num_ctas,
               int32_t* err_word, pa_stream stream);
+
+/*
+ * pa_decode_fp8 -- pa_decode over E4M3 pools written by pa_cache_write_fp8.
+ * Computes out = softmax(scale * q . K^T) . V with K = e4m3(code_K) * k_scale
+ * and V = e4m3(code_V) * v_scale ([P1] "What is the essence of vLLM's
+ * PagedAttention?", on the dequantized cache).  The scales are applied outside
+ * the products (k_scale joins `scale`, v_scale multiplies the output); the
+ * codes convert exactly to binary16, queries in bfloat16 are converted to
+ * binary16 (their magnitudes must stay within binary16's range), the softmax
+ * weights are binary16 and every sum is fp32.
+ *   q, out        [num_seqs][num_q_heads][head_dim] in q_dtype (PA_F16 or PA_BF16)
+ *   k_cache, v_cache  uint8 E4M3 pools [num_blocks][block_size][num_kv_heads][head_dim]
+ *   workspace     as for pa_decode, sized by pa_decode_workspace_size with
+ *                 dtype PA_FP8_E4M3
+ * Every other argument, the errors and the workspace rules are those of
+ * pa_decode.  pa_gather_kv does not take E4M3 pools.
+ */
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, int64_t num_blocks, int32_t q_dtype, float scale,
+                  float k_scale, float v_scale, void* out, void* workspace,
+                  size_t workspace_bytes, int32_t flags, int32_t num_ctas, int32_t* err_word,
+                  pa_stream stream);
 
 /*
  * pa_decode_noalloc -- pa_decode without a caller-provided workspace.

@@ -10,6 +10,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
 # status codes and flags, mirrored from include/pa.h
 PA_F16 = 0
 PA_BF16 = 1
+PA_FP8_E4M3 = 2
 PA_OK = 0
 PA_ERR_INVALID_ARG = 1
 PA_ERR_UNSUPPORTED = 2
@@ -39,10 +40,15 @@ SIGNATURES = {
     "pa_cache_write": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _i32,
                                       _vp, _vp]),
     "pa_copy_blocks": (ctypes.c_int, [_vp, _i32, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pa_cache_write_fp8": (ctypes.c_int, [_vp, _vp, _i32, _vp, _i64, _vp, _vp, _i64, _i32, _i32,
+                                          _i32, ctypes.c_float, ctypes.c_float, _vp, _vp]),
     "pa_decode_workspace_size": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                                 ctypes.POINTER(_sz)]),
     "pa_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i64,
                                  _i32, ctypes.c_float, _vp, _vp, _sz, _i32, _i32, _vp, _vp]),
+    "pa_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                     _i64, _i32, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                     _vp, _vp, _sz, _i32, _i32, _vp, _vp]),
     "pa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                          _i32, _i64, _i32, ctypes.c_float, _vp, _i32, _i32, _vp,
                                          _vp]),

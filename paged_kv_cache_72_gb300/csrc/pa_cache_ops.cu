@@ -7,7 +7,12 @@
 // memory fragmentation, and how does vLLM avoid it?": a shared block is copied
 // only when a sequence needs to write into it.
 //
-// All three are pure data movement: 16-byte vector copies, bit-exact.
+// The slot mapping, the 16-bit cache write and the block copy are pure data
+// movement (16-byte vector copies, bit-exact).  The E4M3 cache write quantizes
+// ("vLLM Framework and Inference Engine Design", section "How can one
+// customize the tokenizer, cache strategy, or scheduler strategy?",
+// kv_cache_dtype="fp8"; our reading: code = e4m3(float32(x) / scale), round to
+// nearest even, saturating).
 #include "pa_device.cuh"
 #include "pa_host.h"
 
@@ -66,6 +71,43 @@ __global__ void cache_write_kernel(const uint4* __restrict__ k, const uint4* __r
   }
 }
 
+// E4M3 cache write: one block per new token; each thread turns 8 16-bit
+// elements (16 bytes) of the token's K and V rows into 8 codes (8 bytes).
+template <bool kBF16>
+__global__ void cache_write_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                       const int64_t* __restrict__ slots, int vecs_per_row,
+                                       long long num_slots, uint2* __restrict__ kc,
+                                       uint2* __restrict__ vc, float k_scale, float v_scale,
+                                       int32_t* err) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const long long tok = blockIdx.x;
+  const long long s = slots[tok];
+  if (s < 0) return;
+  if (s >= num_slots) {
+    if (threadIdx.x == 0) set_error(err, PA_DEVERR_SLOT);
+    return;
+  }
+  auto quantize8 = [](const uint4 x, float scale) -> uint2 {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack2<kBF16>(w[i]);
+      c[i] = f32x2_to_e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  };
+  const uint4* ks = k + tok * vecs_per_row;
+  const uint4* vs = v + tok * vecs_per_row;
+  uint2* kd = kc + s * vecs_per_row;
+  uint2* vd = vc + s * vecs_per_row;
+  for (int e = threadIdx.x; e < vecs_per_row; e += blockDim.x) {
+    kd[e] = quantize8(__ldg(ks + e), k_scale);
+    vd[e] = quantize8(__ldg(vs + e), v_scale);
+  }
+}
+
 // One block per (pair, K or V).  A pair is copied only if it is in range, its
 // dst appears once among the dsts and is no pair's src.
 __global__ void copy_blocks_kernel(const int32_t* __restrict__ pairs, int num_pairs,
@@ -96,9 +138,11 @@ __global__ void copy_blocks_kernel(const int32_t* __restrict__ pairs, int num_pa
   for (int e = threadIdx.x; e < vecs_per_block; e += blockDim.x) d[e] = s[e];
 }
 
-static bool shape_ok(int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t dtype) {
+static bool shape_ok(int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                     bool allow_fp8 = false) {
   return (head_dim == 64 || head_dim == 128) && num_kv_heads > 0 && is_pow2(block_size) &&
-         block_size <= 256 && (dtype == PA_F16 || dtype == PA_BF16);
+         block_size <= 256 &&
+         (dtype == PA_F16 || dtype == PA_BF16 || (allow_fp8 && dtype == PA_FP8_E4M3));
 }
 
 }  // namespace pa
@@ -157,12 +201,13 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
                    int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                    int32_t head_dim, int32_t dtype, int32_t* err_word, pa_stream stream) {
   if (num_pairs < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
-  if (!shape_ok(block_size, num_kv_heads, head_dim, dtype)) return PA_ERR_UNSUPPORTED;
+  if (!shape_ok(block_size, num_kv_heads, head_dim, dtype, true)) return PA_ERR_UNSUPPORTED;
   if (num_pairs == 0) return PA_OK;
   if (num_pairs > 65535) return PA_ERR_INVALID_ARG;
   if (!src_dst_pairs || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
-  const long long vecs = (long long)block_size * num_kv_heads * head_dim * 2 / 16;
+  const int eb = dtype == PA_FP8_E4M3 ? 1 : 2;
+  const long long vecs = (long long)block_size * num_kv_heads * head_dim * eb / 16;
   if (vecs > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   dim3 grid((unsigned)num_pairs, 2);
   clear_stale_error();
@@ -172,6 +217,39 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
                                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                   err_word),
                        "block copy launch");
+}
+
+int pa_cache_write_fp8(const void* k, const void* v, int32_t src_dtype,
+                       const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                       void* v_cache, int64_t num_blocks, int32_t block_size,
+                       int32_t num_kv_heads, int32_t head_dim, float k_scale, float v_scale,
+                       int32_t* err_word, pa_stream stream) {
+  if (num_tokens < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (!shape_ok(block_size, num_kv_heads, head_dim, src_dtype)) return PA_ERR_UNSUPPORTED;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale > 3.0e38f || v_scale > 3.0e38f)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (num_tokens > 0x7fffffffLL) return PA_ERR_INVALID_ARG;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const int vecs = num_kv_heads * head_dim / 8;   // 16-byte input vectors per row
+  const int threads = vecs >= 256 ? 256 : (vecs >= 128 ? 128 : 64);
+  clear_stale_error();
+  const long long num_slots = num_blocks * (long long)block_size;
+  cudaError_t e =
+      src_dtype == PA_BF16
+          ? launch_pdl(cache_write_fp8_kernel<true>, dim3((unsigned)num_tokens), dim3(threads), 0,
+                       static_cast<cudaStream_t>(stream), static_cast<const uint4*>(k),
+                       static_cast<const uint4*>(v), slot_mapping, vecs, num_slots,
+                       static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), k_scale,
+                       v_scale, err_word)
+          : launch_pdl(cache_write_fp8_kernel<false>, dim3((unsigned)num_tokens), dim3(threads), 0,
+                       static_cast<cudaStream_t>(stream), static_cast<const uint4*>(k),
+                       static_cast<const uint4*>(v), slot_mapping, vecs, num_slots,
+                       static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), k_scale,
+                       v_scale, err_word);
+  return launch_status(e, "E4M3 cache write launch");
 }
 
 }  // extern "C"

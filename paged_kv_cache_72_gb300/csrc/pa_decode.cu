@@ -3,6 +3,8 @@
 // KV pools, and the C entry points.
 #include <string.h>
 
+#include <cmath>
+
 #include <mutex>
 
 #include "pa_decode_kernel.cuh"
@@ -20,11 +22,17 @@ int ctrl_bytes(int stages) {
   return 16 * stages + 16 * kQBufs + kScanBytes + kCtrlBytes + kRowScratchBytes;
 }
 
-int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas, bool gather,
-              DecodePlan* p) {
+// kv_dtype: the pools' element type (PA_F16, PA_BF16 or PA_FP8_E4M3);
+// q_dtype: queries and output (PA_F16 or PA_BF16; equal to kv_dtype unless
+// the pools are E4M3).
+int make_plan(int Hq, int Hkv, int D, int B, int kv_dtype, int q_dtype, int flags, int num_ctas,
+              bool gather, DecodePlan* p) {
   if (Hq <= 0 || Hkv <= 0 || num_ctas < 0 || num_ctas > PA_DECODE_MAX_CTAS)
     return PA_ERR_INVALID_ARG;
-  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  const bool f8 = kv_dtype == PA_FP8_E4M3;
+  if (f8 && gather) return PA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
   if (!is_pow2(B) || B < 2 || B > 256) return PA_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
@@ -33,7 +41,9 @@ int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas,
   if (flags != PA_DECODE_AUTO && flags != PA_DECODE_SIMT && flags != PA_DECODE_MMA)
     return PA_ERR_INVALID_ARG;
   DecodePlan q{};
-  q.bf16 = dtype == PA_BF16;
+  q.bf16 = q_dtype == PA_BF16;
+  q.f8 = f8;
+  const int eb = f8 ? 1 : 2;   // bytes of one KV element
   q.D = D;
   q.G = G;
   q.B = B;
@@ -60,10 +70,13 @@ int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas,
   q.R = B < q.CT ? B : q.CT;
   q.nsb = q.CT / q.R;
   if (q.nsb > 32) return PA_ERR_UNSUPPORTED;   // one producer lane per TMA box
-  const int box_bytes = q.R * q.HG * D * 2;
-  q.swz = want_swz && (box_bytes % 1024 == 0);
+  const int box_bytes = q.R * q.HG * D * eb;
+  // the swizzled TMA layout repeats every 1024 bytes (128-byte swizzle) or
+  // 512 bytes (the 64-byte swizzle of 64-byte E4M3 rows); boxes land on
+  // multiples of box_bytes
+  q.swz = want_swz && (box_bytes % ((f8 && D == 64) ? 512 : 1024) == 0);
   q.split_rows = true;
-  q.kv_bytes = q.CT * q.HG * D * 2;
+  q.kv_bytes = q.CT * q.HG * D * eb;
   q.stage_bytes = 2 * q.kv_bytes;
   q.q_bytes = gather ? 0 : q.HG * G * D * 2;
   q.q_stride = ((q.q_bytes + 127) / 128) * 128;
@@ -85,7 +98,10 @@ int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas,
 
   // opts the kernel in to its shared memory and reports its occupancy
   int per_sm = 0;
-  const int rc = D == 64 ? decode_ctas_per_sm_d64(q, &per_sm) : decode_ctas_per_sm_d128(q, &per_sm);
+  const int rc = f8 ? (D == 64 ? decode_ctas_per_sm_f8_d64(q, &per_sm)
+                               : decode_ctas_per_sm_f8_d128(q, &per_sm))
+                    : (D == 64 ? decode_ctas_per_sm_d64(q, &per_sm)
+                               : decode_ctas_per_sm_d128(q, &per_sm));
   if (rc != PA_OK) return rc;
   if (per_sm < 1) return PA_ERR_UNSUPPORTED;
   q.grid = num_ctas > 0 ? num_ctas : di.sm_count * per_sm;
@@ -101,10 +117,11 @@ int make_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas,
 // Plans depend only on the shape and the device: keep them, so that a call
 // does no attribute or occupancy queries after the first one for its shape.
 struct PlanKey {
-  int dev, Hq, Hkv, D, B, dtype, flags, num_ctas, gather;
+  int dev, Hq, Hkv, D, B, kv_dtype, q_dtype, flags, num_ctas, gather;
   bool operator==(const PlanKey& o) const {
     return dev == o.dev && Hq == o.Hq && Hkv == o.Hkv && D == o.D && B == o.B &&
-           dtype == o.dtype && flags == o.flags && num_ctas == o.num_ctas && gather == o.gather;
+           kv_dtype == o.kv_dtype && q_dtype == o.q_dtype && flags == o.flags &&
+           num_ctas == o.num_ctas && gather == o.gather;
   }
 };
 constexpr int kPlanCache = 64;
@@ -113,14 +130,14 @@ DecodePlan g_plan[kPlanCache];
 int g_plan_n = 0, g_plan_next = 0;
 std::mutex g_plan_mu;
 
-int cached_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_ctas, bool gather,
-                DecodePlan* p) {
+int cached_plan(int Hq, int Hkv, int D, int B, int kv_dtype, int q_dtype, int flags,
+                int num_ctas, bool gather, DecodePlan* p) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     // still report shape errors without a device
-    return make_plan(Hq, Hkv, D, B, dtype, flags, num_ctas, gather, p);
+    return make_plan(Hq, Hkv, D, B, kv_dtype, q_dtype, flags, num_ctas, gather, p);
   }
-  const PlanKey k{dev, Hq, Hkv, D, B, dtype, flags, num_ctas, gather ? 1 : 0};
+  const PlanKey k{dev, Hq, Hkv, D, B, kv_dtype, q_dtype, flags, num_ctas, gather ? 1 : 0};
   {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (int i = 0; i < g_plan_n; ++i)
@@ -129,7 +146,7 @@ int cached_plan(int Hq, int Hkv, int D, int B, int dtype, int flags, int num_cta
         return PA_OK;
       }
   }
-  if (int rc = make_plan(Hq, Hkv, D, B, dtype, flags, num_ctas, gather, p)) return rc;
+  if (int rc = make_plan(Hq, Hkv, D, B, kv_dtype, q_dtype, flags, num_ctas, gather, p)) return rc;
   std::lock_guard<std::mutex> lk(g_plan_mu);
   const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
   g_plan_key[slot] = k;
@@ -151,6 +168,23 @@ int encode_kv_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int 
   cuuint64_t strides[4];
   cuuint32_t box[5];
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (p.f8) {
+    // E4M3 rows of D bytes, one plane: the box lands as [HG][R][D] bytes
+    const cuuint64_t row8 = (cuuint64_t)Hkv * D;
+    dims[0] = D; dims[1] = B; dims[2] = 1; dims[3] = Hkv; dims[4] = num_blocks;
+    strides[0] = row8; strides[1] = D; strides[2] = D; strides[3] = row8 * B;
+    box[0] = D; box[1] = p.R; box[2] = 1; box[3] = p.HG; box[4] = 1;
+    memset(map, 0, sizeof(*map));
+    const CUtensorMapSwizzle sw = !p.swz ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                         : (D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                     : CU_TENSOR_MAP_SWIZZLE_64B);
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(cache), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) return PA_OK;
+    note_cuda_error(1000 + (int)r, "cuTensorMapEncodeTiled (E4M3 pool)");
+    return PA_ERR_CUDA;
+  }
   const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
   if (split_rows) {
     dims[0] = 64; dims[1] = B; dims[2] = D / 64; dims[3] = Hkv; dims[4] = num_blocks;
@@ -174,6 +208,10 @@ int encode_kv_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int 
 
 int encode_maps_uncached(CUtensorMap* tk, CUtensorMap* tv, const void* kc, const void* vc,
                          DecodePlan* p, int Hkv, long long nb) {
+  if (p->f8) {
+    if (int rc = encode_kv_map(tk, kc, *p, Hkv, nb, true)) return rc;
+    return encode_kv_map(tv, vc, *p, Hkv, nb, true);
+  }
   if (p->split_rows) {
     if (encode_kv_map(tk, kc, *p, Hkv, nb, true) == PA_OK &&
         encode_kv_map(tv, vc, *p, Hkv, nb, true) == PA_OK)
@@ -190,7 +228,7 @@ struct alignas(64) MapEntry {
   const void* kc;
   const void* vc;
   long long nb;
-  int dev, Hkv, D, B, bf16, swz, split_in, split_out;
+  int dev, Hkv, D, B, bf16, f8, swz, split_in, split_out;
 };
 constexpr int kMapCache = 16;
 MapEntry g_maps[kMapCache];
@@ -207,7 +245,8 @@ int encode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* kc, const void* vc
     for (int i = 0; i < g_maps_n; ++i) {
       const MapEntry& m = g_maps[i];
       if (m.kc == kc && m.vc == vc && m.nb == nb && m.dev == dev && m.Hkv == Hkv && m.D == p->D &&
-          m.B == p->B && m.bf16 == (p->bf16 ? 1 : 0) && m.swz == (p->swz ? 1 : 0) &&
+          m.B == p->B && m.bf16 == (p->bf16 ? 1 : 0) && m.f8 == (p->f8 ? 1 : 0) &&
+          m.swz == (p->swz ? 1 : 0) &&
           m.split_in == split_in) {
         *tk = m.tk;
         *tv = m.tv;
@@ -230,6 +269,7 @@ int encode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* kc, const void* vc
   m.D = p->D;
   m.B = p->B;
   m.bf16 = p->bf16 ? 1 : 0;
+  m.f8 = p->f8 ? 1 : 0;
   m.swz = p->swz ? 1 : 0;
   m.split_in = split_in;
   m.split_out = p->split_rows ? 1 : 0;
@@ -256,9 +296,13 @@ void fill_layout(const DecodePlan& p, DecodeArgs* a) {
   a->merge_off = p.merge_off;
   a->ctrl_off = p.ctrl_off;
   a->split_rows = p.split_rows ? 1 : 0;
-  const int lrow = ilog2((long long)p.D * 2);         // one row of one head
-  a->sub_log2 = a->log2R + ilog2(p.HG) + lrow;         // one box
-  if (p.split_rows) {
+  const int lrow = ilog2((long long)p.D * (p.f8 ? 1 : 2));   // one row of one head
+  a->sub_log2 = a->log2R + ilog2(p.HG) + lrow;               // one box
+  if (p.f8) {   // [HG][R][D] bytes
+    a->head_log2 = a->log2R + lrow;
+    a->hi_log2 = 0;
+    a->r_log2 = lrow;
+  } else if (p.split_rows) {
     a->head_log2 = a->log2R + lrow;
     a->hi_log2 = a->log2R + 7;
     a->r_log2 = 7;
@@ -271,38 +315,23 @@ void fill_layout(const DecodePlan& p, DecodeArgs* a) {
 
 int launch(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
            cudaStream_t s) {
+  if (p.f8)
+    return p.D == 64 ? decode_launch_f8_d64(p, tk, tv, a, s) : decode_launch_f8_d128(p, tk, tv, a, s);
   return p.D == 64 ? decode_launch_d64(p, tk, tv, a, s) : decode_launch_d128(p, tk, tv, a, s);
 }
 
-}  // namespace
-}  // namespace pa
-
-using namespace pa;
-
-extern "C" {
-
-int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                             int32_t block_size, int32_t dtype, int32_t flags, int32_t num_ctas,
-                             size_t* bytes) {
-  if (!bytes) return PA_ERR_INVALID_ARG;
-  DecodePlan p;
-  if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
-                           false, &p))
-    return rc;
-  *bytes = p.ws_count_bytes + p.ws_rec_bytes;
-  return PA_OK;
-}
-
-int pa_decode(const void* q, const void* k_cache, const void* v_cache,
-              const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
-              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-              int32_t block_size, int64_t num_blocks, int32_t dtype, float scale, void* out,
-              void* workspace, size_t workspace_bytes, int32_t flags, int32_t num_ctas,
-              int32_t* err_word, pa_stream stream) {
+// The decode behind pa_decode and pa_decode_fp8.
+int decode_call(const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+                int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                int32_t block_size, int64_t num_blocks, int32_t kv_dtype, int32_t q_dtype,
+                float scale, float k_scale, float v_scale, void* out, void* workspace,
+                size_t workspace_bytes, int32_t flags, int32_t num_ctas, int32_t* err_word,
+                pa_stream stream) {
   if (num_seqs < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   DecodePlan p;
-  if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, flags, num_ctas,
-                           false, &p))
+  if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, q_dtype,
+                           flags, num_ctas, false, &p))
     return rc;
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out || !workspace)
@@ -310,6 +339,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   if (num_blocks == 0 || table_stride == 0 || num_blocks > 0xffffffffLL) return PA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(workspace))
+    return PA_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return PA_ERR_INVALID_ARG;
   if (workspace_bytes < p.ws_count_bytes + p.ws_rec_bytes) return PA_ERR_WORKSPACE;
   CUtensorMap tk, tv;
@@ -327,9 +358,57 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   a.stride = table_stride;
   a.Hq = num_q_heads;
   a.Hkv = num_kv_heads;
-  a.scale_log2 = scale * 1.4426950408889634f;
+  a.scale_log2 = scale * k_scale * 1.4426950408889634f;
+  a.v_scale = v_scale;
   fill_layout(p, &a);
   return launch(p, tk, tv, a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t dtype, int32_t flags, int32_t num_ctas,
+                             size_t* bytes) {
+  if (!bytes) return PA_ERR_INVALID_ARG;
+  // an E4M3 cache: the workspace does not depend on the query dtype
+  const int q_dtype = dtype == PA_FP8_E4M3 ? PA_BF16 : dtype;
+  DecodePlan p;
+  if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, q_dtype, flags,
+                           num_ctas, false, &p))
+    return rc;
+  *bytes = p.ws_count_bytes + p.ws_rec_bytes;
+  return PA_OK;
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+              int32_t block_size, int64_t num_blocks, int32_t dtype, float scale, void* out,
+              void* workspace, size_t workspace_bytes, int32_t flags, int32_t num_ctas,
+              int32_t* err_word, pa_stream stream) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  return decode_call(q, k_cache, v_cache, block_tables, table_stride, seq_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, dtype, dtype,
+                     scale, 1.f, 1.f, out, workspace, workspace_bytes, flags, num_ctas, err_word,
+                     stream);
+}
+
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, int64_t num_blocks, int32_t q_dtype, float scale,
+                  float k_scale, float v_scale, void* out, void* workspace,
+                  size_t workspace_bytes, int32_t flags, int32_t num_ctas, int32_t* err_word,
+                  pa_stream stream) {
+  return decode_call(q, k_cache, v_cache, block_tables, table_stride, seq_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, PA_FP8_E4M3,
+                     q_dtype, scale, k_scale, v_scale, out, workspace, workspace_bytes, flags,
+                     num_ctas, err_word, stream);
 }
 
 int pa_gather_kv(const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -339,8 +418,9 @@ int pa_gather_kv(const void* k_cache, const void* v_cache, const int32_t* block_
                  int32_t* err_word, pa_stream stream) {
   if (num_seqs < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   DecodePlan p;
-  if (int rc = cached_plan(num_kv_heads, num_kv_heads, head_dim, block_size, dtype, flags, 0, true,
-                           &p))
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (int rc = cached_plan(num_kv_heads, num_kv_heads, head_dim, block_size, dtype, dtype, flags, 0,
+                           true, &p))
     return rc;
   if (num_seqs == 0) return PA_OK;
   if (!k_cache || !v_cache || !block_tables || !seq_lens || !out_offsets || !k_out || !v_out)

@@ -3,10 +3,10 @@
 
 namespace pa {
 int decode_ctas_per_sm_d128(const DecodePlan& p, int* ctas) {
-  return ctas_per_sm_impl<128>(p, ctas);
+  return ctas_per_sm_impl<128, false>(p, ctas);
 }
 int decode_launch_d128(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        const DecodeArgs& a, cudaStream_t s) {
-  return launch_impl<128>(p, tk, tv, a, s);
+  return launch_impl<128, false>(p, tk, tv, a, s);
 }
 }  // namespace pa

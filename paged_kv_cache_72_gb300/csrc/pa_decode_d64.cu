@@ -2,9 +2,9 @@
 #include "pa_decode_variants.cuh"
 
 namespace pa {
-int decode_ctas_per_sm_d64(const DecodePlan& p, int* ctas) { return ctas_per_sm_impl<64>(p, ctas); }
+int decode_ctas_per_sm_d64(const DecodePlan& p, int* ctas) { return ctas_per_sm_impl<64, false>(p, ctas); }
 int decode_launch_d64(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
                       const DecodeArgs& a, cudaStream_t s) {
-  return launch_impl<64>(p, tk, tv, a, s);
+  return launch_impl<64, false>(p, tk, tv, a, s);
 }
 }  // namespace pa

@@ -1,0 +1,12 @@
+// Decode kernels for head_dim 128 over E4M3 (FP8) caches.
+#include "pa_decode_variants.cuh"
+
+namespace pa {
+int decode_ctas_per_sm_f8_d128(const DecodePlan& p, int* ctas) {
+  return ctas_per_sm_impl<128, true>(p, ctas);
+}
+int decode_launch_f8_d128(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeArgs& a, cudaStream_t s) {
+  return launch_impl<128, true>(p, tk, tv, a, s);
+}
+}  // namespace pa

@@ -85,6 +85,7 @@ struct DecodeArgs {
   int q_stride;              // bytes between query buffers (multiple of 128)
   int merge_off;             // byte offset of the merge buffer (TPH > 1)
   int ctrl_off;              // byte offset of barriers and control words
+  float v_scale;             // E4M3 cache: V value = code * v_scale (1 otherwise)
 };
 
 // Clamped length: invalid lengths count as 0 tokens.
@@ -363,18 +364,36 @@ struct MmaConsumer {
 // ---------------------------------------------------------------------------
 // Consumer state and tile math: CUDA-core path (group size 1)
 // ---------------------------------------------------------------------------
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kF8 = false>
 struct SimtConsumer {
   static constexpr int VEC = D / 32;   // head_dim elements per lane
   float qf[VEC];
   float o[VEC];
   float m, l;
+  float vscale = 1.f;                  // E4M3 cache: the V scale, applied to the output
 
   __device__ __forceinline__ int col() const { return (threadIdx.x & 31) * VEC; }
 
   __device__ __forceinline__ void load_row(uint32_t part, int tt, const DecodeArgs& a,
                                            float* x) const {
     const int c = col();
+    if constexpr (kF8) {
+      // E4M3 rows of D bytes, unswizzled: this lane's VEC codes, exact in f16
+      const uint32_t ra = row_addr(part, tt, 0, a) + (uint32_t)c;
+      if constexpr (VEC == 4) {
+        uint32_t w;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(ra));
+        const float2 p = unpack2<false>(e4m3x2_to_f16x2(w & 0xffffu));
+        const float2 q = unpack2<false>(e4m3x2_to_f16x2(w >> 16));
+        x[0] = p.x; x[1] = p.y; x[2] = q.x; x[3] = q.y;
+      } else {
+        uint16_t h;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(ra));
+        const float2 p = unpack2<false>(e4m3x2_to_f16x2(h));
+        x[0] = p.x; x[1] = p.y;
+      }
+      return;
+    }
     const uint32_t ra = row_addr(part, tt, c >> 6, a) + (uint32_t)((c & 63) * 2);
     if constexpr (VEC == 4) {
       uint32_t w0, w1;
@@ -483,7 +502,7 @@ struct SimtConsumer {
     }
     float* orow = slot + 32;
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) orow[col() + v] = o[v];
+    for (int v = 0; v < VEC; ++v) orow[col() + v] = o[v] * vscale;
   }
 
   __device__ __forceinline__ void write_direct(uint16_t* out_rows, float* rec, int rec_row0,
@@ -491,7 +510,7 @@ struct SimtConsumer {
     const float lt = total_l();
     const int c = col();
     if (full) {
-      const float inv = 1.f / lt;
+      const float inv = vscale / lt;
 #pragma unroll
       for (int v = 0; v < VEC; v += 2)
         *reinterpret_cast<uint32_t*>(out_rows + c + v) = pack2<kBF16>(o[v] * inv, o[v + 1] * inv);
@@ -502,10 +521,16 @@ struct SimtConsumer {
       }
       float* orow = rec + (size_t)rec_row0 * D;
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) orow[c + v] = o[v];
+      for (int v = 0; v < VEC; ++v) orow[c + v] = o[v] * vscale;
     }
   }
 };
+
+}  // namespace pa
+
+#include "pa_decode_fp8.cuh"
+
+namespace pa {
 
 // ---------------------------------------------------------------------------
 // Segment merge across the TPH warps of each head and the output / partial
@@ -655,7 +680,7 @@ __device__ __forceinline__ void merge_split(const DecodeArgs& a, int i, int grp,
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int D, bool kBF16, int kMode, bool kSwz, bool kHi>
+template <int D, bool kBF16, int kMode, bool kSwz, bool kHi, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
@@ -873,9 +898,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= consumers =======================
-  using Consumer = typename std::conditional<kMode == kModeSimt, SimtConsumer<D, kBF16>,
-                                             MmaConsumer<D, kBF16, kSwz, kHi>>::type;
+  using Mma = typename std::conditional<kF8, MmaConsumerF8<D, kBF16, kSwz, kHi>,
+                                        MmaConsumer<D, kBF16, kSwz, kHi>>::type;
+  using Consumer =
+      typename std::conditional<kMode == kModeSimt, SimtConsumer<D, kBF16, kF8>, Mma>::type;
   Consumer cs;
+  if constexpr (kF8) cs.vscale = a.v_scale;
   float* const mbuf = reinterpret_cast<float*>(gbase + a.merge_off);
   const int slot_floats = 32 + a.G * D;
   const int hl = warp / a.TPH;                 // this warp's head within the group

@@ -10,7 +10,8 @@ struct DecodeArgs;
 
 struct DecodePlan {
   int mode;          // kModeSimt, kModeMma, kModeGather
-  bool bf16;
+  bool bf16;         // queries and output in bfloat16 (else binary16)
+  bool f8;           // the KV pools hold E4M3 codes (else the query dtype)
   bool swz;          // 128-byte swizzled staging (tensor-core reads)
   bool hi;           // group size > 8: query heads fill both MMA row halves
   bool split_rows;   // rows of a box stored as two [R][64] planes
@@ -36,5 +37,11 @@ int decode_launch_d64(const DecodePlan& p, const CUtensorMap& tk, const CUtensor
                       const DecodeArgs& a, cudaStream_t s);
 int decode_launch_d128(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        const DecodeArgs& a, cudaStream_t s);
+int decode_ctas_per_sm_f8_d64(const DecodePlan& p, int* ctas);
+int decode_ctas_per_sm_f8_d128(const DecodePlan& p, int* ctas);
+int decode_launch_f8_d64(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const DecodeArgs& a, cudaStream_t s);
+int decode_launch_f8_d128(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeArgs& a, cudaStream_t s);
 
 }  // namespace pa

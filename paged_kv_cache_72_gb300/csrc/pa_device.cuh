@@ -185,6 +185,39 @@ __device__ __forceinline__ float2 unpack2(uint32_t x) {
   }
 }
 
+// Two E4M3 codes in the low 16 bits of x (the low byte -> the low half) ->
+// f16x2.  Exact: every E4M3 value is a binary16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "r"(x));
+  return r;
+}
+
+// Two fp32 values -> two E4M3 codes (`lo` in the low byte), round to nearest
+// even, magnitudes beyond 448 saturate.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Byte select over the eight bytes {b:a} (a = bytes 0..3, b = bytes 4..7).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// A 16-byte chunk address in a TMA-swizzled shared-memory tile: the chunk
+// index (address bits 4..) is XOR-ed with address bits 7.. under kMask (7 for
+// the 128-byte swizzle, 3 for the 64-byte one, 0 for none).
+template <int kMask>
+__device__ __forceinline__ uint32_t swz16(uint32_t addr) {
+  return addr ^ (((addr >> 7) & (uint32_t)kMask) << 4);
+}
+
 // One fp32 value -> 16-bit pattern, round to nearest even.
 template <bool kBF16>
 __device__ __forceinline__ uint16_t round16(float x) {

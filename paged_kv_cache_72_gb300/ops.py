@@ -9,7 +9,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import PA_BF16, PA_DECODE_AUTO, PA_F16
+from ._lib import PA_BF16, PA_DECODE_AUTO, PA_F16, PA_FP8_E4M3
 
 
 class PAError(RuntimeError):
@@ -56,6 +56,13 @@ def _pool_shape(k_cache, v_cache):
     return k_cache.shape
 
 
+def _fp8_pools(k_cache, v_cache):
+    shape = _pool_shape(k_cache, v_cache)
+    if k_cache.dtype != torch.uint8:
+        raise TypeError("E4M3 pools must be uint8 tensors of codes")
+    return shape
+
+
 def pa_version():
     return _lib.load().pa_version()
 
@@ -99,22 +106,44 @@ def pa_cache_write(k, v, slot_mapping, k_cache, v_cache, err=None):
 
 
 def pa_copy_blocks(pairs, k_cache, v_cache, err=None):
-    """Copy pool block src -> dst (K and V) for each row (src, dst) of pairs."""
+    """Copy pool block src -> dst (K and V) for each row (src, dst) of pairs.
+
+    Pools of float16 / bfloat16 elements, or uint8 E4M3 codes."""
     L = _lib.load()
     nb, B, H, D = _pool_shape(k_cache, v_cache)
     _cuda(pairs, "pairs")
     if pairs.dtype != torch.int32:
         raise TypeError("pairs must be int32 [n, 2]")
     n = pairs.numel() // 2
+    code = PA_FP8_E4M3 if k_cache.dtype == torch.uint8 else _dtype_code(k_cache)
     _check(L.pa_copy_blocks(_ptr(pairs), n, _ptr(k_cache), _ptr(v_cache), nb, B, H, D,
-                            _dtype_code(k_cache), _ptr(err), _stream()), "pa_copy_blocks")
+                            code, _ptr(err), _stream()), "pa_copy_blocks")
+
+
+def pa_cache_write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, err=None):
+    """Quantize k[n], v[n] ([n_tok, H_kv, D], float16 / bfloat16) to E4M3 codes
+    (value / scale, round to nearest even, saturating) at pool slot
+    slot_mapping[n] of the uint8 pools."""
+    L = _lib.load()
+    nb, B, H, D = _fp8_pools(k_cache, v_cache)
+    _cuda(k, "k")
+    _cuda(v, "v")
+    _cuda(slot_mapping, "slot_mapping")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    n_tok = slot_mapping.numel()
+    if k.shape != (n_tok, H, D) or v.shape != (n_tok, H, D) or k.dtype != v.dtype:
+        raise ValueError("k, v must be [num_tokens, H_kv, D] of one dtype")
+    _check(L.pa_cache_write_fp8(_ptr(k), _ptr(v), _dtype_code(k), _ptr(slot_mapping), n_tok,
+                                _ptr(k_cache), _ptr(v_cache), nb, B, H, D, float(k_scale),
+                                float(v_scale), _ptr(err), _stream()), "pa_cache_write_fp8")
 
 
 def pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, block_size, dtype,
                              flags=PA_DECODE_AUTO, num_ctas=0):
     L = _lib.load()
     if isinstance(dtype, torch.dtype):
-        dtype = PA_F16 if dtype == torch.float16 else PA_BF16
+        dtype = {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3}[dtype]
     n = ctypes.c_size_t(0)
     _check(L.pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, block_size, dtype,
                                       flags, num_ctas, ctypes.byref(n)),
@@ -148,6 +177,37 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
                        _dtype_code(q), float(scale), _ptr(out), _ptr(workspace),
                        workspace.numel() * workspace.element_size(), int(flags), int(num_ctas),
                        _ptr(err), _stream()), "pa_decode")
+    return out
+
+
+def pa_decode_fp8(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale, v_scale, out=None,
+                  workspace=None, flags=PA_DECODE_AUTO, num_ctas=0, err=None):
+    """Paged decode over uint8 E4M3 pools (value = code * scale): out [N, Hq, D]
+    in q's dtype."""
+    L = _lib.load()
+    nb, B, H, D = _fp8_pools(k_cache, v_cache)
+    _cuda(q, "q")
+    _cuda(block_tables, "block_tables")
+    _cuda(seq_lens, "seq_lens")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    N, Hq, Dq = q.shape
+    if Dq != D:
+        raise ValueError("q must be [N, Hq, D]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != N or seq_lens.numel() != N:
+        raise ValueError("block_tables must be [N, stride] and seq_lens [N]")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = pa_decode_workspace_size(Hq, H, D, B, PA_FP8_E4M3, flags, num_ctas)
+        # zero-filled once; the decode leaves it ready for the next call
+        workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    _check(L.pa_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                           block_tables.shape[1], _ptr(seq_lens), N, Hq, H, D, B, nb,
+                           _dtype_code(q), float(scale), float(k_scale), float(v_scale),
+                           _ptr(out), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), int(flags),
+                           int(num_ctas), _ptr(err), _stream()), "pa_decode_fp8")
     return out
 
 

@@ -35,8 +35,12 @@ class GpuState:
 
     def __init__(self, wl, device="cuda"):
         self.wl = wl
-        self.k_cache = to_dev(wl.k_cache, wl.dtype, device)
-        self.v_cache = to_dev(wl.v_cache, wl.dtype, device)
+        if wl.fp8:   # uint8 E4M3 codes
+            self.k_cache = torch.from_numpy(wl.k_cache).to(device)
+            self.v_cache = torch.from_numpy(wl.v_cache).to(device)
+        else:
+            self.k_cache = to_dev(wl.k_cache, wl.dtype, device)
+            self.v_cache = to_dev(wl.v_cache, wl.dtype, device)
         self.q = to_dev(wl.q, wl.dtype, device)
         self.k_new = to_dev(wl.k_new, wl.dtype, device)
         self.v_new = to_dev(wl.v_new, wl.dtype, device)
@@ -55,12 +59,26 @@ def gpu_step(st, flags=pa.PA_DECODE_AUTO, num_ctas=0, decode=True):
         pa.pa_copy_blocks(st.pairs, st.k_cache, st.v_cache, err=st.err)
     slots = pa.pa_slot_mapping(st.block_tables, st.new_seq, st.new_pos, wl.block_size,
                                wl.num_blocks, err=st.err)
-    pa.pa_cache_write(st.k_new, st.v_new, slots, st.k_cache, st.v_cache, err=st.err)
+    if wl.fp8:
+        pa.pa_cache_write_fp8(st.k_new, st.v_new, slots, st.k_cache, st.v_cache, wl.k_scale,
+                              wl.v_scale, err=st.err)
+    else:
+        pa.pa_cache_write(st.k_new, st.v_new, slots, st.k_cache, st.v_cache, err=st.err)
     out = None
     if decode:
-        out = pa.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.seq_lens, wl.scale,
-                           flags=flags, num_ctas=num_ctas, err=st.err)
+        out = gpu_decode(st, st.seq_lens, flags=flags, num_ctas=num_ctas)
     return out, slots
+
+
+def gpu_decode(st, seq_lens, flags=pa.PA_DECODE_AUTO, num_ctas=0, workspace=None):
+    """The decode call of the workload's cache type."""
+    wl = st.wl
+    if wl.fp8:
+        return pa.pa_decode_fp8(st.q, st.k_cache, st.v_cache, st.block_tables, seq_lens,
+                                wl.scale, wl.k_scale, wl.v_scale, flags=flags,
+                                num_ctas=num_ctas, workspace=workspace, err=st.err)
+    return pa.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, seq_lens, wl.scale,
+                        flags=flags, num_ctas=num_ctas, workspace=workspace, err=st.err)
 
 
 class OracleState:
@@ -76,12 +94,21 @@ class OracleState:
         if wl.copy_pairs.size:
             oracle.copy_blocks(self.k_cache, self.v_cache, wl.copy_pairs)
         self.slots = oracle.slot_mapping(wl.block_tables, wl.new_seq, wl.new_pos, wl.block_size)
-        oracle.cache_write(self.k_cache, self.v_cache, wl.k_new, wl.v_new, self.slots)
+        if wl.fp8:
+            oracle.cache_write_fp8(self.k_cache, self.v_cache, wl.k_new, wl.v_new, wl.dtype,
+                                   self.slots, wl.k_scale, wl.v_scale)
+        else:
+            oracle.cache_write(self.k_cache, self.v_cache, wl.k_new, wl.v_new, self.slots)
 
-    def decode(self, seq_ids=None, threads=0):
+    def decode(self, seq_ids=None, threads=0, seq_lens=None):
         wl = self.wl
+        sl = wl.seq_lens if seq_lens is None else seq_lens
+        if wl.fp8:
+            return oracle.paged_decode_fp8(wl.q, self.k_cache, self.v_cache, wl.dtype, wl.k_scale,
+                                           wl.v_scale, wl.block_tables, sl, wl.scale,
+                                           seq_ids=seq_ids, threads=threads)
         return oracle.paged_decode(wl.q, self.k_cache, self.v_cache, wl.dtype, wl.block_tables,
-                                   wl.seq_lens, wl.scale, seq_ids=seq_ids, threads=threads)
+                                   sl, wl.scale, seq_ids=seq_ids, threads=threads)
 
 
 def gpu_out_f64(out):

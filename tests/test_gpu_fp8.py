@@ -1,0 +1,108 @@
+"""FP8 (E4M3) KV cache on the GPU against the fp64 oracle.
+
+The quantizing cache write must produce the oracle's codes bit for bit
+(code = e4m3(float32(x) / scale), round to nearest even, saturating); the
+decode over E4M3 pools must match the oracle's decode of the dequantized cache
+element by element within |gpu - oracle| <= 4e-3 + 1e-2 |oracle|, over
+head_dim, query dtype, group size (CUDA-core and tensor-core kernels), block
+size, ragged lengths, NaN codes in unread slots and contexts split across
+thread blocks.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_72_gb300 as pa
+import workloads as W
+from harness import GpuState, OracleState, assert_close, gpu_out_f64, gpu_step
+
+pytestmark = pytest.mark.gpu
+
+EDGE_LENS = [1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 200, 777]
+SCALES = (2.0 ** -6, 2.0 ** -6)
+
+
+def _parity(wl, flags=pa.PA_DECODE_AUTO, num_ctas=0):
+    st = GpuState(wl)
+    out, _ = gpu_step(st, flags=flags, num_ctas=num_ctas)
+    ref = OracleState(wl)
+    ref.step()
+    assert np.array_equal(st.k_cache.cpu().numpy(), ref.k_cache), "K codes differ"
+    assert np.array_equal(st.v_cache.cpu().numpy(), ref.v_cache), "V codes differ"
+    err = assert_close(gpu_out_f64(out), ref.decode(),
+                       "%s flags=%d ctas=%d" % (wl.name, flags, num_ctas))
+    assert pa.pa_get_error(st.err) == 0
+    return err
+
+
+def test_fp8_cache_write_is_bit_exact_with_saturation_and_ties(cuda_device):
+    # small scales push some values past 448 (saturation); f16 and bf16 inputs
+    for dtype, scales in ((W.BF16, (0.004, 0.0021)), (W.F16, (2.0 ** -7, 0.05))):
+        wl = W.random_workload(51, dtype, 8, 8, 128, 16, [3, 40, 129], fp8_scales=scales)
+        st = GpuState(wl)
+        gpu_step(st, decode=False)
+        ref = OracleState(wl)
+        ref.step()
+        assert np.array_equal(st.k_cache.cpu().numpy(), ref.k_cache)
+        assert np.array_equal(st.v_cache.cpu().numpy(), ref.v_cache)
+        assert pa.pa_get_error(st.err) == 0
+        # saturation did happen
+        codes = st.k_cache.cpu().numpy().reshape(-1)
+        assert np.any((codes & 0x7F) == 0x7E)
+
+
+CASES = [
+    # q dtype, Hq, Hkv, D, B
+    (W.BF16, 8, 8, 128, 16),     # G = 1: CUDA-core kernel
+    (W.F16, 4, 4, 64, 16),
+    (W.BF16, 32, 8, 128, 16),    # the Llama-3-8B shape
+    (W.F16, 8, 2, 64, 16),
+    (W.BF16, 16, 2, 128, 8),
+    (W.F16, 64, 8, 128, 16),     # G = 8
+    (W.BF16, 32, 2, 128, 32),    # G = 16: both MMA row halves
+    (W.F16, 6, 3, 64, 4),
+    (W.BF16, 12, 4, 128, 256),
+]
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,B", CASES)
+def test_fp8_decode_parity_sweep(cuda_device, dtype, Hq, Hkv, D, B):
+    wl = W.random_workload(60 + Hq + D + B, dtype, Hq, Hkv, D, B, EDGE_LENS, garbage="nan",
+                           fp8_scales=SCALES)
+    _parity(wl)
+    if Hq == Hkv:
+        _parity(wl, flags=pa.PA_DECODE_MMA)
+
+
+@pytest.mark.parametrize("num_ctas", [1, 3, 50, 1000])
+def test_fp8_split_contexts(cuda_device, num_ctas):
+    lens = [3000, 1, 64, 65, 900, 2048, 5, 4096]
+    wl = W.random_workload(71, W.BF16, 32, 8, 128, 16, lens, fp8_scales=SCALES)
+    _parity(wl, num_ctas=num_ctas)
+
+
+def test_fp8_copy_blocks_is_bit_exact(cuda_device):
+    wl = W.random_workload(72, W.BF16, 8, 2, 64, 16, [40, 70, 5], fp8_scales=SCALES)
+    st = GpuState(wl)
+    used = np.unique(wl.block_tables[wl.block_tables >= 0])
+    free = np.setdiff1d(np.arange(wl.num_blocks), used)
+    pairs = np.stack([used[:3], free[:3]], axis=1).astype(np.int32)
+    pa.pa_copy_blocks(torch.from_numpy(pairs).cuda(), st.k_cache, st.v_cache, err=st.err)
+    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    oracle.copy_blocks(kc, vc, pairs)
+    assert np.array_equal(st.k_cache.cpu().numpy(), kc)
+    assert np.array_equal(st.v_cache.cpu().numpy(), vc)
+    assert pa.pa_get_error(st.err) == 0
+
+
+def test_fp8_scales_are_checked(cuda_device):
+    wl = W.random_workload(73, W.BF16, 8, 2, 64, 16, [10], fp8_scales=SCALES)
+    st = GpuState(wl)
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_decode_fp8(st.q, st.k_cache, st.v_cache, st.block_tables, st.seq_lens, wl.scale,
+                         0.0, 1.0)
+    assert e.value.status == 1
+    with pytest.raises(pa.PAError):
+        pa.pa_decode_fp8(st.q, st.k_cache, st.v_cache, st.block_tables, st.seq_lens, wl.scale,
+                         1.0, float("nan"))
