@@ -37,8 +37,8 @@ UNIT = "seq-steps/s"
 FALLBACK_HBM_GBS = 6800.0
 DATASHEET_HBM_GBS = 7900.0   # nominal GB300 HBM3e figure, for context only
 L2_FLUSH_BYTES = 512 << 20
-KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_device.cuh", "pa_decode_variants.cuh",
-                  "pa_decode.cu"]
+KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_decode_fp8.cuh", "pa_device.cuh",
+                  "pa_decode_variants.cuh", "pa_decode.cu"]
 
 
 # --------------------------------------------------------------------------
@@ -52,17 +52,19 @@ def algorithmic_bytes(wl):
     the queries and outputs (2 * N * Hq * D * e), one block-table entry per
     used block and one length per sequence.  cache write: read the new K/V and
     write them, plus one int64 slot per token (and the two int32 inputs of the
-    slot mapping).  copy-on-write: read and write each copied block, K and V."""
+    slot mapping).  copy-on-write: read and write each copied block, K and V.
+    KV elements take wl.elem_bytes (1 for an E4M3 cache); queries, outputs and
+    the new K/V rows are 16-bit."""
     e = wl.elem_bytes
     T = wl.seq_lens.astype(np.int64)
     N = wl.num_seqs
     kv = 2 * e * wl.num_kv_heads * wl.head_dim * int(T.sum())
-    qo = 2 * N * wl.num_q_heads * wl.head_dim * e
+    qo = 2 * N * wl.num_q_heads * wl.head_dim * 2
     tables = 4 * int(sum(-(-int(t) // wl.block_size) for t in T))
     lens = 4 * N
     decode = kv + qo + tables + lens
     n_new = wl.new_seq.size
-    write = 2 * 2 * e * n_new * wl.num_kv_heads * wl.head_dim + 8 * n_new + 16 * n_new
+    write = 2 * (2 + e) * n_new * wl.num_kv_heads * wl.head_dim + 8 * n_new + 16 * n_new
     cow = 2 * 2 * wl.copy_pairs.shape[0] * wl.block_size * wl.num_kv_heads * wl.head_dim * e
     return {"decode": decode, "kv": kv, "write": write, "cow": cow, "step": decode + write + cow}
 
@@ -182,8 +184,12 @@ class Step:
         def up(bits):
             return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(td)
 
-        self.k_cache = up(wl.k_cache)
-        self.v_cache = up(wl.v_cache)
+        if wl.fp8:   # uint8 E4M3 codes
+            self.k_cache = torch.from_numpy(wl.k_cache).to(device)
+            self.v_cache = torch.from_numpy(wl.v_cache).to(device)
+        else:
+            self.k_cache = up(wl.k_cache)
+            self.v_cache = up(wl.v_cache)
         self.q = up(wl.q)
         self.k_new = up(wl.k_new)
         self.v_new = up(wl.v_new)
@@ -195,7 +201,7 @@ class Step:
         self.slots = torch.empty(wl.new_seq.size, dtype=torch.int64, device=device)
         self.out = torch.empty_like(self.q)
         nbytes = pa.pa_decode_workspace_size(wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-                                             wl.block_size, wl.dtype)
+                                             wl.block_size, W.FP8 if wl.fp8 else wl.dtype)
         self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.ev0 = torch.cuda.Event(enable_timing=True)
@@ -213,13 +219,23 @@ class Step:
             pa.pa_copy_blocks(self.pairs, self.k_cache, self.v_cache, err=self.err)
         pa.pa_slot_mapping(self.block_tables, self.new_seq, self.new_pos, wl.block_size,
                            wl.num_blocks, out=self.slots, err=self.err)
-        pa.pa_cache_write(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
-                          err=self.err)
+        if wl.fp8:
+            pa.pa_cache_write_fp8(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
+                                  wl.k_scale, wl.v_scale, err=self.err)
+        else:
+            pa.pa_cache_write(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
+                              err=self.err)
 
     def decode_phase(self):
         wl = self.wl
-        self.pa.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
-                          wl.scale, out=self.out, workspace=self.workspace, err=self.err)
+        if wl.fp8:
+            self.pa.pa_decode_fp8(self.q, self.k_cache, self.v_cache, self.block_tables,
+                                  self.seq_lens, wl.scale, wl.k_scale, wl.v_scale, out=self.out,
+                                  workspace=self.workspace, err=self.err)
+        else:
+            self.pa.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables,
+                              self.seq_lens, wl.scale, out=self.out, workspace=self.workspace,
+                              err=self.err)
 
     def run(self):
         self.write_phase()
@@ -398,9 +414,16 @@ class OracleStep:
         ids = np.arange(n, dtype=np.int32)
         mask = np.isin(wl.new_seq, ids)
         t0 = time.perf_counter()
-        o.cache_write(self.kc, self.vc, wl.k_new[mask], wl.v_new[mask], self.slots[mask])
-        o.paged_decode(wl.q, self.kc, self.vc, wl.dtype, wl.block_tables, wl.seq_lens, wl.scale,
-                       seq_ids=ids, threads=self.cores)
+        if wl.fp8:
+            o.cache_write_fp8(self.kc, self.vc, wl.k_new[mask], wl.v_new[mask], wl.dtype,
+                              self.slots[mask], wl.k_scale, wl.v_scale)
+            o.paged_decode_fp8(wl.q, self.kc, self.vc, wl.dtype, wl.k_scale, wl.v_scale,
+                               wl.block_tables, wl.seq_lens, wl.scale, seq_ids=ids,
+                               threads=self.cores)
+        else:
+            o.cache_write(self.kc, self.vc, wl.k_new[mask], wl.v_new[mask], self.slots[mask])
+            o.paged_decode(wl.q, self.kc, self.vc, wl.dtype, wl.block_tables, wl.seq_lens,
+                           wl.scale, seq_ids=ids, threads=self.cores)
         return time.perf_counter() - t0
 
     def sample_size(self, budget_s):
@@ -456,7 +479,7 @@ def run_reference(args):
 
 
 DEFAULT_SEEDS = {"tiny": 1, "llama2-7b": 2, "llama3-8b-gqa": 3, "qwen2-0.5b-shared-prefix": 4,
-                 "70b-long-context": 5}
+                 "70b-long-context": 5, "llama3-8b-gqa-fp8": 3}
 
 
 def _seed(args):
@@ -467,7 +490,7 @@ def _config(wl, args):
     return {
         "workload": wl.name, "num_seqs": wl.num_seqs, "q_heads": wl.num_q_heads,
         "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
-        "kv_dtype": W.DTYPE_NAMES[wl.dtype], "num_blocks": wl.num_blocks,
+        "kv_dtype": W.DTYPE_NAMES[W.FP8 if wl.fp8 else wl.dtype], "num_blocks": wl.num_blocks,
         "total_context_tokens": int(wl.seq_lens.sum()), "max_seq_len": wl.max_seq_len,
         "new_tokens_per_step": int(wl.new_seq.size), "copy_pairs": int(wl.copy_pairs.shape[0]),
         "seed": _seed(args), "recipe": wl.recipe,
@@ -516,7 +539,8 @@ def main():
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": W.DTYPE_NAMES[wl.dtype], "data": "synthetic", "config": _config(wl, args),
+            "dtype": "e4m3 kv, f16 mma" if wl.fp8 else W.DTYPE_NAMES[wl.dtype],
+            "data": "synthetic", "config": _config(wl, args),
             "roofline": res["roofline"], "cpu_baseline": cpu,
             "e2e": {"value": round(e2e, 1), "unit": UNIT, "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(res["e2e_ms"], 4)},

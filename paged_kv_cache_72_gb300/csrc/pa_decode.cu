@@ -66,7 +66,8 @@ int make_plan(int Hq, int Hkv, int D, int B, int kv_dtype, int q_dtype, int flag
   while (q.HG > 1 && q.HG * G > 64) q.HG /= 2;
   q.NGR = Hkv / q.HG;
   q.TPH = kCWarps / q.HG;
-  q.CT = kTile * q.TPH;
+  // tokens per warp per chunk: the E4M3 tensor-core consumer takes 32
+  q.CT = ((f8 && q.mode == kModeMma) ? kTileF8 : kTile) * q.TPH;
   q.R = B < q.CT ? B : q.CT;
   q.nsb = q.CT / q.R;
   if (q.nsb > 32) return PA_ERR_UNSUPPORTED;   // one producer lane per TMA box

@@ -271,10 +271,14 @@ struct MmaConsumer {
       const uint32_t p23 = pack2<kBF16>(exp2f(v[2] - mn), exp2f(v[3] - mn));
       const float2 f01 = unpack2<kBF16>(p01), f23 = unpack2<kBF16>(p23);
       l[hr] = l[hr] * alpha + ((f01.x + f01.y) + (f23.x + f23.y));
+      // once the running maximum settles, alpha is exactly 1 in every lane
+      // and the rescale is skipped (multiplying by 1 changes nothing)
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        o[n][hr * 2 + 0] *= alpha;
-        o[n][hr * 2 + 1] *= alpha;
+        for (int n = 0; n < NT; ++n) {
+          o[n][hr * 2 + 0] *= alpha;
+          o[n][hr * 2 + 1] *= alpha;
+        }
       }
       pa[hr] = p01;       // row gid (+8): tokens 2tig, 2tig+1
       pa[hr + 2] = p23;   // tokens 8 + 2tig, 9 + 2tig
@@ -907,7 +911,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* const mbuf = reinterpret_cast<float*>(gbase + a.merge_off);
   const int slot_floats = 32 + a.G * D;
   const int hl = warp / a.TPH;                 // this warp's head within the group
-  const int tile0 = (warp % a.TPH) * kTile;    // and its 16 tokens of every chunk
+  // tokens per warp per chunk: 32 for the E4M3 tensor-core consumer, else 16
+  constexpr int kWarpTile = (kF8 && kMode == kModeMma) ? kTileF8 : kTile;
+  const int tile0 = (warp % a.TPH) * kWarpTile;   // and its tokens of every chunk
   const uint32_t head_off = (uint32_t)hl << a.head_log2;
   const int rows = a.HG * a.G;
   Walk w = w0;
@@ -949,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = base + (uint32_t)st * a.stage_bytes;
     const uint32_t kpart = sbase + head_off, vpart = sbase + a.kv_bytes + head_off;
     const int valid_tok = min(a.CT, w.T - w.c * a.CT);
-    const int nv = max(0, min(kTile, valid_tok - tile0));
+    const int nv = max(0, min(kWarpTile, valid_tok - tile0));
     if (live && nv > 0) {
       if constexpr (kMode == kModeGather) {
         gather_tile<D, kSwz>(a, kpart, vpart, tile0, nv, w.i, w.g * a.HG + hl, w.c);

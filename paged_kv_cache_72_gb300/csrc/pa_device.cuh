@@ -195,6 +195,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
   return r;
 }
 
+// Four E4M3 codes in one word -> two f16x2: bytes 0, 1 -> lo, bytes 2, 3 ->
+// hi (each low byte -> the low half).  Exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
 // Two fp32 values -> two E4M3 codes (`lo` in the low byte), round to nearest
 // even, magnitudes beyond 448 saturate.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {

@@ -73,6 +73,9 @@ def test_host_checks_need_no_device(lib):
     assert lib.pa_decode_workspace_size(6, 4, 128, 16, 0, 0, 0, ctypes.byref(n)) == 1
     assert lib.pa_decode_workspace_size(8, 8, 128, 16, 7, 0, 0, ctypes.byref(n)) == 2
     assert lib.pa_decode_workspace_size(8, 8, 128, 16, 0, 0, 0, None) == 1
+    # an E4M3 cache whose chunk would need more than 32 TMA boxes (32 tokens
+    # per warp, one KV head per group, 4-token blocks) is refused
+    assert lib.pa_decode_workspace_size(6, 3, 64, 4, 2, 0, 0, ctypes.byref(n)) == 2
     # a grid beyond the fixed counter region is refused
     assert lib.pa_decode_workspace_size(8, 8, 128, 16, 0, 0, _lib.PA_DECODE_MAX_CTAS + 1,
                                         ctypes.byref(n)) == 1

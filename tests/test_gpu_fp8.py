@@ -61,7 +61,7 @@ CASES = [
     (W.BF16, 16, 2, 128, 8),
     (W.F16, 64, 8, 128, 16),     # G = 8
     (W.BF16, 32, 2, 128, 32),    # G = 16: both MMA row halves
-    (W.F16, 6, 3, 64, 4),
+    (W.F16, 6, 3, 64, 8),        # H_kv = 3: one KV head per group, 8 boxes a chunk
     (W.BF16, 12, 4, 128, 256),
 ]
 
