@@ -91,6 +91,12 @@ def lib():
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_double, f64p,
                                           ctypes.c_int]
         L.or_paged_decode_fp8.restype = ctypes.c_int
+        L.or_paged_decode_window.argtypes = [u16p, u16p, u16p, ctypes.c_int, i32p,
+                                             ctypes.c_int64, i32p, ctypes.c_int32, i32p,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                             f64p, ctypes.c_int]
+        L.or_paged_decode_window.restype = ctypes.c_int
         L.or_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -245,6 +251,32 @@ def paged_decode(q, k_cache, v_cache, dtype, block_tables, seq_lens, scale,
                                bt.shape[1], _p(sl, ctypes.c_int32), _p(ids, ctypes.c_int32),
                                ids.size, Hq, H_kv, D, B, float(scale),
                                _p(out, ctypes.c_double), int(threads))
+    if rc != 0:
+        raise MemoryError("oracle decode could not allocate its gather buffers")
+    return out
+
+
+def paged_decode_window(q, k_cache, v_cache, dtype, block_tables, seq_lens, window, scale,
+                        seq_ids=None, threads=0):
+    """Sliding-window decode [P1 "How does it support prompts of arbitrary
+    length? Does it have a sliding window?"]: the query of position T - 1
+    attends to tokens [max(0, T - window), T); table entries before the window
+    are never read.  window <= 0: full attention."""
+    q = _u16(q)
+    k_cache = _u16(k_cache)
+    v_cache = _u16(v_cache)
+    N, Hq, D = q.shape
+    nb, B, H_kv, D2 = k_cache.shape
+    assert D == D2 and Hq % H_kv == 0
+    bt = _i32(block_tables)
+    sl = _i32(seq_lens)
+    ids = _i32(np.arange(N) if seq_ids is None else seq_ids)
+    out = np.empty((ids.size, Hq, D), dtype=np.float64)
+    rc = lib().or_paged_decode_window(_p(q, ctypes.c_uint16), _p(k_cache, ctypes.c_uint16),
+                                      _p(v_cache, ctypes.c_uint16), int(dtype),
+                                      _p(bt, ctypes.c_int32), bt.shape[1], _p(sl, ctypes.c_int32),
+                                      int(window), _p(ids, ctypes.c_int32), ids.size, Hq, H_kv, D,
+                                      B, float(scale), _p(out, ctypes.c_double), int(threads))
     if rc != 0:
         raise MemoryError("oracle decode could not allocate its gather buffers")
     return out

@@ -260,6 +260,77 @@ int or_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* 
     return failed ? -1 : 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * Sliding-window paged decode ("vLLM Framework and Inference Engine Design",
+ * section "How does it support prompts of arbitrary length? Does it have a
+ * sliding window?": in a model trained with sliding-window attention each
+ * token attends only to the last W tokens, so only the blocks inside the
+ * window are needed and the older ones can be released).  Our reading: the
+ * query of position T - 1 attends to tokens [max(0, T - W), T); table entries
+ * of blocks wholly before the window may have been released (any value) and
+ * are never read.  W <= 0 means no window.  Arguments otherwise as
+ * or_paged_decode.
+ * ------------------------------------------------------------------------- */
+int or_paged_decode_window(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                           int dtype, const int32_t* block_tables, int64_t table_stride,
+                           const int32_t* seq_lens, int32_t window, const int32_t* seq_ids,
+                           int32_t n_ids, int32_t Hq, int32_t H_kv, int32_t D, int32_t B,
+                           double scale, double* out, int threads) {
+    int32_t G = Hq / H_kv;
+    int64_t n_work = (int64_t)n_ids * H_kv;
+    int failed = 0;
+#ifdef _OPENMP
+    if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+    for (int64_t w = 0; w < n_work; ++w) {
+        int32_t idx = (int32_t)(w / H_kv);
+        int32_t h = (int32_t)(w % H_kv);
+        int32_t i = seq_ids[idx];
+        int64_t T = seq_lens[i];
+        double* o = out + (int64_t)idx * Hq * D;
+        if (T <= 0) {
+            for (int32_t g = 0; g < G; ++g)
+                for (int32_t d = 0; d < D; ++d) o[(int64_t)(h * G + g) * D + d] = 0.0;
+            continue;
+        }
+        int64_t s0 = (window > 0 && T > window) ? T - window : 0;
+        int64_t n = T - s0;   /* tokens attended */
+        const int32_t* row = block_tables + (int64_t)i * table_stride;
+        double* K = (double*)malloc((size_t)(n * D) * sizeof(double));
+        double* V = (double*)malloc((size_t)(n * D) * sizeof(double));
+        double* s = (double*)malloc((size_t)n * sizeof(double));
+        double* qv = (double*)malloc((size_t)D * sizeof(double));
+        if (!K || !V || !s || !qv) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+            for (int64_t t = s0; t < T; ++t) {
+                int64_t slot = or_slot(row, t, B);
+                const uint16_t* kr = k_cache + (slot * H_kv + h) * (int64_t)D;
+                const uint16_t* vr = v_cache + (slot * H_kv + h) * (int64_t)D;
+                for (int32_t d = 0; d < D; ++d) {
+                    K[(t - s0) * D + d] = or_decode(kr[d], dtype);
+                    V[(t - s0) * D + d] = or_decode(vr[d], dtype);
+                }
+            }
+            for (int32_t g = 0; g < G; ++g) {
+                int32_t hq = h * G + g;
+                const uint16_t* qrow = q + ((int64_t)i * Hq + hq) * D;
+                for (int32_t d = 0; d < D; ++d) qv[d] = or_decode(qrow[d], dtype);
+                or_attention_1q(qv, K, V, n, D, scale, o + (int64_t)hq * D, s);
+            }
+        }
+        free(K);
+        free(V);
+        free(s);
+        free(qv);
+    }
+    return failed ? -1 : 0;
+}
+
 /* The same single-query attention over a contiguous (unpaged) cache
  * K[T][H_kv][D] (fp64), used to check that paging changes only the addressing
  * ("the attention kernel is the only part of the model that has to change"). */

@@ -145,6 +145,7 @@ class Workload:
     recipe: str
     shared_blocks: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))
     kv_dtype: int = -1            # FP8 for an E4M3 pool; -1: the pools hold `dtype`
+    window: int = 0               # sliding-window attention over the last `window` tokens (0: none)
     k_scale: float = 1.0          # E4M3 pools: value = e4m3(code) * scale
     v_scale: float = 1.0
 
@@ -174,11 +175,13 @@ class Workload:
         return 1 if self.fp8 else 2
 
 
-def _tables_from_lengths(lens, B, pool):
+def _tables_from_lengths(lens, B, pool, window=0):
     seqs = []
     for T in lens:
         s = Sequence(pool, B)
         s.reserve(int(T))
+        if window > 0:
+            s.release_before_window(window)
         seqs.append(s)
     stride = max([len(s.table) for s in seqs] + [1])
     bt = np.full((len(seqs), stride), -1, np.int32)
@@ -199,16 +202,18 @@ def valid_slot_mask(wl):
     mask = np.zeros((wl.num_blocks, B), bool)
     for i, T in enumerate(wl.seq_lens):
         T = int(T)
+        s0 = max(0, T - wl.window) if wl.window > 0 else 0
         nblk = -(-T // B)
-        for j in range(nblk):
+        for j in range(s0 // B, nblk):
             p = wl.block_tables[i, j]
+            lo = max(0, s0 - j * B)
             n = min(B, T - j * B)
-            mask[p, :n] = True
+            mask[p, lo:n] = True
     return mask
 
 
 def decode_workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, seed, q_sigma=1.0,
-                    kv_sigma=1.0, garbage="random", recipe="", fp8_scales=None):
+                    kv_sigma=1.0, garbage="random", recipe="", fp8_scales=None, window=0):
     """One new token per sequence at position T_i - 1, then decode.
 
     Blocks are popped, sequence by sequence and block by block, from a free
@@ -219,7 +224,7 @@ def decode_workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, seed, q_sigma
     s_perm, s_q, s_k, s_v, s_nk, s_nv = ss.spawn(6)
     free_order = np.random.default_rng(s_perm).permutation(num_blocks)
     pool = BlockPool(num_blocks, free_order)
-    bt = _tables_from_lengths(lens, B, pool)
+    bt = _tables_from_lengths(lens, B, pool, window)
     N = lens.shape[0]
     q = np.empty((N, Hq, D), np.uint16)
     _normal_bits_into(q, q_sigma, dtype, s_q)
@@ -243,6 +248,7 @@ def decode_workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, seed, q_sigma
     _normal_bits_into(v_new, kv_sigma, dtype, s_nv)
     wl = Workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, bt, q, k_cache, v_cache,
                   new_seq, new_pos, k_new, v_new, np.zeros((0, 2), np.int32), seed, recipe)
+    wl.window = int(window)
     if fp8_scales is not None:
         wl.kv_dtype = FP8
         wl.k_scale = float(np.float32(fp8_scales[0]))
@@ -313,6 +319,25 @@ def llama3_8b_fp8(seed=3, num_seqs=256, garbage="random", num_blocks=40_000):
                            recipe="llama3-8b-gqa lengths and tables; pool = random E4M3 "
                                   "codes (sign uniform, exponent field ~ round(N(12.5, "
                                   "1.2)), fraction uniform); k_scale = v_scale = 2^-7")
+
+
+def mistral_7b_swa(seed=6, num_seqs=64, lo=4_096, hi=16_384, window=4_096, garbage="random",
+                   num_blocks=20_000):
+    """Sliding-window layer of Mistral 7B v0.1 (the model and its 4,096-token
+    window are the pages' example, "How does it support prompts of arbitrary
+    length? Does it have a sliding window?"; its layer shape, 32 q heads / 8
+    KV heads / head_dim 128, is the public model card's): bf16, 16-token
+    blocks, lengths uniform in [4,096, 16,384]; every sequence keeps only the
+    blocks that reach into its window, the others are released back to the
+    pool (table entries -1), so at most ceil(W/B) + 1 = 257 blocks a sequence."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 106]))
+    lens = rng.integers(lo, hi + 1, size=num_seqs).astype(np.int32)
+    return decode_workload("mistral-7b-swa", BF16, 32, 8, 128, 16, num_blocks, lens, seed,
+                           q_sigma=1.0, kv_sigma=0.5, garbage=garbage, window=window,
+                           recipe="T ~ U[4096, 16384]; window 4096; blocks before the window "
+                                  "released to the free list (table entries -1); q ~ N(0,1), "
+                                  "k,v ~ N(0,0.25) bf16; free list = seeded permutation of "
+                                  "20,000 blocks")
 
 
 def long_context_70b(seed=5, num_seqs=32, lo=16_384, hi=32_768, garbage="random"):
@@ -386,16 +411,17 @@ def shared_prefix(seed=4, num_seqs=12, prefix=1800, suffix_hi=300, num_blocks=10
 
 
 def random_workload(seed, dtype, Hq, H_kv, D, B, lens, num_blocks=None, q_sigma=1.0,
-                    kv_sigma=1.0, garbage="random", spare_blocks=7, fp8_scales=None):
+                    kv_sigma=1.0, garbage="random", spare_blocks=7, fp8_scales=None, window=0):
     """A parity-test case of any shape: blocks scattered through a pool with
-    spare_blocks extra blocks."""
+    spare_blocks extra blocks.  With a window, blocks wholly before it are
+    released (table entries -1) once each sequence is built."""
     lens = np.asarray(lens, np.int32)
     need = int(sum(-(-int(T) // B) for T in lens))
     if num_blocks is None:
         num_blocks = need + spare_blocks
     return decode_workload("random", dtype, Hq, H_kv, D, B, num_blocks, lens, seed,
                            q_sigma=q_sigma, kv_sigma=kv_sigma, garbage=garbage,
-                           recipe="parity case", fp8_scales=fp8_scales)
+                           recipe="parity case", fp8_scales=fp8_scales, window=window)
 
 
 CONFIGS = {
@@ -405,4 +431,5 @@ CONFIGS = {
     "qwen2-0.5b-shared-prefix": shared_prefix,
     "70b-long-context": long_context_70b,
     "llama3-8b-gqa-fp8": llama3_8b_fp8,
+    "mistral-7b-swa": mistral_7b_swa,
 }

@@ -86,8 +86,20 @@ class Sequence:
         self.num_tokens = target
         return copies
 
+    def release_before_window(self, W):
+        """Sliding-window attention ("How does it support prompts of arbitrary
+        length? Does it have a sliding window?"): with each token attending
+        only to the last W, blocks wholly before the window are released; their
+        table entries become -1 (logical indices stay as they are)."""
+        first = max(0, self.num_tokens - W) // self.B   # first block still in the window
+        for j in range(min(first, len(self.table))):
+            if self.table[j] >= 0:
+                self.pool.release(self.table[j])
+                self.table[j] = -1
+
     def release(self):
         for b in self.table:
-            self.pool.release(b)
+            if b >= 0:
+                self.pool.release(b)
         self.table = []
         self.num_tokens = 0
