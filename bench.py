@@ -58,9 +58,12 @@ def algorithmic_bytes(wl):
     e = wl.elem_bytes
     T = wl.seq_lens.astype(np.int64)
     N = wl.num_seqs
-    kv = 2 * e * wl.num_kv_heads * wl.head_dim * int(T.sum())
+    # a sliding window attends to the last `window` tokens only
+    s0 = np.maximum(T - wl.window, 0) if wl.window > 0 else np.zeros_like(T)
+    kv = 2 * e * wl.num_kv_heads * wl.head_dim * int((T - s0).sum())
     qo = 2 * N * wl.num_q_heads * wl.head_dim * 2
-    tables = 4 * int(sum(-(-int(t) // wl.block_size) for t in T))
+    B = wl.block_size
+    tables = 4 * int(sum(-(-int(t) // B) - int(s) // B for t, s in zip(T, s0)))
     lens = 4 * N
     decode = kv + qo + tables + lens
     n_new = wl.new_seq.size
@@ -228,7 +231,11 @@ class Step:
 
     def decode_phase(self):
         wl = self.wl
-        if wl.fp8:
+        if wl.window > 0:
+            self.pa.pa_decode_window(self.q, self.k_cache, self.v_cache, self.block_tables,
+                                     self.seq_lens, wl.scale, wl.window, out=self.out,
+                                     workspace=self.workspace, err=self.err)
+        elif wl.fp8:
             self.pa.pa_decode_fp8(self.q, self.k_cache, self.v_cache, self.block_tables,
                                   self.seq_lens, wl.scale, wl.k_scale, wl.v_scale, out=self.out,
                                   workspace=self.workspace, err=self.err)
@@ -414,7 +421,12 @@ class OracleStep:
         ids = np.arange(n, dtype=np.int32)
         mask = np.isin(wl.new_seq, ids)
         t0 = time.perf_counter()
-        if wl.fp8:
+        if wl.window > 0:
+            o.cache_write(self.kc, self.vc, wl.k_new[mask], wl.v_new[mask], self.slots[mask])
+            o.paged_decode_window(wl.q, self.kc, self.vc, wl.dtype, wl.block_tables,
+                                  wl.seq_lens, wl.window, wl.scale, seq_ids=ids,
+                                  threads=self.cores)
+        elif wl.fp8:
             o.cache_write_fp8(self.kc, self.vc, wl.k_new[mask], wl.v_new[mask], wl.dtype,
                               self.slots[mask], wl.k_scale, wl.v_scale)
             o.paged_decode_fp8(wl.q, self.kc, self.vc, wl.dtype, wl.k_scale, wl.v_scale,
@@ -479,7 +491,7 @@ def run_reference(args):
 
 
 DEFAULT_SEEDS = {"tiny": 1, "llama2-7b": 2, "llama3-8b-gqa": 3, "qwen2-0.5b-shared-prefix": 4,
-                 "70b-long-context": 5, "llama3-8b-gqa-fp8": 3}
+                 "70b-long-context": 5, "llama3-8b-gqa-fp8": 3, "mistral-7b-swa": 6}
 
 
 def _seed(args):
@@ -493,6 +505,7 @@ def _config(wl, args):
         "kv_dtype": W.DTYPE_NAMES[W.FP8 if wl.fp8 else wl.dtype], "num_blocks": wl.num_blocks,
         "total_context_tokens": int(wl.seq_lens.sum()), "max_seq_len": wl.max_seq_len,
         "new_tokens_per_step": int(wl.new_seq.size), "copy_pairs": int(wl.copy_pairs.shape[0]),
+        "window": wl.window,
         "seed": _seed(args), "recipe": wl.recipe,
         "l2": "flushed between timed steps: a %d MiB device buffer is written, then read" %
               (L2_FLUSH_BYTES >> 20),

@@ -193,6 +193,28 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               int32_t* err_word, pa_stream stream);
 
 /*
+ * pa_decode_window -- pa_decode with sliding-window attention.
+ * [P1] "How does it support prompts of arbitrary length? Does it have a
+ * sliding window?": in a model trained with sliding-window attention each
+ * token attends only to the last W tokens, so only the blocks inside the
+ * window are needed and the older ones can be released (at most
+ * ceil(W / B) + 1 blocks per sequence).  The query of position T - 1 attends
+ * to tokens [max(0, T - window), T) (our reading of "the last W tokens").
+ *   window        >= 1 (tokens)
+ *   block_tables  logical indexing as for pa_decode; the entries of blocks
+ *                 wholly before the block that holds token max(0, T - window)
+ *                 are never read and may hold anything (a released block, -1)
+ * Every other argument, the errors and the workspace are those of pa_decode.
+ */
+int pa_decode_window(const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t dtype,
+                     float scale, int32_t window, void* out, void* workspace,
+                     size_t workspace_bytes, int32_t flags, int32_t num_ctas, int32_t* err_word,
+                     pa_stream stream);
+
+/*
  * pa_decode_fp8 -- pa_decode over E4M3 pools written by pa_cache_write_fp8.
  * Computes out = softmax(scale * q . K^T) . V with K = e4m3(code_K) * k_scale
  * and V = e4m3(code_V) * v_scale ([P1] "What is the essence of vLLM's

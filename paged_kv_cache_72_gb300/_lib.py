@@ -46,6 +46,9 @@ SIGNATURES = {
                                                 ctypes.POINTER(_sz)]),
     "pa_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i64,
                                  _i32, ctypes.c_float, _vp, _vp, _sz, _i32, _i32, _vp, _vp]),
+    "pa_decode_window": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                        _i32, _i64, _i32, ctypes.c_float, _i32, _vp, _vp, _sz,
+                                        _i32, _i32, _vp, _vp]),
     "pa_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                      _i64, _i32, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                      _vp, _vp, _sz, _i32, _i32, _vp, _vp]),

@@ -326,10 +326,10 @@ int decode_call(const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                 int32_t block_size, int64_t num_blocks, int32_t kv_dtype, int32_t q_dtype,
-                float scale, float k_scale, float v_scale, void* out, void* workspace,
-                size_t workspace_bytes, int32_t flags, int32_t num_ctas, int32_t* err_word,
-                pa_stream stream) {
-  if (num_seqs < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+                float scale, float k_scale, float v_scale, int32_t window, void* out,
+                void* workspace, size_t workspace_bytes, int32_t flags, int32_t num_ctas,
+                int32_t* err_word, pa_stream stream) {
+  if (num_seqs < 0 || table_stride < 0 || num_blocks < 0 || window < 0) return PA_ERR_INVALID_ARG;
   DecodePlan p;
   if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, q_dtype,
                            flags, num_ctas, false, &p))
@@ -361,6 +361,7 @@ int decode_call(const void* q, const void* k_cache, const void* v_cache,
   a.Hkv = num_kv_heads;
   a.scale_log2 = scale * k_scale * 1.4426950408889634f;
   a.v_scale = v_scale;
+  a.window = window;
   fill_layout(p, &a);
   return launch(p, tk, tv, a, static_cast<cudaStream_t>(stream));
 }
@@ -395,8 +396,23 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   return decode_call(q, k_cache, v_cache, block_tables, table_stride, seq_lens, num_seqs,
                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, dtype, dtype,
-                     scale, 1.f, 1.f, out, workspace, workspace_bytes, flags, num_ctas, err_word,
-                     stream);
+                     scale, 1.f, 1.f, 0, out, workspace, workspace_bytes, flags, num_ctas,
+                     err_word, stream);
+}
+
+int pa_decode_window(const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t dtype,
+                     float scale, int32_t window, void* out, void* workspace,
+                     size_t workspace_bytes, int32_t flags, int32_t num_ctas, int32_t* err_word,
+                     pa_stream stream) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (window <= 0) return PA_ERR_INVALID_ARG;
+  return decode_call(q, k_cache, v_cache, block_tables, table_stride, seq_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, dtype, dtype,
+                     scale, 1.f, 1.f, window, out, workspace, workspace_bytes, flags, num_ctas,
+                     err_word, stream);
 }
 
 int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
@@ -408,7 +424,7 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                   pa_stream stream) {
   return decode_call(q, k_cache, v_cache, block_tables, table_stride, seq_lens, num_seqs,
                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, PA_FP8_E4M3,
-                     q_dtype, scale, k_scale, v_scale, out, workspace, workspace_bytes, flags,
+                     q_dtype, scale, k_scale, v_scale, 0, out, workspace, workspace_bytes, flags,
                      num_ctas, err_word, stream);
 }
 

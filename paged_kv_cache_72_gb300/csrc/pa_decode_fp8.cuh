@@ -95,10 +95,11 @@ struct MmaConsumerF8 {
     }
   }
 
-  // 32 tokens [tile0, tile0 + 32) of the chunk; `nv` >= 1 of them are valid
-  // (the codes of the others may be anything, NaN codes included: their
-  // scores are masked and their V bytes cleared before conversion).
-  __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int nv,
+  // 32 tokens [tile0, tile0 + 32) of the chunk; tokens [lo, nv) of them are
+  // valid, lo < nv (the codes of the others may be anything, NaN codes
+  // included: their scores are masked and their V bytes cleared before
+  // conversion).
+  __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int lo, int nv,
                                        const DecodeArgs& a, float sl2) {
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     // ---- S^T = K Q^T: m-tile mt holds tokens 16 mt + gid (rows gid) and
@@ -138,7 +139,7 @@ struct MmaConsumerF8 {
     // ---- online softmax per head column (heads 8 nh + 2 tig + e): the 8
     // lanes of a tig share a head and reduce its maximum by shuffles.  The B
     // fragment of P^T for PV k-step kk is the transpose of m-tile kk's packed
-    // weights.  Token 0 of the tile is valid, so every maximum is finite.
+    // weights.  Token lo of the tile is valid, so every maximum is finite.
     uint32_t pb[2][NH][2];
 #pragma unroll
     for (int nh = 0; nh < NH; ++nh) {
@@ -149,7 +150,7 @@ struct MmaConsumerF8 {
         for (int e = 0; e < 4; ++e) {
           const int t = 16 * mt + gid + ((e >> 1) << 3);
           const float x = s[mt][nh][e] * sl2;
-          s[mt][nh][e] = (t < nv) ? x : -INFINITY;
+          s[mt][nh][e] = (t >= lo && t < nv) ? x : -INFINITY;
           mx[e & 1] = fmaxf(mx[e & 1], s[mt][nh][e]);
         }
       float alpha[2];
@@ -211,7 +212,7 @@ struct MmaConsumerF8 {
                        : "=r"(vw[r][0]), "=r"(vw[r][1])
                        : "r"(pa16));
         }
-        if (t >= nv) {
+        if (t < lo || t >= nv) {
 #pragma unroll
           for (int w = 0; w < VB / 4; ++w) vw[r][w] = 0u;
         }

@@ -86,6 +86,7 @@ struct DecodeArgs {
   int merge_off;             // byte offset of the merge buffer (TPH > 1)
   int ctrl_off;              // byte offset of barriers and control words
   float v_scale;             // E4M3 cache: V value = code * v_scale (1 otherwise)
+  int window;                // sliding window: attend to the last `window` tokens (0: all)
 };
 
 // Clamped length: invalid lengths count as 0 tokens.
@@ -93,13 +94,32 @@ __device__ __forceinline__ int clamp_len(int T, int stride, int B) {
   return (T < 0 || (long long)T > (long long)stride * B) ? 0 : T;
 }
 
+// Attended tokens of a sequence of length T: [s0, T), s0 = max(0, T - window)
+// with a sliding window ("vLLM Framework and Inference Engine Design", section
+// "How does it support prompts of arbitrary length? Does it have a sliding
+// window?": each token attends only to the last W tokens), else 0.  Chunks
+// start at t0 = s0 rounded down to a multiple of R (so that every TMA box
+// stays inside one block); the first lo = s0 - t0 < R tokens of chunk 0 are
+// masked.  Table entries of blocks wholly before t0 are never read.
+__device__ __forceinline__ int attend_origin(int T, const DecodeArgs& a) {
+  const int s0 = (a.window > 0 && T > a.window) ? T - a.window : 0;
+  return (s0 >> a.log2R) << a.log2R;
+}
+
+__device__ __forceinline__ int seq_chunks(int T, const DecodeArgs& a) {
+  return (T - attend_origin(T, a) + a.CT - 1) / a.CT;
+}
+
 struct Walk {
   int i, g, c, nc, T;   // sequence, head group, chunk, chunks of the sequence, its length
+  int t0, lo;           // first token of chunk 0, leading tokens of chunk 0 outside the window
 };
 
 __device__ __forceinline__ void walk_load_seq(Walk& w, const DecodeArgs& a) {
   w.T = clamp_len(__ldg(a.seq_lens + w.i), a.stride, a.B);
-  w.nc = (w.T + a.CT - 1) / a.CT;
+  w.t0 = attend_origin(w.T, a);
+  w.lo = (a.window > 0 && w.T > a.window) ? w.T - a.window - w.t0 : 0;
+  w.nc = (w.T - w.t0 + a.CT - 1) / a.CT;
 }
 
 __device__ __forceinline__ void walk_advance(Walk& w, const DecodeArgs& a) {
@@ -198,10 +218,11 @@ struct MmaConsumer {
     l[0] = l[1] = 0.f;
   }
 
-  // 16 tokens [tile0, tile0 + 16) of the chunk for this warp's head; `nv` of
-  // them are valid (rows past the sequence's end may hold anything, NaN
-  // included: their scores are masked and their V values zeroed in registers).
-  __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int nv,
+  // 16 tokens [tile0, tile0 + 16) of the chunk for this warp's head; tokens
+  // [lo, nv) of them are valid (rows before a sliding window or past the
+  // sequence's end may hold anything, NaN included: their scores are masked
+  // and their V values zeroed in registers).
+  __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int lo, int nv,
                                        const DecodeArgs& a, float sl2) {
     const int lane = threadIdx.x & 31, tig = lane & 3;
     // S = Q . K^T : two n-tiles of 8 tokens.  All K fragments are loaded
@@ -259,7 +280,7 @@ struct MmaConsumer {
         for (int e = 0; e < 2; ++e) {
           const int t = nt * 8 + 2 * tig + e;
           const float x = s[nt][hr * 2 + e] * sl2;
-          v[nt * 2 + e] = (t < nv) ? x : -INFINITY;
+          v[nt * 2 + e] = (t >= lo && t < nv) ? x : -INFINITY;
         }
       float mt = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
@@ -284,12 +305,12 @@ struct MmaConsumer {
       pa[hr + 2] = p23;   // tokens 8 + 2tig, 9 + 2tig
     }
     if (!kHi) { pa[1] = 0u; pa[3] = 0u; }
-    if (nv < kTile) {
-      // zero the V values of tokens past the end (the low 16 bits of a
+    if (nv < kTile || lo > 0) {
+      // zero the V values of tokens outside [lo, nv) (the low 16 bits of a
       // fragment register hold token 2tig (+8), the high bits token 2tig+1)
-      const uint32_t mlo = (2 * tig < nv ? 0x0000ffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
-      const uint32_t mhi =
-          (8 + 2 * tig < nv ? 0x0000ffffu : 0u) | (9 + 2 * tig < nv ? 0xffff0000u : 0u);
+      auto in = [&](int t) { return t >= lo && t < nv; };
+      const uint32_t mlo = (in(2 * tig) ? 0x0000ffffu : 0u) | (in(2 * tig + 1) ? 0xffff0000u : 0u);
+      const uint32_t mhi = (in(8 + 2 * tig) ? 0x0000ffffu : 0u) | (in(9 + 2 * tig) ? 0xffff0000u : 0u);
 #pragma unroll
       for (int j = 0; j < D / 16; ++j) {
         vb[j][0] &= mlo;
@@ -428,7 +449,8 @@ struct SimtConsumer {
     l = 0.f;
   }
 
-  __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int nv,
+  // tokens [lo, nv) of [tile0, tile0 + 16) are valid
+  __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int lo, int nv,
                                        const DecodeArgs& a, float sl2) {
     const int lane = threadIdx.x & 31;
     // partial dot products of the 16 tokens over this lane's head_dim slice
@@ -460,7 +482,7 @@ struct SimtConsumer {
     }
     float sc = part[0] + __shfl_xor_sync(0xffffffffu, part[0], 1);
     const int my_t = lane >> 1;
-    sc = (my_t < nv) ? sc * sl2 : -INFINITY;
+    sc = (my_t >= lo && my_t < nv) ? sc * sl2 : -INFINITY;
     float mt = sc;
 #pragma unroll
     for (int off = 2; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
@@ -471,7 +493,7 @@ struct SimtConsumer {
     l = l * alpha + ((lane & 1) ? 0.f : p);
 #pragma unroll
     for (int v = 0; v < VEC; ++v) o[v] *= alpha;
-    if (nv == kTile) {
+    if (nv == kTile && lo == 0) {
 #pragma unroll
       for (int t = 0; t < kTile; ++t) {
         const float pt = __shfl_sync(0xffffffffu, p, 2 * t);
@@ -481,7 +503,7 @@ struct SimtConsumer {
         for (int v = 0; v < VEC; ++v) o[v] = fmaf(pt, x[v], o[v]);
       }
     } else {
-      for (int t = 0; t < nv; ++t) {
+      for (int t = lo; t < nv; ++t) {
         const float pt = __shfl_sync(0xffffffffu, p, 2 * t);
         float x[VEC];
         load_row(vpart, tile0 + t, a, x);
@@ -756,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = run0; i < run1; ++i) {
     const int T0 = __ldg(a.seq_lens + i);
     const int T = clamp_len(T0, a.stride, a.B);
-    my_nc += (T + a.CT - 1) / a.CT;
+    my_nc += seq_chunks(T, a);
     if ((i % gridDim.x) == blockIdx.x) {
       if (T != T0) set_error(a.err, PA_DEVERR_SEQ_LEN);
       if (kMode != kModeGather && T == 0) {
@@ -775,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_chunks > 0 && my_nc > 0 && start >= my_excl * a.NGR && start < (my_excl + my_nc) * a.NGR) {
     long long off = my_excl * a.NGR;
     for (int i = run0; i < run1; ++i) {
-      const int nc = (clamp_len(__ldg(a.seq_lens + i), a.stride, a.B) + a.CT - 1) / a.CT;
+      const int nc = seq_chunks(clamp_len(__ldg(a.seq_lens + i), a.stride, a.B), a);
       const long long span = (long long)nc * a.NGR;
       if (nc > 0 && start < off + span) {
         const long long rem = start - off;
@@ -813,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_entry = [&](const Walk& ww) -> int {
       int ent = -1;
       if (lane < a.nsb) {
-        const int tok0 = ww.c * a.CT + lane * a.R;
+        const int tok0 = ww.t0 + ww.c * a.CT + lane * a.R;
         if (tok0 < ww.T) ent = __ldg(a.bt + (size_t)ww.i * a.stride + (tok0 >> a.log2B));
       }
       return ent;
@@ -858,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         break;
       }
-      const int valid_tok = min(a.CT, w.T - w.c * a.CT);
+      const int valid_tok = min(a.CT, w.T - w.t0 - w.c * a.CT);
       const int nvsub = (valid_tok + a.R - 1) >> a.log2R;
       const bool in_sub = lane < nvsub;
       const bool ok = in_sub && ent >= 0 && (long long)ent < a.num_blocks;
@@ -871,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (ok) {
-        const int row_off = (w.c * a.CT + lane * a.R) & (a.B - 1);
+        const int row_off = (w.t0 + w.c * a.CT + lane * a.R) & (a.B - 1);
         const uint32_t dk = sbase + (uint32_t)lane * box_bytes;
         const int h0 = w.g * a.HG;
         if (a.split_rows) {
@@ -954,13 +976,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = !__any_sync(0xffffffffu, *abort_flag != 0);
     const uint32_t sbase = base + (uint32_t)st * a.stage_bytes;
     const uint32_t kpart = sbase + head_off, vpart = sbase + a.kv_bytes + head_off;
-    const int valid_tok = min(a.CT, w.T - w.c * a.CT);
+    const int valid_tok = min(a.CT, w.T - w.t0 - w.c * a.CT);
     const int nv = max(0, min(kWarpTile, valid_tok - tile0));
-    if (live && nv > 0) {
+    // tokens of this warp's tile before the window (chunk 0 only)
+    const int lo = w.c == 0 ? max(0, w.lo - tile0) : 0;
+    if (live && nv > lo) {
       if constexpr (kMode == kModeGather) {
         gather_tile<D, kSwz>(a, kpart, vpart, tile0, nv, w.i, w.g * a.HG + hl, w.c);
       } else {
-        cs.tile(kpart, vpart, tile0, nv, a, sl2);
+        cs.tile(kpart, vpart, tile0, lo, nv, a, sl2);
       }
     }
     __syncwarp();

@@ -180,6 +180,37 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
     return out
 
 
+def pa_decode_window(q, k_cache, v_cache, block_tables, seq_lens, scale, window, out=None,
+                     workspace=None, flags=PA_DECODE_AUTO, num_ctas=0, err=None):
+    """Sliding-window decode: the query of position T - 1 attends to tokens
+    [max(0, T - window), T); table entries of blocks before the window are
+    never read (released blocks may be -1)."""
+    L = _lib.load()
+    nb, B, H, D = _pool_shape(k_cache, v_cache)
+    _cuda(q, "q")
+    _cuda(block_tables, "block_tables")
+    _cuda(seq_lens, "seq_lens")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    N, Hq, Dq = q.shape
+    if Dq != D or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [N, Hq, D] in the pool dtype")
+    if block_tables.dim() != 2 or block_tables.shape[0] != N or seq_lens.numel() != N:
+        raise ValueError("block_tables must be [N, stride] and seq_lens [N]")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = pa_decode_workspace_size(Hq, H, D, B, _dtype_code(q), flags, num_ctas)
+        workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    _check(L.pa_decode_window(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                              block_tables.shape[1], _ptr(seq_lens), N, Hq, H, D, B, nb,
+                              _dtype_code(q), float(scale), int(window), _ptr(out),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              int(flags), int(num_ctas), _ptr(err), _stream()),
+           "pa_decode_window")
+    return out
+
+
 def pa_decode_fp8(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale, v_scale, out=None,
                   workspace=None, flags=PA_DECODE_AUTO, num_ctas=0, err=None):
     """Paged decode over uint8 E4M3 pools (value = code * scale): out [N, Hq, D]

@@ -73,6 +73,10 @@ def gpu_step(st, flags=pa.PA_DECODE_AUTO, num_ctas=0, decode=True):
 def gpu_decode(st, seq_lens, flags=pa.PA_DECODE_AUTO, num_ctas=0, workspace=None):
     """The decode call of the workload's cache type."""
     wl = st.wl
+    if wl.window > 0:
+        return pa.pa_decode_window(st.q, st.k_cache, st.v_cache, st.block_tables, seq_lens,
+                                   wl.scale, wl.window, flags=flags, num_ctas=num_ctas,
+                                   workspace=workspace, err=st.err)
     if wl.fp8:
         return pa.pa_decode_fp8(st.q, st.k_cache, st.v_cache, st.block_tables, seq_lens,
                                 wl.scale, wl.k_scale, wl.v_scale, flags=flags,
@@ -103,6 +107,10 @@ class OracleState:
     def decode(self, seq_ids=None, threads=0, seq_lens=None):
         wl = self.wl
         sl = wl.seq_lens if seq_lens is None else seq_lens
+        if wl.window > 0:
+            return oracle.paged_decode_window(wl.q, self.k_cache, self.v_cache, wl.dtype,
+                                              wl.block_tables, sl, wl.window, wl.scale,
+                                              seq_ids=seq_ids, threads=threads)
         if wl.fp8:
             return oracle.paged_decode_fp8(wl.q, self.k_cache, self.v_cache, wl.dtype, wl.k_scale,
                                            wl.v_scale, wl.block_tables, sl, wl.scale,
