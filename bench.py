@@ -494,6 +494,66 @@ DEFAULT_SEEDS = {"tiny": 1, "llama2-7b": 2, "llama3-8b-gqa": 3, "qwen2-0.5b-shar
                  "70b-long-context": 5, "llama3-8b-gqa-fp8": 3, "mistral-7b-swa": 6}
 
 
+def run_swap(args):
+    """Block swap bandwidth: --swap-blocks blocks of the workload's pools out
+    to a pinned host pool and back in, one C-ABI call each way per step; the
+    link's own rate is a contiguous device -> pinned host copy of the same
+    bytes on the same stream."""
+    import torch
+    import paged_kv_cache_72_gb300 as pa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    wl = W.CONFIGS[args.workload](seed=_seed(args))
+    st = Step(wl, device)
+    used = np.unique(wl.block_tables[wl.block_tables >= 0]).astype(np.int32)
+    n = min(args.swap_blocks, used.size)
+    hk = torch.empty((n,) + tuple(st.k_cache.shape[1:]), dtype=st.k_cache.dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    out_pairs = torch.from_numpy(np.stack([used[:n], np.arange(n)], 1).astype(np.int32)).cuda()
+    in_pairs = torch.from_numpy(np.stack([np.arange(n), used[:n]], 1).astype(np.int32)).cuda()
+    nbytes = 2 * n * st.k_cache[0].numel() * st.k_cache.element_size()   # K and V, one way
+    flat = st.k_cache[:2 * n].reshape(-1) if 2 * n <= st.k_cache.shape[0] else None
+    link_host = torch.empty(nbytes // st.k_cache.element_size(),
+                            dtype=st.k_cache.dtype).pin_memory()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    t_out, t_in, t_link = [], [], []
+    for k in range(args.warmup + args.steps):
+        ev[0].record()
+        pa.pa_swap_blocks(out_pairs, st.k_cache, st.v_cache, hk, hv, err=st.err)
+        ev[1].record()
+        pa.pa_swap_blocks(in_pairs, hk, hv, st.k_cache, st.v_cache, err=st.err)
+        ev[2].record()
+        if flat is not None:
+            ev[3].record()
+            link_host.copy_(flat[:link_host.numel()], non_blocking=True)
+            ev[4].record()
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            t_out.append(ev[0].elapsed_time(ev[1]))
+            t_in.append(ev[1].elapsed_time(ev[2]))
+            if flat is not None:
+                t_link.append(ev[3].elapsed_time(ev[4]))
+    flags = pa.pa_get_error(st.err)
+    if flags:
+        raise RuntimeError("kernel reported error bits 0x%x" % flags)
+    gbs = lambda ms: nbytes / (ms * 1e-3) / 1e9
+    out_gbs, in_gbs = gbs(statistics.mean(t_out)), gbs(statistics.mean(t_in))
+    link = gbs(statistics.mean(t_link)) if t_link else None
+    line = {
+        "metric": "KV block swap GB/s (device pool <-> pinned host pool)", "value":
+        round((out_gbs + in_gbs) / 2, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "dtype": st.k_cache.dtype.__repr__(),
+        "data": "synthetic", "config": {"workload": wl.name, "blocks": n,
+                                        "bytes_each_way": nbytes},
+        "swap_out_gbs": round(out_gbs, 1), "swap_in_gbs": round(in_gbs, 1),
+        "ms_out": round(statistics.mean(t_out), 4), "ms_in": round(statistics.mean(t_in), 4),
+        "link_copy_gbs": None if link is None else round(link, 1),
+        "link_copy": "one contiguous device -> pinned host copy of the same bytes (torch copy_)",
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def _seed(args):
     return DEFAULT_SEEDS[args.workload] if args.seed is None else args.seed
 
@@ -525,11 +585,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-blocks", type=int, default=None,
                     help="smaller pool for the Llama-3-8B workload (profiling captures)")
+    ap.add_argument("--mode", default="step", choices=["step", "swap"],
+                    help="step: the decode step (default); swap: block swap bandwidth")
+    ap.add_argument("--swap-blocks", type=int, default=4096)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.mode == "swap":
+        run_swap(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

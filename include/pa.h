@@ -64,6 +64,10 @@ extern "C" {
 #define PA_DEVERR_TIMEOUT 0x10   /* a pipeline wait passed its bound; the result is invalid */
 #define PA_DEVERR_POSITION 0x20  /* slot mapping: sequence index or position outside its table */
 
+/* pa_swap_blocks directions */
+#define PA_SWAP_OUT 0   /* device pool -> host pool */
+#define PA_SWAP_IN 1    /* host pool -> device pool */
+
 /* pa_decode flags */
 #define PA_DECODE_AUTO 0
 #define PA_DECODE_SIMT 1  /* CUDA-core kernel (group size 1 only) */
@@ -118,6 +122,33 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, in
  */
 int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cache, void* v_cache,
                    int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t dtype, int32_t* err_word, pa_stream stream);
+
+/*
+ * pa_swap_blocks -- move whole blocks between the device pool and a host pool.
+ * [P3] "Memory Pressure and Preemption": swapping moves physical blocks from
+ * GPU memory to the CPU's system memory and, when GPU memory is free again,
+ * back; [P1] notes the V1 engine preempts by recomputation instead.
+ *   src_dst_pairs int32 [num_pairs][2] in device memory: (src block, dst
+ *                 block); src in the source pool, dst in the destination pool
+ *   direction     PA_SWAP_OUT: device -> host; PA_SWAP_IN: host -> device
+ *   dev_k, dev_v  device pools [dev_num_blocks][block_size][num_kv_heads][head_dim]
+ *   host_k, host_v  host pools of the same block shape that the GPU can
+ *                 address: pinned, mapped memory (cudaHostAlloc /
+ *                 cudaMallocHost), or, on a node whose GPU reads pageable host
+ *                 memory through the host's page tables (a Grace-Blackwell
+ *                 node over NVLink-C2C), any host memory; memory that
+ *                 cudaHostGetDevicePointer cannot translate returns
+ *                 PA_ERR_INVALID_ARG
+ *   dtype         PA_F16, PA_BF16 or PA_FP8_E4M3 (1-byte codes)
+ * One kernel launch copies every pair (K and V), bit-exact, reading or
+ * writing the host pool through its mapped device address.  A pair out of
+ * range, or a dst that appears twice, sets PA_DEVERR_COPY_PAIR and is not
+ * copied.  Stream-ordered like every call.
+ */
+int pa_swap_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, int32_t direction,
+                   void* dev_k, void* dev_v, int64_t dev_num_blocks, void* host_k, void* host_v,
+                   int64_t host_num_blocks, int32_t block_size, int32_t num_kv_heads,
                    int32_t head_dim, int32_t dtype, int32_t* err_word, pa_stream stream);
 
 /*

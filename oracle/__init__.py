@@ -97,6 +97,7 @@ def lib():
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
                                              f64p, ctypes.c_int]
         L.or_paged_decode_window.restype = ctypes.c_int
+        L.or_swap_blocks.argtypes = [u8p, u8p, u8p, u8p, i32p, ctypes.c_int64, ctypes.c_int64]
         L.or_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -186,6 +187,20 @@ def copy_blocks(k_cache, v_cache, pairs):
     blk = k_cache.shape[1] * k_cache.shape[2] * k_cache.shape[3]
     lib().or_copy_blocks(_p(k_cache, ctypes.c_uint16), _p(v_cache, ctypes.c_uint16),
                          _p(pr, ctypes.c_int32), pr.shape[0], blk)
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs):
+    """In place: destination pool block dst <- source pool block src, K and V,
+    for each (src, dst) pair (pools of any element type, same block shape)."""
+    for a in (src_k, src_v, dst_k, dst_v):
+        assert a.flags.c_contiguous
+    assert src_k.shape[1:] == dst_k.shape[1:] and src_k.dtype == dst_k.dtype
+    pr = _i32(pairs).reshape(-1, 2)
+    block_bytes = src_k[0].nbytes
+    u8 = ctypes.c_uint8
+    lib().or_swap_blocks(_p(src_k.view(np.uint8), u8), _p(src_v.view(np.uint8), u8),
+                         _p(dst_k.view(np.uint8), u8), _p(dst_v.view(np.uint8), u8),
+                         _p(pr, ctypes.c_int32), pr.shape[0], block_bytes)
 
 
 def gather_bits(cache, table_row, T):

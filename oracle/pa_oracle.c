@@ -143,6 +143,23 @@ void or_copy_blocks(uint16_t* k_cache, uint16_t* v_cache,
     }
 }
 
+/* ---------------------------------------------------------------------------
+ * Block swap between two pools ("vLLM anatomy" / [P3] "Memory Pressure and
+ * Preemption": swapping moves physical blocks from GPU memory to the CPU's
+ * memory and back): block dst of the destination pool <- block src of the
+ * source pool, K and V, for each (src, dst) pair, in order.  block_bytes is
+ * the size of one block of one pool.
+ * ------------------------------------------------------------------------- */
+void or_swap_blocks(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k, uint8_t* dst_v,
+                    const int32_t* pairs, int64_t n, int64_t block_bytes) {
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t src = pairs[2 * i];
+        int64_t dst = pairs[2 * i + 1];
+        memcpy(dst_k + dst * block_bytes, src_k + src * block_bytes, (size_t)block_bytes);
+        memcpy(dst_v + dst * block_bytes, src_v + src * block_bytes, (size_t)block_bytes);
+    }
+}
+
 /* Gather the first T tokens of one sequence, one KV head, into a contiguous
  * fp64 array out[T][D] by following the block table token by token. */
 void or_gather_head(const uint16_t* cache, int dtype, const int32_t* table_row,

@@ -23,6 +23,8 @@ PA_DEVERR_SEQ_LEN = 0x4
 PA_DEVERR_COPY_PAIR = 0x8
 PA_DEVERR_TIMEOUT = 0x10
 PA_DEVERR_POSITION = 0x20
+PA_SWAP_OUT = 0
+PA_SWAP_IN = 1
 PA_DECODE_AUTO = 0
 PA_DECODE_SIMT = 1
 PA_DECODE_MMA = 2
@@ -40,6 +42,8 @@ SIGNATURES = {
     "pa_cache_write": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _i32,
                                       _vp, _vp]),
     "pa_copy_blocks": (ctypes.c_int, [_vp, _i32, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pa_swap_blocks": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32,
+                                      _i32, _i32, _vp, _vp]),
     "pa_cache_write_fp8": (ctypes.c_int, [_vp, _vp, _i32, _vp, _i64, _vp, _vp, _i64, _i32, _i32,
                                           _i32, ctypes.c_float, ctypes.c_float, _vp, _vp]),
     "pa_decode_workspace_size": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32, _i32,

@@ -138,6 +138,40 @@ __global__ void copy_blocks_kernel(const int32_t* __restrict__ pairs, int num_pa
   for (int e = threadIdx.x; e < vecs_per_block; e += blockDim.x) d[e] = s[e];
 }
 
+// Block swap between the device pool and a pinned host pool ("vLLM anatomy",
+// section "Memory Pressure and Preemption": swapping moves physical blocks from
+// GPU memory to the CPU's memory and back).  One CTA per (pair, K or V) copies
+// a block in 16-byte vectors; the host pool is addressed through its mapped
+// device address, so any number of blocks moves in one launch (over
+// NVLink-C2C on a Grace-Blackwell node).  A pair is copied only if both
+// blocks are in range and its dst appears once among the dsts.
+__global__ void swap_blocks_kernel(const int32_t* __restrict__ pairs, int num_pairs,
+                                   long long src_blocks, long long dst_blocks, int vecs_per_block,
+                                   const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
+                                   uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                                   int32_t* err) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int p = blockIdx.x;
+  const int which = blockIdx.y;  // 0 = K, 1 = V
+  const int src = pairs[2 * p], dst = pairs[2 * p + 1];
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  int mine = (src < 0 || (long long)src >= src_blocks || dst < 0 || (long long)dst >= dst_blocks);
+  for (int j = threadIdx.x; j < num_pairs && !mine; j += blockDim.x)
+    if (j != p && pairs[2 * j + 1] == dst) mine = 1;
+  if (mine) atomicOr(&bad, 1);
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0 && which == 0) set_error(err, PA_DEVERR_COPY_PAIR);
+    return;
+  }
+  const uint4* s = (which ? src_v : src_k) + (long long)src * vecs_per_block;
+  uint4* d = (which ? dst_v : dst_k) + (long long)dst * vecs_per_block;
+  for (int e = threadIdx.x; e < vecs_per_block; e += blockDim.x) d[e] = s[e];
+}
+
 static bool shape_ok(int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
                      bool allow_fp8 = false) {
   return (head_dim == 64 || head_dim == 128) && num_kv_heads > 0 && is_pow2(block_size) &&
@@ -217,6 +251,42 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
                                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                   err_word),
                        "block copy launch");
+}
+
+int pa_swap_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, int32_t direction,
+                   void* dev_k, void* dev_v, int64_t dev_num_blocks, void* host_k, void* host_v,
+                   int64_t host_num_blocks, int32_t block_size, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t dtype, int32_t* err_word, pa_stream stream) {
+  if (num_pairs < 0 || dev_num_blocks < 0 || host_num_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (direction != PA_SWAP_OUT && direction != PA_SWAP_IN) return PA_ERR_INVALID_ARG;
+  if (!shape_ok(block_size, num_kv_heads, head_dim, dtype, true)) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (num_pairs > 65535) return PA_ERR_INVALID_ARG;
+  if (!src_dst_pairs || !dev_k || !dev_v || !host_k || !host_v) return PA_ERR_INVALID_ARG;
+  if (!aligned16(dev_k) || !aligned16(dev_v) || !aligned16(host_k) || !aligned16(host_v))
+    return PA_ERR_INVALID_ARG;
+  // the device-side addresses of the host pool (pinned and mapped memory, or
+  // pageable memory where the GPU reads the host's page tables)
+  void* hk = nullptr;
+  void* hv = nullptr;
+  if (cudaHostGetDevicePointer(&hk, host_k, 0) != cudaSuccess ||
+      cudaHostGetDevicePointer(&hv, host_v, 0) != cudaSuccess) {
+    cudaGetLastError();   // not addressable from the GPU: the caller's error, not a sticky one
+    return PA_ERR_INVALID_ARG;
+  }
+  const int eb = dtype == PA_FP8_E4M3 ? 1 : 2;
+  const long long vecs = (long long)block_size * num_kv_heads * head_dim * eb / 16;
+  if (vecs > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  const bool out = direction == PA_SWAP_OUT;
+  clear_stale_error();
+  const cudaError_t e = launch_pdl(
+      swap_blocks_kernel, dim3((unsigned)num_pairs, 2), dim3(256), 0,
+      static_cast<cudaStream_t>(stream), src_dst_pairs, (int)num_pairs,
+      (long long)(out ? dev_num_blocks : host_num_blocks),
+      (long long)(out ? host_num_blocks : dev_num_blocks), (int)vecs,
+      static_cast<const uint4*>(out ? dev_k : hk), static_cast<const uint4*>(out ? dev_v : hv),
+      static_cast<uint4*>(out ? hk : dev_k), static_cast<uint4*>(out ? hv : dev_v), err_word);
+  return launch_status(e, "block swap launch");
 }
 
 int pa_cache_write_fp8(const void* k, const void* v, int32_t src_dtype,

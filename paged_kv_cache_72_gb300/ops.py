@@ -9,7 +9,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import PA_BF16, PA_DECODE_AUTO, PA_F16, PA_FP8_E4M3
+from ._lib import PA_BF16, PA_DECODE_AUTO, PA_F16, PA_FP8_E4M3, PA_SWAP_IN, PA_SWAP_OUT
 
 
 class PAError(RuntimeError):
@@ -118,6 +118,36 @@ def pa_copy_blocks(pairs, k_cache, v_cache, err=None):
     code = PA_FP8_E4M3 if k_cache.dtype == torch.uint8 else _dtype_code(k_cache)
     _check(L.pa_copy_blocks(_ptr(pairs), n, _ptr(k_cache), _ptr(v_cache), nb, B, H, D,
                             code, _ptr(err), _stream()), "pa_copy_blocks")
+
+
+def pa_swap_blocks(pairs, src_k, src_v, dst_k, dst_v, err=None):
+    """Copy block src of the source pools to block dst of the destination
+    pools for each row (src, dst) of pairs: one pool pair on the GPU, the other
+    in host memory the GPU can address (pinned; or any host memory where the
+    GPU reads the host's page tables).  The direction follows from which is
+    which."""
+    L = _lib.load()
+    _cuda(pairs, "pairs")
+    if pairs.dtype != torch.int32:
+        raise TypeError("pairs must be int32 [n, 2]")
+    if src_k.is_cuda == dst_k.is_cuda:
+        raise ValueError("one pool pair must be on the GPU and the other in pinned host memory")
+    dev_k, dev_v, host_k, host_v = (src_k, src_v, dst_k, dst_v) if src_k.is_cuda else \
+        (dst_k, dst_v, src_k, src_v)
+    for t in (host_k, host_v):
+        if not t.is_contiguous():
+            raise ValueError("the host pools must be contiguous")
+    _pool_shape(dev_k, dev_v)
+    if host_k.shape[1:] != dev_k.shape[1:] or host_k.dtype != dev_k.dtype or \
+            host_v.shape != host_k.shape or host_v.dtype != host_k.dtype:
+        raise ValueError("host and device pools must share the block shape and dtype")
+    nbd, B, H, D = dev_k.shape
+    code = PA_FP8_E4M3 if dev_k.dtype == torch.uint8 else _dtype_code(dev_k)
+    direction = PA_SWAP_OUT if src_k.is_cuda else PA_SWAP_IN
+    _check(L.pa_swap_blocks(_ptr(pairs), pairs.numel() // 2, direction, _ptr(dev_k), _ptr(dev_v),
+                            nbd, ctypes.c_void_p(host_k.data_ptr()),
+                            ctypes.c_void_p(host_v.data_ptr()), host_k.shape[0], B, H, D, code,
+                            _ptr(err), _stream()), "pa_swap_blocks")
 
 
 def pa_cache_write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, err=None):

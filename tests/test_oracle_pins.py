@@ -15,6 +15,7 @@ import pytest
 import scipy.special
 
 import oracle
+import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_worked_examples.json")
 
@@ -400,3 +401,29 @@ def test_capacity_example(golden):
 def test_sliding_window_bound(golden):
     g = golden["sliding_window"]
     assert oracle.sliding_window_max_blocks(g["window"], g["block_size"]) == g["max_blocks"]
+
+
+def test_swap_blocks_moves_whole_blocks_and_round_trips():
+    # "Swapping moves physical blocks from the GPU memory to the CPU's system
+    # memory ... the engine swaps the blocks back": a block swapped out and
+    # back into another block holds the same bits, and the decode through a
+    # table that points at the new blocks does not change
+    wl = W.random_workload(61, W.BF16, 8, 2, 64, 16, [40, 70], num_blocks=20)
+    host_k = np.zeros((10,) + wl.k_cache.shape[1:], np.uint16)
+    host_v = np.zeros_like(host_k)
+    used = np.unique(wl.block_tables[wl.block_tables >= 0])
+    out_pairs = np.stack([used, np.arange(used.size)], axis=1)
+    oracle.swap_blocks(wl.k_cache, wl.v_cache, host_k, host_v, out_pairs)
+    assert np.array_equal(host_k[:used.size], wl.k_cache[used])
+    assert np.array_equal(host_v[:used.size], wl.v_cache[used])
+    assert not host_k[used.size:].any()
+    kc = np.zeros_like(wl.k_cache)
+    vc = np.zeros_like(wl.v_cache)
+    free = np.setdiff1d(np.arange(wl.num_blocks), used)[::-1][:used.size]
+    oracle.swap_blocks(host_k, host_v, kc, vc, np.stack([np.arange(used.size), free], axis=1))
+    remap = dict(zip(used.tolist(), free.tolist()))
+    bt = np.vectorize(lambda b: remap.get(int(b), -1))(wl.block_tables).astype(np.int32)
+    a = oracle.paged_decode(wl.q, wl.k_cache, wl.v_cache, wl.dtype, wl.block_tables,
+                            wl.seq_lens, wl.scale)
+    b = oracle.paged_decode(wl.q, kc, vc, wl.dtype, bt, wl.seq_lens, wl.scale)
+    assert np.array_equal(a, b)
