@@ -98,6 +98,11 @@ def lib():
                                              f64p, ctypes.c_int]
         L.or_paged_decode_window.restype = ctypes.c_int
         L.or_swap_blocks.argtypes = [u8p, u8p, u8p, u8p, i32p, ctypes.c_int64, ctypes.c_int64]
+        L.or_paged_prefill.argtypes = [u16p, u16p, u16p, ctypes.c_int, i32p, ctypes.c_int64,
+                                       i32p, i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_double, f64p,
+                                       ctypes.c_int]
+        L.or_paged_prefill.restype = ctypes.c_int
         L.or_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -294,6 +299,33 @@ def paged_decode_window(q, k_cache, v_cache, dtype, block_tables, seq_lens, wind
                                       B, float(scale), _p(out, ctypes.c_double), int(threads))
     if rc != 0:
         raise MemoryError("oracle decode could not allocate its gather buffers")
+    return out
+
+
+def paged_prefill(q, k_cache, v_cache, dtype, block_tables, seq_lens, query_start, scale,
+                  threads=0):
+    """Multi-query paged attention (chunked prefill; decode is L_i = 1):
+    fp64 out [total_q, Hq, D].  Sequence i's new tokens are q rows
+    [query_start[i], query_start[i+1]), sitting at the end of its seq_lens[i]
+    cached tokens; token j of them attends causally to [0, T_i - L_i + j]."""
+    q = _u16(q)
+    k_cache = _u16(k_cache)
+    v_cache = _u16(v_cache)
+    total, Hq, D = q.shape
+    nb, B, H_kv, D2 = k_cache.shape
+    assert D == D2 and Hq % H_kv == 0
+    bt = _i32(block_tables)
+    sl = _i32(seq_lens)
+    qs = _i32(query_start)
+    assert qs.size == sl.size + 1 and qs[-1] == total
+    out = np.zeros((total, Hq, D), dtype=np.float64)
+    rc = lib().or_paged_prefill(_p(q, ctypes.c_uint16), _p(k_cache, ctypes.c_uint16),
+                                _p(v_cache, ctypes.c_uint16), int(dtype), _p(bt, ctypes.c_int32),
+                                bt.shape[1], _p(sl, ctypes.c_int32), _p(qs, ctypes.c_int32),
+                                sl.size, Hq, H_kv, D, B, float(scale), _p(out, ctypes.c_double),
+                                int(threads))
+    if rc != 0:
+        raise MemoryError("oracle prefill could not allocate its gather buffers")
     return out
 
 

@@ -348,6 +348,68 @@ int or_paged_decode_window(const uint16_t* q, const uint16_t* k_cache, const uin
     return failed ? -1 : 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * Multi-query paged attention for chunked prefill and prefix-cache hits
+ * ("vLLM Framework and Inference Engine Design", section "How does it support
+ * prompts of arbitrary length?": a long prompt is processed in chunks, mixed
+ * with other requests' decode tokens in one batch; "vLLM self-hosted", section
+ * "Two phases: prefill and decode").  Sequence i has L_i = query_start[i + 1] -
+ * query_start[i] new tokens, already written to the cache, at the end of its
+ * seq_lens[i] tokens; new token j sits at position p = seq_lens[i] - L_i + j
+ * and attends causally to tokens [0, p] through the block table.  Decode is
+ * the case L_i = 1.
+ *   q, out   [total_q][Hq][D] (q 16-bit in dtype, out fp64), rows of sequence
+ *            i at [query_start[i], query_start[i + 1])
+ * ------------------------------------------------------------------------- */
+int or_paged_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                     int dtype, const int32_t* block_tables, int64_t table_stride,
+                     const int32_t* seq_lens, const int32_t* query_start, int32_t num_seqs,
+                     int32_t Hq, int32_t H_kv, int32_t D, int32_t B, double scale,
+                     double* out, int threads) {
+    int32_t G = Hq / H_kv;
+    int64_t n_work = (int64_t)num_seqs * H_kv;
+    int failed = 0;
+#ifdef _OPENMP
+    if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+    for (int64_t w = 0; w < n_work; ++w) {
+        int32_t i = (int32_t)(w / H_kv);
+        int32_t h = (int32_t)(w % H_kv);
+        int64_t T = seq_lens[i];
+        int64_t q0 = query_start[i], L = query_start[i + 1] - q0;
+        if (L <= 0 || T <= 0 || L > T) continue;
+        const int32_t* row = block_tables + (int64_t)i * table_stride;
+        double* K = (double*)malloc((size_t)(T * D) * sizeof(double));
+        double* V = (double*)malloc((size_t)(T * D) * sizeof(double));
+        double* s = (double*)malloc((size_t)T * sizeof(double));
+        double* qv = (double*)malloc((size_t)D * sizeof(double));
+        if (!K || !V || !s || !qv) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+            or_gather_head(k_cache, dtype, row, T, B, H_kv, D, h, K);
+            or_gather_head(v_cache, dtype, row, T, B, H_kv, D, h, V);
+            for (int64_t j = 0; j < L; ++j) {
+                int64_t p = T - L + j;   /* the token's position: it sees [0, p] */
+                for (int32_t g = 0; g < G; ++g) {
+                    int32_t hq = h * G + g;
+                    const uint16_t* qrow = q + ((q0 + j) * Hq + hq) * D;
+                    for (int32_t d = 0; d < D; ++d) qv[d] = or_decode(qrow[d], dtype);
+                    or_attention_1q(qv, K, V, p + 1, D, scale, out + ((q0 + j) * Hq + hq) * D, s);
+                }
+            }
+        }
+        free(K);
+        free(V);
+        free(s);
+        free(qv);
+    }
+    return failed ? -1 : 0;
+}
+
 /* The same single-query attention over a contiguous (unpaged) cache
  * K[T][H_kv][D] (fp64), used to check that paging changes only the addressing
  * ("the attention kernel is the only part of the model that has to change"). */

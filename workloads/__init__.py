@@ -146,6 +146,9 @@ class Workload:
     shared_blocks: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))
     kv_dtype: int = -1            # FP8 for an E4M3 pool; -1: the pools hold `dtype`
     window: int = 0               # sliding-window attention over the last `window` tokens (0: none)
+    # multi-query steps (chunked prefill): q holds every new token's rows
+    # [total_q, Hq, D]; sequence i's are rows [query_start[i], query_start[i+1])
+    query_start: np.ndarray = None
     k_scale: float = 1.0          # E4M3 pools: value = e4m3(code) * scale
     v_scale: float = 1.0
 
@@ -410,6 +413,74 @@ def shared_prefix(seed=4, num_seqs=12, prefix=1800, suffix_hi=300, num_blocks=10
     return wl
 
 
+def prefill_workload(name, dtype, Hq, H_kv, D, B, num_blocks, prefix_lens, chunk_lens, seed,
+                     q_sigma=1.0, kv_sigma=1.0, garbage="random", recipe=""):
+    """A chunked-prefill step ("vLLM Framework and Inference Engine Design",
+    "How does it support prompts of arbitrary length?": a long prompt is
+    processed in chunks, with other requests' decode tokens in the same batch):
+    sequence i holds prefix_lens[i] cached tokens and brings chunk_lens[i] >= 1
+    new tokens (1 = a decode token).  The step writes the new tokens' K/V at
+    positions prefix_lens[i] .. prefix_lens[i] + chunk_lens[i] - 1, then every
+    new token's query attends causally through the block table."""
+    prefix_lens = np.asarray(prefix_lens, np.int32)
+    chunk_lens = np.asarray(chunk_lens, np.int32)
+    assert np.all(chunk_lens >= 1) and np.all(prefix_lens >= 0)
+    lens = prefix_lens + chunk_lens
+    ss = np.random.SeedSequence(seed)
+    s_perm, s_q, s_k, s_v, s_nk, s_nv = ss.spawn(6)
+    free_order = np.random.default_rng(s_perm).permutation(num_blocks)
+    pool = BlockPool(num_blocks, free_order)
+    bt = _tables_from_lengths(lens, B, pool)
+    total = int(chunk_lens.sum())
+    q = np.empty((total, Hq, D), np.uint16)
+    _normal_bits_into(q, q_sigma, dtype, s_q)
+    k_cache = np.zeros((num_blocks, B, H_kv, D), np.uint16)
+    v_cache = np.zeros((num_blocks, B, H_kv, D), np.uint16)
+    used = bt[bt >= 0]
+    _normal_bits_into(k_cache, kv_sigma, dtype, s_k, rows=used)
+    _normal_bits_into(v_cache, kv_sigma, dtype, s_v, rows=used)
+    new_seq = np.repeat(np.arange(lens.size, dtype=np.int32), chunk_lens)
+    new_pos = np.concatenate([np.arange(p, p + c, dtype=np.int32)
+                              for p, c in zip(prefix_lens, chunk_lens)])
+    k_new = np.empty((total, H_kv, D), np.uint16)
+    v_new = np.empty((total, H_kv, D), np.uint16)
+    _normal_bits_into(k_new, kv_sigma, dtype, s_nk)
+    _normal_bits_into(v_new, kv_sigma, dtype, s_nv)
+    wl = Workload(name, dtype, Hq, H_kv, D, B, num_blocks, lens, bt, q, k_cache, v_cache,
+                  new_seq, new_pos, k_new, v_new, np.zeros((0, 2), np.int32), seed, recipe)
+    wl.query_start = np.concatenate([[0], np.cumsum(chunk_lens)]).astype(np.int32)
+    if garbage == "nan":
+        _garbage_fill(k_cache, v_cache, valid_slot_mask(wl), dtype)
+    return wl
+
+
+def random_prefill(seed, dtype, Hq, H_kv, D, B, prefix_lens, chunk_lens, spare_blocks=7,
+                   garbage="random"):
+    """A chunked-prefill parity case of any shape."""
+    lens = np.asarray(prefix_lens) + np.asarray(chunk_lens)
+    need = int(sum(-(-int(T) // B) for T in lens))
+    return prefill_workload("random-prefill", dtype, Hq, H_kv, D, B, need + spare_blocks,
+                            prefix_lens, chunk_lens, seed, garbage=garbage, recipe="parity case")
+
+
+def llama3_8b_chunked_prefill(seed=7, num_seqs=16, chunk=512, garbage="random",
+                              num_blocks=8_000):
+    """Llama-3-8B GQA layer (32 q / 8 KV heads, head_dim 128, bf16, block 16),
+    a chunked-prefill step: 16 prompts each bring a 512-token chunk (an 8,192-
+    token step budget) on top of lognormal cached prefixes (median about 1,300
+    tokens, clipped to [0, 6,144]) -- a long prompt's later chunks or a
+    prefix-cache hit."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 107]))
+    prefix = np.clip(np.rint(rng.lognormal(np.log(1300), 0.8, size=num_seqs)), 0,
+                     6144).astype(np.int32)
+    chunks = np.full(num_seqs, chunk, np.int32)
+    return prefill_workload("llama3-8b-chunked-prefill", BF16, 32, 8, 128, 16, num_blocks,
+                            prefix, chunks, seed, kv_sigma=0.5, garbage=garbage,
+                            recipe="16 sequences x 512-token chunks on lognormal(ln 1300, 0.8) "
+                                   "prefixes clipped to [0, 6144]; q ~ N(0,1), k,v ~ N(0,0.25) "
+                                   "bf16; 8,000-block pool")
+
+
 def random_workload(seed, dtype, Hq, H_kv, D, B, lens, num_blocks=None, q_sigma=1.0,
                     kv_sigma=1.0, garbage="random", spare_blocks=7, fp8_scales=None, window=0):
     """A parity-test case of any shape: blocks scattered through a pool with
@@ -432,4 +503,5 @@ CONFIGS = {
     "70b-long-context": long_context_70b,
     "llama3-8b-gqa-fp8": llama3_8b_fp8,
     "mistral-7b-swa": mistral_7b_swa,
+    "llama3-8b-chunked-prefill": llama3_8b_chunked_prefill,
 }
