@@ -35,6 +35,7 @@ import workloads as W  # noqa: E402
 METRIC = "Paged decode attention: achieved HBM GB/s vs GB300 peak; seq-steps/sec"
 UNIT = "seq-steps/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 DATASHEET_HBM_GBS = 7900.0   # nominal GB300 HBM3e figure, for context only
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_decode_fp8.cuh", "pa_device.cuh",
@@ -65,6 +66,8 @@ def algorithmic_bytes(wl):
     B = wl.block_size
     tables = 4 * int(sum(-(-int(t) // B) - int(s) // B for t, s in zip(T, s0)))
     lens = 4 * N
+    if wl.query_start is not None:
+        qo = 2 * int(wl.query_start[-1]) * wl.num_q_heads * wl.head_dim * 2
     decode = kv + qo + tables + lens
     n_new = wl.new_seq.size
     write = 2 * (2 + e) * n_new * wl.num_kv_heads * wl.head_dim + 8 * n_new + 16 * n_new
@@ -72,13 +75,26 @@ def algorithmic_bytes(wl):
     return {"decode": decode, "kv": kv, "write": write, "cow": cow, "step": decode + write + cow}
 
 
-def measured_peaks():
+def prefill_flops(wl):
+    """Tensor-core work of a multi-query step, causal: every new token at
+    position p scores and weights p + 1 keys, 2 D flops each for Q.K^T and
+    for P.V, over all query heads."""
+    qs = wl.query_start
+    keys = 0
+    for i, T in enumerate(wl.seq_lens.astype(np.int64)):
+        L = int(qs[i + 1] - qs[i])
+        first = int(T) - L + 1   # keys seen by the first new token
+        keys += L * first + L * (L - 1) // 2
+    return 4 * wl.head_dim * wl.num_q_heads * keys
+
+
+def measured_peaks(key="hbm_gbs"):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d[key]), "measured"
+    return (FALLBACK_HBM_GBS if key == "hbm_gbs" else FALLBACK_BF16_TFLOPS), "fallback"
 
 
 def kernel_sha():
@@ -207,6 +223,9 @@ class Step:
                                              wl.block_size, W.FP8 if wl.fp8 else wl.dtype)
         self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.query_start = (None if wl.query_start is None
+                            else torch.from_numpy(wl.query_start).to(device))
+        self.pf_ws = torch.zeros(256, dtype=torch.uint8, device=device)
         self.ev0 = torch.cuda.Event(enable_timing=True)
         self.ev1 = torch.cuda.Event(enable_timing=True)
         self.decode_ms = []
@@ -231,7 +250,11 @@ class Step:
 
     def decode_phase(self):
         wl = self.wl
-        if wl.window > 0:
+        if wl.query_start is not None:
+            self.pa.pa_prefill(self.q, self.k_cache, self.v_cache, self.block_tables,
+                               self.seq_lens, self.query_start, wl.scale, out=self.out,
+                               workspace=self.pf_ws, err=self.err)
+        elif wl.window > 0:
             self.pa.pa_decode_window(self.q, self.k_cache, self.v_cache, self.block_tables,
                                      self.seq_lens, wl.scale, wl.window, out=self.out,
                                      workspace=self.workspace, err=self.err)
@@ -330,6 +353,8 @@ def run_gpu(args, rank, world, local_rank):
         "seq_lens": st.seq_lens.cpu().pin_memory(), "new_seq": st.new_seq.cpu().pin_memory(),
         "new_pos": st.new_pos.cpu().pin_memory(), "pairs": st.pairs.cpu().pin_memory(),
     }
+    if st.query_start is not None:
+        host["query_start"] = st.query_start.cpu().pin_memory()
     out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -352,6 +377,25 @@ def run_gpu(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     achieved = nbytes["decode"] / (dms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
+    if wl.query_start is not None:
+        # a dense contraction: its roofline is the tensor rate (the kernel
+        # timed alone: the burst figure)
+        flops = prefill_flops(wl)
+        tpeak, tkind = measured_peaks("bf16_tflops")
+        tach = flops / (dms * 1e-3) / 1e12
+        roof = {
+            "bound": "tensor", "achieved": round(tach, 1), "peak": tpeak, "unit": "TFLOP/s",
+            "frac": round(tach / tpeak, 4), "traffic": traffic,
+            "peak_source": tkind + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS bf16 burst)",
+            "kernel": "pa_prefill: paged_prefill_kernel (mma.sync m16n8k16)",
+            "algorithmic_flops_per_launch": flops,
+            "kv_gbs": round(achieved, 1),
+        }
+        return {
+            "wl": wl, "ms": ms_max, "ms_local": ms, "decode_ms": dms, "e2e_ms": e2e_max,
+            "h2d": h2d, "d2h": d2h, "bytes": nbytes, "clocks": clk,
+            "launches": st.launches_per_step() * args.steps, "roofline": roof,
+        }
     return {
         "wl": wl, "ms": ms_max, "ms_local": ms, "decode_ms": dms, "e2e_ms": e2e_max,
         "h2d": h2d, "d2h": d2h, "bytes": nbytes, "clocks": clk,
@@ -421,7 +465,13 @@ class OracleStep:
         ids = np.arange(n, dtype=np.int32)
         mask = np.isin(wl.new_seq, ids)
         t0 = time.perf_counter()
-        if wl.window > 0:
+        if wl.query_start is not None:
+            # the sampled sequences' chunks: their new tokens' K/V, then their rows
+            o.cache_write(self.kc, self.vc, wl.k_new[mask], wl.v_new[mask], self.slots[mask])
+            qs = wl.query_start
+            o.paged_prefill(wl.q[qs[0]:qs[n]], self.kc, self.vc, wl.dtype, wl.block_tables[:n],
+                            wl.seq_lens[:n], qs[:n + 1], wl.scale, threads=self.cores)
+        elif wl.window > 0:
             o.cache_write(self.kc, self.vc, wl.k_new[mask], wl.v_new[mask], self.slots[mask])
             o.paged_decode_window(wl.q, self.kc, self.vc, wl.dtype, wl.block_tables,
                                   wl.seq_lens, wl.window, wl.scale, seq_ids=ids,
@@ -491,7 +541,8 @@ def run_reference(args):
 
 
 DEFAULT_SEEDS = {"tiny": 1, "llama2-7b": 2, "llama3-8b-gqa": 3, "qwen2-0.5b-shared-prefix": 4,
-                 "70b-long-context": 5, "llama3-8b-gqa-fp8": 3, "mistral-7b-swa": 6}
+                 "70b-long-context": 5, "llama3-8b-gqa-fp8": 3, "mistral-7b-swa": 6,
+                 "llama3-8b-chunked-prefill": 7}
 
 
 def run_swap(args):

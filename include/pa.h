@@ -270,6 +270,35 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                   pa_stream stream);
 
 /*
+ * pa_prefill -- multi-query paged attention for chunked prefill, with decode
+ * tokens allowed in the same batch.
+ * [P1] "How does it support prompts of arbitrary length?": a long prompt is
+ * processed in chunks, which run in one batch with other requests' decode
+ * tokens; [P4] "Two phases: prefill and decode".  Sequence i brings
+ * L_i = query_start[i + 1] - query_start[i] new tokens whose K/V are already in
+ * the cache (pa_cache_write) as its last L_i of seq_lens[i] tokens; new token
+ * j, at position p = seq_lens[i] - L_i + j, attends causally to tokens [0, p]:
+ *   out = softmax(scale * q . K[0..p]^T) . V[0..p]   (fp32 sums, one rounding).
+ *   q, out        [total_q][num_q_heads][head_dim], dtype; rows of sequence i
+ *                 at [query_start[i], query_start[i + 1]); out must not alias q
+ *   query_start   int32 [num_seqs + 1], query_start[0] = 0, non-decreasing,
+ *                 query_start[num_seqs] = total_q
+ *   workspace     pa_prefill_workspace_size() bytes, zero-filled before its
+ *                 first use; every call that runs to its end leaves it zero
+ * A sequence with L_i > seq_lens[i] or a length outside its table row sets
+ * PA_DEVERR_SEQ_LEN and gets zero rows.  num_seqs <= 4096.  Block sizes of at
+ * least 4 (head_dim 128) or 8 (head_dim 64); head_dim 64 or 128; group size
+ * at most 16.  Query head hq reads KV head hq / G.
+ */
+int pa_prefill_workspace_size(size_t* bytes);
+int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+               const int32_t* query_start, int32_t num_seqs, int64_t total_q,
+               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+               int64_t num_blocks, int32_t dtype, float scale, void* out, void* workspace,
+               size_t workspace_bytes, int32_t* err_word, pa_stream stream);
+
+/*
  * pa_decode_noalloc -- pa_decode without a caller-provided workspace.
  * The paper has no counterpart to this entry point: it exists for callers that
  * cannot allocate device memory (a runtime whose device memory another

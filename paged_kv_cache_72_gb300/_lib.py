@@ -56,6 +56,9 @@ SIGNATURES = {
     "pa_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                      _i64, _i32, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                      _vp, _vp, _sz, _i32, _i32, _vp, _vp]),
+    "pa_prefill_workspace_size": (ctypes.c_int, [ctypes.POINTER(_sz)]),
+    "pa_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                                  _i32, _i64, _i32, ctypes.c_float, _vp, _vp, _sz, _vp, _vp]),
     "pa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                          _i32, _i64, _i32, ctypes.c_float, _vp, _i32, _i32, _vp,
                                          _vp]),

@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build", "libpa")
 LIB = os.path.join(PKG, "libpa.so")
 
 SOURCES = ["pa_api.cu", "pa_cache_ops.cu", "pa_decode.cu", "pa_decode_d64.cu", "pa_decode_d128.cu",
-           "pa_decode_f8_d64.cu", "pa_decode_f8_d128.cu", "pa_decode_noalloc.cu"]
+           "pa_decode_f8_d64.cu", "pa_decode_f8_d128.cu", "pa_decode_noalloc.cu", "pa_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

@@ -367,6 +367,14 @@ int decode_call(const void* q, const void* k_cache, const void* v_cache,
 }
 
 }  // namespace
+
+// A TMA map over one 16-bit pool for other kernels of the library: boxes of
+// p.R rows of p.HG heads of one block, split-row layout, swizzled if p.swz.
+int encode_pool_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int Hkv,
+                    long long num_blocks) {
+  return encode_kv_map(map, cache, p, Hkv, num_blocks, true);
+}
+
 }  // namespace pa
 
 using namespace pa;

@@ -24,6 +24,10 @@ struct DecodePlan {
   size_t ws_count_bytes, ws_rec_bytes;   // workspace: per-CTA piece counters, then records
 };
 
+// TMA map over one 16-bit pool (split-row layout) for other kernels.
+int encode_pool_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int Hkv,
+                    long long num_blocks);
+
 // Per-variant occupancy (CTAs per SM) for a given dynamic shared-memory size.
 int decode_ctas_per_sm(const DecodePlan& p, int* ctas);
 

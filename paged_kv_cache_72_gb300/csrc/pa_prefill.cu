@@ -1,0 +1,587 @@
+// Multi-query paged attention for chunked prefill (and decode tokens in the
+// same batch) on sm_103a.
+//
+// What it computes ("vLLM Framework and Inference Engine Design", section "How
+// does it support prompts of arbitrary length?": a long prompt is processed in
+// chunks, run in one batch with other requests' decode tokens; "vLLM
+// self-hosted", section "Two phases: prefill and decode"): sequence i brings
+// L_i new tokens, already written to the cache at the end of its T_i tokens;
+// new token j, at position p = T_i - L_i + j, attends causally to cached tokens
+// [0, p] through the block table:
+//   out = softmax(scale * q . K[0..p]^T) . V[0..p].
+//
+// Design (one GPU, persistent, tensor cores):
+//  * A work item is (sequence, KV head, tile of BM = 128 / G new tokens): 128
+//    query rows (token, head of the KV head's group), so that every K/V byte
+//    staged in shared memory serves 128 rows.  Items are handed out by an
+//    atomic counter, the later tiles of each sequence (more keys) first.
+//  * One producer warp walks an item's keys [0, p_last] in stages of 64 tokens:
+//    for each it reads the block table and issues 5-D TMA copies of the K and
+//    V boxes of that KV head (a box is R = min(B, 64) rows of one block), and
+//    tags the stage with its item, so that the consumers need no other
+//    handshake.  Stages are guarded by mbarriers.
+//  * Eight consumer warps each own 16 query rows: S = Q . K^T and O += P . V
+//    with m16n8k16 MMAs (rows on M), online softmax in fp32, a causal mask per
+//    row; a 64-token stage is taken as two halves of 32 tokens, and a half that
+//    lies wholly past every row's position is skipped.
+//  * Every wait is bounded; a wait that gives up sets PA_DEVERR_TIMEOUT.
+#include <string.h>
+
+#include <type_traits>
+
+#include "pa_decode_launch.h"
+#include "pa_device.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kPW = 8;                   // consumer warps
+constexpr int kPProducer = kPW;
+constexpr int kPThreads = (kPW + 1) * 32;
+constexpr int kPRows = 16 * kPW;         // query rows per work item
+constexpr int kPBN = 64;                 // key tokens per stage
+constexpr int kPMaxSeqs = 4096;          // per-sequence item offsets kept in shared memory
+constexpr int kPMaxStages = 8;
+
+struct PrefillArgs {
+  const uint16_t* q;            // [total_q][Hq][D]
+  uint16_t* out;                // [total_q][Hq][D]
+  const int32_t* bt;            // [N][stride]
+  const int32_t* seq_lens;      // [N]: tokens in the cache, the new ones included
+  const int32_t* query_start;   // [N + 1]: new tokens of sequence i are q rows [qs[i], qs[i+1])
+  uint32_t* ws;                 // [0] next work item, [1] CTAs finished; zero between calls
+  int32_t* err;
+  long long num_blocks;
+  int num_seqs, stride, Hq, Hkv, G, B, log2B, BM, R, log2R, nsb, stages;
+  float scale_log2;             // scale * log2(e)
+  int sub_log2, hi_log2;        // in a stage part: box j at j << sub_log2, 64-column plane at
+                                // hi << hi_log2, row r at r << 7
+  int kv_bytes, stage_bytes, ctrl_off;
+};
+
+struct Item {
+  int i, h, q0, ntok, p0, T, n_kt;   // sequence, KV head, first q row, tokens, first position,
+                                     // cached tokens, key stages
+};
+
+__device__ __forceinline__ int clamp_seq(int T, int stride, int B) {
+  return (T < 0 || (long long)T > (long long)stride * B) ? -1 : T;
+}
+
+// Item number -> (sequence, KV head, token tile).  toff[i] = Hkv * (tiles of
+// sequences < i); within a sequence the items run over KV heads, then over
+// token tiles from the last (most keys) to the first.
+__device__ __forceinline__ void decode_item(int item, const int* toff, const PrefillArgs& a,
+                                            Item& it) {
+  int lo = 0, hi = a.num_seqs;   // the largest i with toff[i] <= item
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (toff[mid] <= item) lo = mid;
+    else hi = mid;
+  }
+  const int i = lo;
+  const int tiles = (toff[i + 1] - toff[i]) / a.Hkv;
+  const int r = item - toff[i];
+  const int qt = tiles - 1 - r % tiles;
+  const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
+  const int T = __ldg(a.seq_lens + i);
+  it.i = i;
+  it.h = r / tiles;
+  it.q0 = __ldg(a.query_start + i) + qt * a.BM;
+  it.ntok = min(a.BM, L - qt * a.BM);
+  it.p0 = T - L + qt * a.BM;
+  it.T = T;
+  it.n_kt = (it.p0 + it.ntok - 1) / kPBN + 1;
+}
+
+__device__ __forceinline__ uint32_t stage_row(uint32_t part, int tt, int hi, const PrefillArgs& a) {
+  return part + ((uint32_t)(tt >> a.log2R) << a.sub_log2) + ((uint32_t)hi << a.hi_log2) +
+         ((uint32_t)(tt & (a.R - 1)) << 7);
+}
+
+__device__ __forceinline__ uint32_t swz_chunk(uint32_t row, int j) {
+  // 128-byte swizzle: the 16-byte chunk index is XOR-ed with address bits 7..9
+  return row + ((uint32_t)(j ^ (int)((row >> 7) & 7)) << 4);
+}
+
+// Block-wide exclusive scan of one value per thread (kPThreads threads).
+__device__ __forceinline__ long long scan_excl(long long v, long long* tmp, long long& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  long long off = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kPThreads / 32; ++w) {
+    if (w < warp) off += tmp[w];
+    total += tmp[w];
+  }
+  __syncthreads();
+  return off + x - v;
+}
+
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(kPThreads, 1)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = a.stages;
+  const uint32_t bar_full = base + a.ctrl_off;
+  const uint32_t bar_empty = bar_full + 8 * S;
+  int4* const meta = reinterpret_cast<int4*>(gbase + a.ctrl_off + 16 * S);   // per stage
+  int* const toff = reinterpret_cast<int*>(gbase + a.ctrl_off + 32 * S);    // [N + 1]
+  long long* const scan_tmp = reinterpret_cast<long long*>(gbase + a.ctrl_off + 32 * S +
+                                                           4 * (kPMaxSeqs + 1) + 12);
+  volatile int* const abort_flag = reinterpret_cast<int*>(scan_tmp + 16);
+  int* const total_items_s = reinterpret_cast<int*>(scan_tmp + 16) + 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kPW);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kPProducer && lane == 0) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  grid_dep_wait();
+
+  // ---- item offsets: each thread sums the tiles of a run of sequences
+  const int per = (a.num_seqs + kPThreads - 1) / kPThreads;
+  const int run0 = min(a.num_seqs, tid * per), run1 = min(a.num_seqs, run0 + per);
+  long long mine = 0;
+  for (int i = run0; i < run1; ++i) {
+    const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
+    const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
+    const bool ok = L >= 0 && T >= 0 && L <= T;
+    if (ok) mine += (long long)((L + a.BM - 1) / a.BM) * a.Hkv;
+    if ((i % gridDim.x) == blockIdx.x && !ok) {
+      // a length outside its table, or more new tokens than tokens: reported,
+      // and its rows get zeros
+      set_error(a.err, PA_DEVERR_SEQ_LEN);
+      if (L > 0) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(
+            a.out + (size_t)__ldg(a.query_start + i) * a.Hq * D);
+        for (long long e = 0; e < (long long)L * a.Hq * D / 2; ++e) dst[e] = 0u;
+      }
+    }
+  }
+  long long total;
+  long long off = scan_excl(mine, scan_tmp, total);
+  for (int i = run0; i < run1; ++i) {
+    toff[i] = (int)off;
+    const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
+    const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
+    if (L >= 0 && T >= 0 && L <= T) off += (long long)((L + a.BM - 1) / a.BM) * a.Hkv;
+  }
+  if (tid == 0) {
+    toff[a.num_seqs] = (int)total;
+    *total_items_s = (int)total;
+  }
+  __syncthreads();
+  if (tid == 0) grid_dep_launch();
+  const int total_items = *total_items_s;
+
+  if (warp == kPProducer) {
+    // ======================= producer =======================
+    const uint64_t pol = policy_evict_first();
+    const uint32_t box_bytes = 1u << a.sub_log2;
+    int n = 0;   // stages issued so far
+    bool stop = false;
+    while (!stop) {
+      int item = 0;
+      if (lane == 0) item = (int)atomicAdd(a.ws, 1u);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      Item it;
+      if (item < total_items) decode_item(item, toff, a, it);
+      else stop = true;
+      const int n_kt = stop ? 1 : it.n_kt;
+      for (int kt = 0; kt < n_kt; ++kt) {
+        const int st = n % S;
+        const bool waited =
+            mbar_wait_bounded(bar_empty + 8 * st, ((uint32_t)(n / S) & 1u) ^ 1u, abort_flag);
+        if (__any_sync(0xffffffffu, !waited)) {
+          if (lane == 0) {
+            set_error(a.err, PA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+        }
+        if (*abort_flag) {   // the consumers leave on the flag
+          stop = true;
+          break;
+        }
+        if (stop) {
+          // tell the consumers to finish: a stage that carries no item
+          if (lane == 0) {
+            meta[st] = make_int4(-1, 0, 0, 0);
+            mbar_arrive(bar_full + 8 * st);
+          }
+          break;
+        }
+        const int tok0 = kt * kPBN + lane * a.R;
+        int ent = -1;
+        bool ok = false;
+        if (lane < a.nsb && tok0 < it.T) {
+          ent = __ldg(a.bt + (size_t)it.i * a.stride + (tok0 >> a.log2B));
+          ok = ent >= 0 && (long long)ent < a.num_blocks;
+          if (!ok) set_error(a.err, PA_DEVERR_BLOCK_ID);
+        }
+        const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+        const uint32_t sbase = base + (uint32_t)st * a.stage_bytes;
+        if (lane == 0) {
+          meta[st] = make_int4(item, kt, it.n_kt, 0);
+          mbar_arrive_expect_tx(bar_full + 8 * st, (uint32_t)__popc(okmask) * box_bytes * 2u);
+        }
+        __syncwarp();
+        if (ok) {
+          const uint32_t dk = sbase + (uint32_t)lane * box_bytes;
+          const int row_off = tok0 & (a.B - 1);
+          tma_load_5d(dk, &tmk, bar_full + 8 * st, 0, row_off, 0, it.h, ent, pol);
+          tma_load_5d(dk + a.kv_bytes, &tmv, bar_full + 8 * st, 0, row_off, 0, it.h, ent, pol);
+        }
+        ++n;
+      }
+    }
+    // after an abort, drain: no TMA write may land in shared memory after the
+    // CTA exits (otherwise the consumers waited for every stage issued)
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+      for (int k = max(0, n - S); k < n; ++k)
+        mbar_wait_bounded(bar_full + 8 * (k % S), (uint32_t)(k / S) & 1u, nullptr);
+    }
+  } else {
+    // ======================= consumers =======================
+    constexpr int KS = D / 16, NT = D / 8;
+    const int gid = lane >> 2, tig = lane & 3;
+    uint32_t qa[KS][4];
+    float o[NT][4];
+    float m[2], l[2];
+    int prow[2];      // positions of this lane's two rows (-1: padding row)
+    int pmax = -1;    // the warp's largest row position
+    Item it;
+    const float sl2 = a.scale_log2;
+    int n = 0;
+    while (true) {
+      const int st = n % S;
+      if (!*abort_flag) {
+        if (!mbar_wait_bounded(bar_full + 8 * st, (uint32_t)(n / S) & 1u, abort_flag) &&
+            lane == 0) {
+          set_error(a.err, PA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+      }
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int4 md = meta[st];
+      if (md.x < 0) break;
+      const int kt = md.y;
+      if (kt == 0) {
+        // a new item: its query rows, as A fragments, straight from global memory
+        decode_item(md.x, toff, a, it);
+        pmax = -1;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int rr = 16 * warp + gid + 8 * hr;
+          const int tok = rr / a.G, g = rr - tok * a.G;
+          const bool valid = tok < it.ntok && rr < a.BM * a.G;
+          prow[hr] = valid ? it.p0 + tok : -1;
+          const uint16_t* qrow =
+              a.q + ((size_t)(it.q0 + (valid ? tok : 0)) * a.Hq + (size_t)it.h * a.G + g) * D;
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const int d = ks * 16 + 2 * tig;
+            qa[ks][hr] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d)) : 0u;
+            qa[ks][hr + 2] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d + 8)) : 0u;
+          }
+          m[hr] = -INFINITY;
+          l[hr] = 0.f;
+        }
+        if (16 * warp < min(it.ntok * a.G, a.BM * a.G)) {
+          const int last = min(16 * warp + 15, a.BM * a.G - 1) / a.G;   // the warp's last token
+          pmax = it.p0 + min(last, it.ntok - 1);
+        }   // else every row of the warp is padding: it idles through the item
+#pragma unroll
+        for (int nn = 0; nn < NT; ++nn) o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.f;
+      }
+      const uint32_t sbase = base + (uint32_t)st * a.stage_bytes;
+      const uint32_t kpart = sbase, vpart = sbase + a.kv_bytes;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        const int tb = kt * kPBN + 32 * hh;   // first key position of this half
+        if (tb > pmax) break;                 // wholly past every row of the warp
+        // ---- S = Q K^T over 32 keys: four n-tiles of 8
+        float s[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const int tt = 32 * hh + 8 * nt + (lane & 7);   // key row within the stage
+#pragma unroll
+          for (int kp = 0; kp < D / 32; ++kp) {
+            const int cidx = kp * 4 + (lane >> 3);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(swz_chunk(stage_row(kpart, tt, cidx >> 3, a), cidx & 7), b0, b1, b2, b3);
+            mma_16816<kBF16>(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3],
+                             b0, b1);
+            mma_16816<kBF16>(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2],
+                             qa[2 * kp + 1][3], b2, b3);
+          }
+        }
+        // ---- causal mask and online softmax, rows gid (hr = 0) and gid + 8
+        uint32_t pa[2][4];   // A fragments of the two 16-key steps
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int p = prow[hr];
+          float v[8];
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int t = tb + 8 * nt + 2 * tig + e;
+              // a padding row keeps finite scores against cached keys
+              const bool in = p >= 0 ? t <= p : t < it.T;
+              v[2 * nt + e] = in ? s[nt][2 * hr + e] * sl2 : -INFINITY;
+            }
+          float mt = v[0];
+#pragma unroll
+          for (int k = 1; k < 8; ++k) mt = fmaxf(mt, v[k]);
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+          const float mn = fmaxf(m[hr], mt);
+          const float alpha = mn == -INFINITY ? 1.f : exp2f(m[hr] - mn);
+          float sum = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            const float p0 = mn == -INFINITY ? 0.f : exp2f(v[2 * nt] - mn);
+            const float p1 = mn == -INFINITY ? 0.f : exp2f(v[2 * nt + 1] - mn);
+            const uint32_t pk = pack2<kBF16>(p0, p1);
+            const float2 f = unpack2<kBF16>(pk);
+            sum += f.x + f.y;
+            pa[nt >> 1][hr + 2 * (nt & 1)] = pk;
+          }
+          m[hr] = mn;
+          l[hr] = l[hr] * alpha + sum;
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int nn = 0; nn < NT; ++nn) {
+              o[nn][2 * hr] *= alpha;
+              o[nn][2 * hr + 1] *= alpha;
+            }
+          }
+        }
+        // ---- O += P V: two steps of 16 keys; keys at or past T hold no data
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int t0 = tb + 16 * kk;
+          const int nv = it.T - t0;   // valid keys in this step (may be <= 0 or >= 16)
+          if (nv <= 0) break;
+          const uint32_t mlo = (2 * tig < nv ? 0x0000ffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
+          const uint32_t mhi =
+              (8 + 2 * tig < nv ? 0x0000ffffu : 0u) | (9 + 2 * tig < nv ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            const int mat = lane >> 3;
+            const int tt = 32 * hh + 16 * kk + ((mat & 1) << 3) + (lane & 7);
+            const int cidx = 2 * j + (mat >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(swz_chunk(stage_row(vpart, tt, cidx >> 3, a), cidx & 7), b0, b1,
+                              b2, b3);
+            if (nv < 16) {
+              b0 &= mlo;
+              b2 &= mlo;
+              b1 &= mhi;
+              b3 &= mhi;
+            }
+            mma_16816<kBF16>(o[2 * j], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
+            mma_16816<kBF16>(o[2 * j + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+      if (kt == md.z - 1) {
+        // the item's last stage: normalize and write its rows
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          float lt = l[hr];
+          lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+          lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+          if (prow[hr] < 0) continue;
+          const int rr = 16 * warp + gid + 8 * hr;
+          const int tok = rr / a.G, g = rr - tok * a.G;
+          const float inv = 1.f / lt;
+          uint16_t* orow = a.out + ((size_t)(it.q0 + tok) * a.Hq + (size_t)it.h * a.G + g) * D;
+#pragma unroll
+          for (int nn = 0; nn < NT; ++nn)
+            *reinterpret_cast<uint32_t*>(orow + nn * 8 + 2 * tig) =
+                pack2<kBF16>(o[nn][2 * hr] * inv, o[nn][2 * hr + 1] * inv);
+        }
+      }
+      ++n;
+    }
+  }
+  // ---- the last CTA to finish resets the work counters for the next call
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.ws + 1, 1u) == gridDim.x - 1) {
+      a.ws[0] = 0u;
+      a.ws[1] = 0u;
+      __threadfence();
+    }
+  }
+}
+
+struct PrefillPlan {
+  bool bf16;
+  int D, G, B, R, nsb, BM, stages, kv_bytes, stage_bytes, ctrl_off, smem_bytes, grid;
+};
+
+int ctrl_bytes(int S) { return 32 * S + 4 * (kPMaxSeqs + 1) + 12 + 16 * 8 + 16; }
+
+template <int D, bool BF>
+int prepare_kernel(const PrefillPlan& p, int smem_optin, int* per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D, BF>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+  if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute (prefill)");
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, paged_prefill_kernel<D, BF>,
+                                                    kPThreads, p.smem_bytes);
+  return launch_status(e, "occupancy query (prefill)");
+}
+
+int make_plan(int Hq, int Hkv, int D, int B, int dtype, PrefillPlan* out) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (!is_pow2(B) || B < 2 || B > 256) return PA_ERR_UNSUPPORTED;
+  PrefillPlan p{};
+  p.bf16 = dtype == PA_BF16;
+  p.D = D;
+  p.G = Hq / Hkv;
+  if (p.G > 16) return PA_ERR_UNSUPPORTED;
+  p.B = B;
+  p.R = B < kPBN ? B : kPBN;
+  p.nsb = kPBN / p.R;
+  if (p.nsb > 32) return PA_ERR_UNSUPPORTED;
+  // the 128-byte swizzled box must start on 1024 bytes
+  if ((p.R * D * 2) % 1024 != 0) return PA_ERR_UNSUPPORTED;
+  p.BM = kPRows / p.G;
+  p.kv_bytes = kPBN * D * 2;
+  p.stage_bytes = 2 * p.kv_bytes;
+  DeviceInfo di;
+  if (int rc = current_device_info(&di)) return rc;
+  int st = (di.smem_per_block - 1024 - ctrl_bytes(kPMaxStages)) / p.stage_bytes;
+  if (st > kPMaxStages) st = kPMaxStages;
+  if (st < 2) return PA_ERR_UNSUPPORTED;
+  p.stages = st;
+  p.ctrl_off = st * p.stage_bytes;
+  p.smem_bytes = 1024 + p.ctrl_off + ctrl_bytes(st);
+  int per_sm = 0;
+  int rc = D == 64 ? (p.bf16 ? prepare_kernel<64, true>(p, di.smem_per_block, &per_sm)
+                             : prepare_kernel<64, false>(p, di.smem_per_block, &per_sm))
+                   : (p.bf16 ? prepare_kernel<128, true>(p, di.smem_per_block, &per_sm)
+                             : prepare_kernel<128, false>(p, di.smem_per_block, &per_sm));
+  if (rc != PA_OK) return rc;
+  if (per_sm < 1) return PA_ERR_UNSUPPORTED;
+  p.grid = di.sm_count * per_sm;
+  *out = p;
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_prefill_workspace_size(size_t* bytes) {
+  if (!bytes) return PA_ERR_INVALID_ARG;
+  *bytes = 256;
+  return PA_OK;
+}
+
+int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
+               const int32_t* query_start, int32_t num_seqs, int64_t total_q,
+               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+               int64_t num_blocks, int32_t dtype, float scale, void* out, void* workspace,
+               size_t workspace_bytes, int32_t* err_word, pa_stream stream) {
+  if (num_seqs < 0 || total_q < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  PrefillPlan p;
+  if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, &p)) return rc;
+  if (num_seqs == 0 || total_q == 0) return PA_OK;
+  if (num_seqs > kPMaxSeqs) return PA_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start || !out ||
+      !workspace)
+    return PA_ERR_INVALID_ARG;
+  if (num_blocks == 0 || table_stride == 0 || num_blocks > 0xffffffffLL) return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace))
+    return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < 256) return PA_ERR_WORKSPACE;
+  DecodePlan mp{};
+  mp.bf16 = p.bf16;
+  mp.D = p.D;
+  mp.B = p.B;
+  mp.R = p.R;
+  mp.HG = 1;
+  mp.swz = true;
+  CUtensorMap tk, tv;
+  if (int rc = encode_pool_map(&tk, k_cache, mp, num_kv_heads, num_blocks)) return rc;
+  if (int rc = encode_pool_map(&tv, v_cache, mp, num_kv_heads, num_blocks)) return rc;
+  PrefillArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.bt = block_tables;
+  a.seq_lens = seq_lens;
+  a.query_start = query_start;
+  a.ws = static_cast<uint32_t*>(workspace);
+  a.err = err_word;
+  a.num_blocks = num_blocks;
+  a.num_seqs = num_seqs;
+  a.stride = table_stride;
+  a.Hq = num_q_heads;
+  a.Hkv = num_kv_heads;
+  a.G = p.G;
+  a.B = p.B;
+  a.log2B = ilog2(p.B);
+  a.BM = p.BM;
+  a.R = p.R;
+  a.log2R = ilog2(p.R);
+  a.nsb = p.nsb;
+  a.stages = p.stages;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.hi_log2 = a.log2R + 7;                     // a plane is R rows of 128 bytes
+  a.sub_log2 = a.hi_log2 + ilog2(p.D / 64);    // a box is D/64 planes
+  a.kv_bytes = p.kv_bytes;
+  a.stage_bytes = p.stage_bytes;
+  a.ctrl_off = p.ctrl_off;
+  clear_stale_error();
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (p.D == 64)
+    e = p.bf16 ? launch_pdl(paged_prefill_kernel<64, true>, dim3(p.grid), dim3(kPThreads),
+                            (size_t)p.smem_bytes, s, tk, tv, a)
+               : launch_pdl(paged_prefill_kernel<64, false>, dim3(p.grid), dim3(kPThreads),
+                            (size_t)p.smem_bytes, s, tk, tv, a);
+  else
+    e = p.bf16 ? launch_pdl(paged_prefill_kernel<128, true>, dim3(p.grid), dim3(kPThreads),
+                            (size_t)p.smem_bytes, s, tk, tv, a)
+               : launch_pdl(paged_prefill_kernel<128, false>, dim3(p.grid), dim3(kPThreads),
+                            (size_t)p.smem_bytes, s, tk, tv, a);
+  return launch_status(e, "prefill kernel launch");
+}
+
+}  // extern "C"

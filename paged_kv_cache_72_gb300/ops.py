@@ -272,6 +272,39 @@ def pa_decode_fp8(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale, v
     return out
 
 
+def pa_prefill(q, k_cache, v_cache, block_tables, seq_lens, query_start, scale, out=None,
+               workspace=None, err=None):
+    """Multi-query paged attention (chunked prefill, decode tokens allowed):
+    q [total_q, Hq, D]; sequence i's new tokens are rows [query_start[i],
+    query_start[i+1]), already written at the end of its seq_lens[i] tokens."""
+    L = _lib.load()
+    nb, B, H, D = _pool_shape(k_cache, v_cache)
+    for t, n in ((q, "q"), (block_tables, "block_tables"), (seq_lens, "seq_lens"),
+                 (query_start, "query_start")):
+        _cuda(t, n)
+    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"),
+                 (query_start, "query_start")):
+        if t.dtype != torch.int32:
+            raise TypeError("%s must be int32" % n)
+    total, Hq, Dq = q.shape
+    N = seq_lens.numel()
+    if Dq != D or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [total_q, Hq, D] in the pool dtype")
+    if query_start.numel() != N + 1 or block_tables.dim() != 2 or block_tables.shape[0] != N:
+        raise ValueError("query_start must be [N + 1] and block_tables [N, stride]")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _check(L.pa_prefill_workspace_size(ctypes.byref(n)), "pa_prefill_workspace_size")
+        workspace = torch.zeros(n.value, dtype=torch.uint8, device=q.device)
+    _check(L.pa_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                        block_tables.shape[1], _ptr(seq_lens), _ptr(query_start), N, total, Hq, H,
+                        D, B, nb, _dtype_code(q), float(scale), _ptr(out), _ptr(workspace),
+                        workspace.numel(), _ptr(err), _stream()), "pa_prefill")
+    return out
+
+
 def pa_gather_kv(k_cache, v_cache, block_tables, seq_lens, out_offsets, total_rows,
                  flags=PA_DECODE_AUTO, err=None):
     """Contiguous copies [total_rows, H_kv, D] of every sequence's K and V."""

@@ -49,6 +49,8 @@ class GpuState:
         self.new_seq = torch.from_numpy(wl.new_seq).to(device)
         self.new_pos = torch.from_numpy(wl.new_pos).to(device)
         self.pairs = torch.from_numpy(np.ascontiguousarray(wl.copy_pairs, np.int32)).to(device)
+        self.query_start = (None if wl.query_start is None
+                            else torch.from_numpy(wl.query_start).to(device))
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
 
 
@@ -73,6 +75,9 @@ def gpu_step(st, flags=pa.PA_DECODE_AUTO, num_ctas=0, decode=True):
 def gpu_decode(st, seq_lens, flags=pa.PA_DECODE_AUTO, num_ctas=0, workspace=None):
     """The decode call of the workload's cache type."""
     wl = st.wl
+    if wl.query_start is not None:
+        return pa.pa_prefill(st.q, st.k_cache, st.v_cache, st.block_tables, seq_lens,
+                             st.query_start, wl.scale, workspace=workspace, err=st.err)
     if wl.window > 0:
         return pa.pa_decode_window(st.q, st.k_cache, st.v_cache, st.block_tables, seq_lens,
                                    wl.scale, wl.window, flags=flags, num_ctas=num_ctas,
@@ -107,6 +112,10 @@ class OracleState:
     def decode(self, seq_ids=None, threads=0, seq_lens=None):
         wl = self.wl
         sl = wl.seq_lens if seq_lens is None else seq_lens
+        if wl.query_start is not None:
+            return oracle.paged_prefill(wl.q, self.k_cache, self.v_cache, wl.dtype,
+                                        wl.block_tables, sl, wl.query_start, wl.scale,
+                                        threads=threads)
         if wl.window > 0:
             return oracle.paged_decode_window(wl.q, self.k_cache, self.v_cache, wl.dtype,
                                               wl.block_tables, sl, wl.window, wl.scale,
