@@ -19,7 +19,7 @@ constexpr int kMaxStages = 8;
 // mbarriers (16 B per stage, 16 B per query buffer), scan scratch, control
 // words, merge row scratch
 int ctrl_bytes(int stages) {
-  return 16 * stages + 16 * kQBufs + kScanBytes + kCtrlBytes + kRowScratchBytes;
+  return 16 * stages + 16 * kQBufs + kScanBytes + kCtrlBytes + kRowScratchBytes + kLenCacheBytes;
 }
 
 // kv_dtype: the pools' element type (PA_F16, PA_BF16 or PA_FP8_E4M3);
@@ -80,7 +80,8 @@ int make_plan(int Hq, int Hkv, int D, int B, int kv_dtype, int q_dtype, int flag
   q.kv_bytes = q.CT * q.HG * D * eb;
   q.stage_bytes = 2 * q.kv_bytes;
   q.q_bytes = gather ? 0 : q.HG * G * D * 2;
-  q.q_stride = ((q.q_bytes + 127) / 128) * 128;
+  // rows land q_pitch apart (pa_decode_kernel.cuh)
+  q.q_stride = gather ? 0 : ((q.HG * G * (D * 2 + 16) + 127) / 128) * 128;
   const int merge_bytes = (gather || q.TPH == 1) ? 0 : kCWarps * (32 + G * D) * 4;
 
   DeviceInfo di;

@@ -65,10 +65,13 @@ struct MmaConsumerF8 {
   float l[NH][2];           // this lane's share of their running sums
   float vscale = 1.f;
 
-  // query elements (d, d + 1) of row `row` of the query slot, as f16x2
+  // query elements (d, d + 1) of row `row` of the query slot (rows q_pitch
+  // bytes apart), as f16x2
   __device__ __forceinline__ static uint32_t q_pair(uint32_t qslot, int row, int d) {
     uint32_t w;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(qslot + (uint32_t)(row * D + d) * 2));
+    asm volatile("ld.shared.b32 %0, [%1];"
+                 : "=r"(w)
+                 : "r"(qslot + (uint32_t)(row * q_pitch<D>() + d * 2)));
     if constexpr (kBF16) {
       const float2 f = unpack2<true>(w);
       return pack2<false>(f.x, f.y);

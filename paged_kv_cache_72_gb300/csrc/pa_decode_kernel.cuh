@@ -48,11 +48,19 @@ constexpr int kCWarps = 8;         // consumer warps; stage = kCWarps * 16 token
 constexpr int kProducerWarp = kCWarps;
 constexpr int kThreads = (kCWarps + 1) * 32;
 constexpr int kQBufs = 2;          // query-row buffers in flight
+// Query rows sit in shared memory at a pitch of one row plus 16 bytes, so
+// that the fragment loads of rows a full row apart fall in different banks.
+template <int D>
+__host__ __device__ constexpr int q_pitch() { return D * 2 + 16; }
+// Lengths of the first kLenCache sequences, kept in shared memory by the scan
+// for the walks of the producer and the consumers.
+constexpr int kLenCache = 1024;
 // Shared-memory control area after the mbarriers: scan scratch, control words
 // (walk start, abort flag, merges this CTA owes), merge row scratch.
 constexpr int kScanBytes = 128;
 constexpr int kCtrlBytes = 64;
 constexpr int kRowScratchBytes = 512;
+constexpr int kLenCacheBytes = 4 * kLenCache;
 constexpr int kCtrlMerges = 5;     // ctrl[5] = pending merges, then 4 ints per merge
 // counter bit set by a piece whose CTA gave up: the context is left unmerged
 constexpr uint32_t kPieceAborted = 0x80000000u;
@@ -115,14 +123,15 @@ struct Walk {
   int t0, lo;           // first token of chunk 0, leading tokens of chunk 0 outside the window
 };
 
-__device__ __forceinline__ void walk_load_seq(Walk& w, const DecodeArgs& a) {
-  w.T = clamp_len(__ldg(a.seq_lens + w.i), a.stride, a.B);
+// s_len: the clamped lengths of sequences [0, kLenCache) in shared memory
+__device__ __forceinline__ void walk_load_seq(Walk& w, const DecodeArgs& a, const int* s_len) {
+  w.T = w.i < kLenCache ? s_len[w.i] : clamp_len(__ldg(a.seq_lens + w.i), a.stride, a.B);
   w.t0 = attend_origin(w.T, a);
   w.lo = (a.window > 0 && w.T > a.window) ? w.T - a.window - w.t0 : 0;
   w.nc = (w.T - w.t0 + a.CT - 1) / a.CT;
 }
 
-__device__ __forceinline__ void walk_advance(Walk& w, const DecodeArgs& a) {
+__device__ __forceinline__ void walk_advance(Walk& w, const DecodeArgs& a, const int* s_len) {
   if (++w.c < w.nc) return;
   w.c = 0;
   if (++w.g < a.NGR) return;
@@ -130,7 +139,7 @@ __device__ __forceinline__ void walk_advance(Walk& w, const DecodeArgs& a) {
   do {
     ++w.i;
     if (w.i >= a.num_seqs) { w.nc = 0; w.T = 0; return; }
-    walk_load_seq(w, a);
+    walk_load_seq(w, a, s_len);
   } while (w.nc == 0);
 }
 
@@ -186,11 +195,12 @@ template <int D, bool kBF16, bool kSwz, bool kHi>
 struct MmaConsumer {
   static constexpr int KS = D / 16;   // k-steps of QK
   static constexpr int NT = D / 8;    // n-tiles of PV
+  static constexpr int QP = q_pitch<D>();
   uint32_t qa[KS][4];
   float o[NT][4];
   float m[2], l[2];
 
-  // qslot: this head's G query rows [G][D]
+  // qslot: this head's G query rows, QP bytes apart
   __device__ __forceinline__ void begin(uint32_t qslot, int G) {
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
 #pragma unroll
@@ -198,14 +208,14 @@ struct MmaConsumer {
       const int d0 = ks * 16 + 2 * tig;
       uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
       if (gid < G) {
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a0) : "r"(qslot + (gid * D + d0) * 2));
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a2) : "r"(qslot + (gid * D + d0 + 8) * 2));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a0) : "r"(qslot + gid * QP + d0 * 2));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a2) : "r"(qslot + gid * QP + (d0 + 8) * 2));
       }
       if (kHi && gid + 8 < G) {
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a1) : "r"(qslot + ((gid + 8) * D + d0) * 2));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a1) : "r"(qslot + (gid + 8) * QP + d0 * 2));
         asm volatile("ld.shared.b32 %0, [%1];"
                      : "=r"(a3)
-                     : "r"(qslot + ((gid + 8) * D + d0 + 8) * 2));
+                     : "r"(qslot + (gid + 8) * QP + (d0 + 8) * 2));
       }
       qa[ks][0] = a0;
       qa[ks][1] = a1;
@@ -727,6 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* const ctrl = reinterpret_cast<int*>(gbase + ctrl_words + kScanBytes);
   volatile int* const abort_flag = ctrl + 4;
   float* const s_row = reinterpret_cast<float*>(gbase + ctrl_words + kScanBytes + kCtrlBytes);
+  int* const s_len = reinterpret_cast<int*>(gbase + ctrl_words + kScanBytes + kCtrlBytes +
+                                            kRowScratchBytes);
 
   if (tid == 0) {
     ctrl[0] = -1;
@@ -779,6 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int T0 = __ldg(a.seq_lens + i);
     const int T = clamp_len(T0, a.stride, a.B);
     my_nc += seq_chunks(T, a);
+    if (i < kLenCache) s_len[i] = T;
     if ((i % gridDim.x) == blockIdx.x) {
       if (T != T0) set_error(a.err, PA_DEVERR_SEQ_LEN);
       if (kMode != kModeGather && T == 0) {
@@ -823,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   w0.i = ctrl[0];
   w0.g = ctrl[1];
   w0.c = ctrl[2];
-  walk_load_seq(w0, a);
+  walk_load_seq(w0, a, s_len);
 
   const int qbytes = a.q_bytes;
   const uint32_t box_bytes = 1u << a.sub_log2;
@@ -843,6 +856,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ent = load_entry(w);
     int issued = 0;
     uint32_t seg = 0;
+    int st = 0;          // stage of chunk n (n % S), kept incrementally
+    uint32_t ph = 0;     // phase parity of that stage ((n / S) & 1)
     for (int n = 0; n < n_chunks; ++n) {
       const bool seg_start = (n == 0) || (w.c == 0);
       if (kMode != kModeGather && seg_start) {
@@ -860,18 +875,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           break;
         }
-        if (lane == 0) {
+        {
+          // one bulk copy per query row, into rows q_pitch apart
           const uint32_t qdst = base + a.q_off + (uint32_t)qb * a.q_stride;
           const uint16_t* qsrc = a.q + ((size_t)w.i * a.Hq + (size_t)w.g * a.HG * a.G) * D;
-          mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)qbytes);
-          bulk_load(qdst, qsrc, (uint32_t)qbytes, bar_qfull + 8 * qb);
+          if (lane == 0) mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)qbytes);
+          __syncwarp();
+          for (int r = lane; r < a.HG * a.G; r += 32)
+            bulk_load(qdst + (uint32_t)(r * q_pitch<D>()), qsrc + (size_t)r * D, D * 2,
+                      bar_qfull + 8 * qb);
         }
         __syncwarp();
         ++seg;
       }
-      const int st = n % S;
-      const uint32_t round = (uint32_t)(n / S);
-      const bool waited = mbar_wait_bounded(bar_empty + 8 * st, (round & 1u) ^ 1u, abort_flag);
+      const bool waited = mbar_wait_bounded(bar_empty + 8 * st, ph ^ 1u, abort_flag);
       const bool timed_out = __any_sync(0xffffffffu, !waited);
       if (__any_sync(0xffffffffu, timed_out || *abort_flag != 0)) {
         if (lane == 0) {
@@ -909,7 +926,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.c == 0 && w.g == 0 && lane < 2 && w.i + 1 < a.num_seqs && lane * 32 < a.stride)
         asm volatile("prefetch.global.L1 [%0];" ::"l"(a.bt + (size_t)(w.i + 1) * a.stride + lane * 32));
       ++issued;
-      walk_advance(w, a);
+      if (++st == S) {
+        st = 0;
+        ph ^= 1u;
+      }
+      walk_advance(w, a, s_len);
       if (n + 1 < n_chunks) ent = load_entry(w);
     }
     // drain: make sure no TMA write is still in flight into this CTA's shared
@@ -943,9 +964,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool first_seg = true;
   uint32_t seg = 0;
   const float sl2 = a.scale_log2;
+  int st = 0;          // stage of chunk n (n % S), kept incrementally
+  uint32_t ph = 0;     // phase parity of that stage ((n / S) & 1)
   for (int n = 0; n < n_chunks; ++n) {
-    const int st = n % S;
-    const uint32_t round = (uint32_t)(n / S);
     const bool seg_start = (n == 0) || (w.c == 0);
     if (seg_start) {
       seg_c0 = w.c;
@@ -959,14 +980,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!__any_sync(0xffffffffu, *abort_flag != 0))
-          cs.begin(base + a.q_off + (uint32_t)qb * a.q_stride + (uint32_t)(hl * a.G * D * 2), a.G);
+          cs.begin(base + a.q_off + (uint32_t)qb * a.q_stride +
+                       (uint32_t)(hl * a.G * q_pitch<D>()), a.G);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_qempty + 8 * qb);
         ++seg;
       }
     }
     if (!*abort_flag) {
-      if (!mbar_wait_bounded(bar_full + 8 * st, round & 1u, abort_flag)) {
+      if (!mbar_wait_bounded(bar_full + 8 * st, ph, abort_flag)) {
         if (lane == 0) {
           set_error(a.err, PA_DEVERR_TIMEOUT);
           *abort_flag = 1;
@@ -1036,7 +1058,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_seg = false;
       }
     }
-    walk_advance(w, a);
+    if (++st == S) {
+      st = 0;
+      ph ^= 1u;
+    }
+    walk_advance(w, a, s_len);
   }
   if constexpr (kMode != kModeGather) {
     // the merges this CTA owes (at most two: its first and its last segment
