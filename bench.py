@@ -223,6 +223,9 @@ class Step:
                                              wl.block_size, W.FP8 if wl.fp8 else wl.dtype)
         self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        # a step's lengths and block tables are in place before its first
+        # kernel, so the decode may read them while the cache write drains
+        self.flags = pa.PA_DECODE_TABLES_READY
         self.query_start = (None if wl.query_start is None
                             else torch.from_numpy(wl.query_start).to(device))
         self.pf_ws = torch.zeros(256, dtype=torch.uint8, device=device)
@@ -257,15 +260,15 @@ class Step:
         elif wl.window > 0:
             self.pa.pa_decode_window(self.q, self.k_cache, self.v_cache, self.block_tables,
                                      self.seq_lens, wl.scale, wl.window, out=self.out,
-                                     workspace=self.workspace, err=self.err)
+                                     workspace=self.workspace, flags=self.flags, err=self.err)
         elif wl.fp8:
             self.pa.pa_decode_fp8(self.q, self.k_cache, self.v_cache, self.block_tables,
                                   self.seq_lens, wl.scale, wl.k_scale, wl.v_scale, out=self.out,
-                                  workspace=self.workspace, err=self.err)
+                                  workspace=self.workspace, flags=self.flags, err=self.err)
         else:
             self.pa.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables,
                               self.seq_lens, wl.scale, out=self.out, workspace=self.workspace,
-                              err=self.err)
+                              flags=self.flags, err=self.err)
 
     def run(self):
         self.write_phase()

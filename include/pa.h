@@ -72,6 +72,13 @@ extern "C" {
 #define PA_DECODE_AUTO 0
 #define PA_DECODE_SIMT 1  /* CUDA-core kernel (group size 1 only) */
 #define PA_DECODE_MMA 2   /* tensor-core kernel (any supported group size) */
+/* OR-ed into the flags of pa_decode, pa_decode_window and pa_decode_fp8: the
+ * caller promises that seq_lens and block_tables are complete before the
+ * preceding kernel in the stream starts (as a serving step's metadata is).
+ * The decode then reads them while that kernel drains, under programmatic
+ * dependent launch; q, the pools, out and the workspace are still touched
+ * only after it completes. */
+#define PA_DECODE_TABLES_READY 0x100
 
 typedef void* pa_stream; /* cudaStream_t */
 
@@ -214,7 +221,8 @@ int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t 
  * state in the workspace and counts itself, and the block whose piece
  * completes the count merges them (one kernel launch, no block waits for
  * another, any num_ctas).
- * flags: PA_DECODE_AUTO, PA_DECODE_SIMT or PA_DECODE_MMA; num_ctas: 0 = default.
+ * flags: PA_DECODE_AUTO, PA_DECODE_SIMT or PA_DECODE_MMA, optionally OR-ed with
+ * PA_DECODE_TABLES_READY; num_ctas: 0 = default.
  */
 int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,

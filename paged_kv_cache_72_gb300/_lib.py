@@ -28,6 +28,7 @@ PA_SWAP_IN = 1
 PA_DECODE_AUTO = 0
 PA_DECODE_SIMT = 1
 PA_DECODE_MMA = 2
+PA_DECODE_TABLES_READY = 0x100
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 PA_DECODE_MAX_CTAS = 16384
 

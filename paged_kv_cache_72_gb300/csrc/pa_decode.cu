@@ -38,6 +38,7 @@ int make_plan(int Hq, int Hkv, int D, int B, int kv_dtype, int q_dtype, int flag
   if (Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
   if (G > 16) return PA_ERR_UNSUPPORTED;
+  flags &= ~PA_DECODE_TABLES_READY;   // a launch option, not part of the plan
   if (flags != PA_DECODE_AUTO && flags != PA_DECODE_SIMT && flags != PA_DECODE_MMA)
     return PA_ERR_INVALID_ARG;
   DecodePlan q{};
@@ -332,6 +333,8 @@ int decode_call(const void* q, const void* k_cache, const void* v_cache,
                 int32_t* err_word, pa_stream stream) {
   if (num_seqs < 0 || table_stride < 0 || num_blocks < 0 || window < 0) return PA_ERR_INVALID_ARG;
   DecodePlan p;
+  const int early = (flags & PA_DECODE_TABLES_READY) ? 1 : 0;
+  flags &= ~PA_DECODE_TABLES_READY;
   if (int rc = cached_plan(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, q_dtype,
                            flags, num_ctas, false, &p))
     return rc;
@@ -363,6 +366,7 @@ int decode_call(const void* q, const void* k_cache, const void* v_cache,
   a.scale_log2 = scale * k_scale * 1.4426950408889634f;
   a.v_scale = v_scale;
   a.window = window;
+  a.early_tables = early;
   fill_layout(p, &a);
   return launch(p, tk, tv, a, static_cast<cudaStream_t>(stream));
 }
@@ -386,6 +390,7 @@ int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t 
                              int32_t block_size, int32_t dtype, int32_t flags, int32_t num_ctas,
                              size_t* bytes) {
   if (!bytes) return PA_ERR_INVALID_ARG;
+  flags &= ~PA_DECODE_TABLES_READY;   // the workspace does not depend on it
   // an E4M3 cache: the workspace does not depend on the query dtype
   const int q_dtype = dtype == PA_FP8_E4M3 ? PA_BF16 : dtype;
   DecodePlan p;

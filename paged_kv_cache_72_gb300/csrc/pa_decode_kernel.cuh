@@ -62,6 +62,7 @@ constexpr int kCtrlBytes = 64;
 constexpr int kRowScratchBytes = 512;
 constexpr int kLenCacheBytes = 4 * kLenCache;
 constexpr int kCtrlMerges = 5;     // ctrl[5] = pending merges, then 4 ints per merge
+constexpr int kCtrlEmpty = 14;     // this CTA owns empty or invalid sequences (early tables)
 // counter bit set by a piece whose CTA gave up: the context is left unmerged
 constexpr uint32_t kPieceAborted = 0x80000000u;
 
@@ -95,6 +96,8 @@ struct DecodeArgs {
   int ctrl_off;              // byte offset of barriers and control words
   float v_scale;             // E4M3 cache: V value = code * v_scale (1 otherwise)
   int window;                // sliding window: attend to the last `window` tokens (0: all)
+  int early_tables;          // seq_lens and block tables are complete before the preceding
+                             // kernel starts: read them before waiting for it
 };
 
 // Clamped length: invalid lengths count as 0 tokens.
@@ -752,6 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *abort_flag = 0;
     ctrl[kCtrlMerges] = 0;
+    ctrl[kCtrlEmpty] = 0;
     fence_barrier_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -775,8 +779,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (size_t o = t0; o < q_bytes; o += step) prefetch_l2(qp + o);
     }
   }
-  // inputs may come from the previous kernel in the stream
-  grid_dep_wait();
+  // inputs may come from the previous kernel in the stream; with early
+  // tables only q, the pools, out and the workspace may, and the lengths and
+  // tables are read first, while that kernel drains
+  if (!a.early_tables) grid_dep_wait();
 
   // ---- find this CTA's range of chunks -------------------------------------
   // The work is the list of chunks over (sequence, head group, CT tokens), in
@@ -792,11 +798,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int T = clamp_len(T0, a.stride, a.B);
     my_nc += seq_chunks(T, a);
     if (i < kLenCache) s_len[i] = T;
-    if ((i % gridDim.x) == blockIdx.x) {
-      if (T != T0) set_error(a.err, PA_DEVERR_SEQ_LEN);
-      if (kMode != kModeGather && T == 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + (size_t)i * a.Hq * D);
-        for (int e = 0; e < a.Hq * D / 2; ++e) dst[e] = 0u;
+    if ((i % gridDim.x) == blockIdx.x && (T != T0 || (kMode != kModeGather && T == 0))) {
+      if (a.early_tables) {
+        ctrl[kCtrlEmpty] = 1;   // reported and zeroed below, once err and out may be written
+      } else {
+        if (T != T0) set_error(a.err, PA_DEVERR_SEQ_LEN);
+        if (kMode != kModeGather && T == 0) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + (size_t)i * a.Hq * D);
+          for (int e = 0; e < a.Hq * D / 2; ++e) dst[e] = 0u;
+        }
       }
     }
   }
@@ -826,8 +836,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // let the next kernel get scheduled; it still waits for this whole grid
   // before reading anything
   if (tid == 0) grid_dep_launch();
+  if (a.early_tables && ctrl[kCtrlEmpty]) {
+    grid_dep_wait();
+    for (int i = run0; i < run1; ++i) {
+      if ((i % gridDim.x) != blockIdx.x) continue;
+      const int T0 = __ldg(a.seq_lens + i);
+      const int T = clamp_len(T0, a.stride, a.B);
+      if (T != T0) set_error(a.err, PA_DEVERR_SEQ_LEN);
+      if (kMode != kModeGather && T == 0) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + (size_t)i * a.Hq * D);
+        for (int e = 0; e < a.Hq * D / 2; ++e) dst[e] = 0u;
+      }
+    }
+  }
   if (n_chunks == 0) return;
   if (ctrl[0] < 0) {   // cannot happen for a consistent scan; never walk blind
+    if (a.early_tables) grid_dep_wait();
     if (tid == 0) set_error(a.err, PA_DEVERR_SEQ_LEN);
     return;
   }
@@ -854,6 +878,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return ent;
     };
     int ent = load_entry(w);
+    // the pools and q may come from the preceding kernel
+    if (a.early_tables) grid_dep_wait();
     int issued = 0;
     uint32_t seg = 0;
     int st = 0;          // stage of chunk n (n % S), kept incrementally
@@ -945,6 +971,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= consumers =======================
+  // out and the workspace may be touched by the preceding kernel
+  if (a.early_tables) grid_dep_wait();
   using Mma = typename std::conditional<kF8, MmaConsumerF8<D, kBF16, kSwz, kHi>,
                                         MmaConsumer<D, kBF16, kSwz, kHi>>::type;
   using Consumer =
