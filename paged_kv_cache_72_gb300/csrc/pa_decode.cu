@@ -19,7 +19,7 @@ constexpr int kMaxStages = 8;
 // mbarriers (16 B per stage, 16 B per query buffer), scan scratch, control
 // words, merge row scratch
 int ctrl_bytes(int stages) {
-  return 16 * stages + 16 * kQBufs + kScanBytes + kCtrlBytes + kRowScratchBytes + kLenCacheBytes;
+  return 16 * stages + 16 * kQBufs + kScanBytes + kCtrlBytes + kLenCacheBytes;
 }
 
 // kv_dtype: the pools' element type (PA_F16, PA_BF16 or PA_FP8_E4M3);

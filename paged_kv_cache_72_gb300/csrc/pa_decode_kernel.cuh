@@ -56,10 +56,9 @@ __host__ __device__ constexpr int q_pitch() { return D * 2 + 16; }
 // for the walks of the producer and the consumers.
 constexpr int kLenCache = 1024;
 // Shared-memory control area after the mbarriers: scan scratch, control words
-// (walk start, abort flag, merges this CTA owes), merge row scratch.
+// (walk start, abort flag, merges this CTA owes), the lengths cache.
 constexpr int kScanBytes = 128;
 constexpr int kCtrlBytes = 64;
-constexpr int kRowScratchBytes = 512;
 constexpr int kLenCacheBytes = 4 * kLenCache;
 constexpr int kCtrlMerges = 5;     // ctrl[5] = pending merges, then 4 ints per merge
 constexpr int kCtrlEmpty = 14;     // this CTA owns empty or invalid sequences (early tables)
@@ -644,76 +643,63 @@ __device__ __forceinline__ void gather_tile(const DecodeArgs& a, uint32_t kpart,
 // each in record slot 0 except the first CTA's when the context began after
 // that CTA's own first chunk (then it is that CTA's second segment, slot 1):
 //   out = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k.
-// Pass 1: tpr threads per row fold the pieces' (m, l) pairs online and
-// combine by shuffles; pass 2: four head_dim columns per thread, weights
-// 2^(m_k - m*) recomputed next to each o_k load.  s_row: 128 floats of shared
-// memory.  Consumer threads only; the records come from other CTAs, so they
-// are read from L2 (ld.global.cg).
+// One pass: D / 16 threads share a row, each owning 16 of its head_dim
+// columns, and fold the pieces in with the online rescaling, loading a
+// piece's (m, l) and its 16 o values together, so that a merge waits on L2
+// about once per piece rather than once per step.  Consumer threads only;
+// the records come from other CTAs, so they are read from L2 (ld.global.cg).
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16>
 __device__ __forceinline__ void merge_split(const DecodeArgs& a, int i, int grp, long long g0,
-                                            int nc, long long cpc, float* s_row) {
+                                            int nc, long long cpc) {
   const int tid = threadIdx.x;   // consumer threads 0 .. kCWarps * 32 - 1
-  const int nthr = kCWarps * 32;
+  constexpr int kTPR = D / 16;   // threads per row
+  constexpr int kRowsPerPass = kCWarps * 32 / kTPR;
   const int first = (int)(g0 / cpc);
   const int last = (int)((g0 + nc - 1) / cpc);
   const int rows = a.HG * a.G;
   const size_t rf = rec_floats(rows, D);
   const size_t ml = (size_t)rows * D;   // m[] then l[] follow o[][]
-  auto rec_of = [&](int k) -> const float* {
-    const int slot = (k == first && g0 != (long long)first * cpc) ? 1 : 0;
-    return a.ws_rec + ((size_t)k * 2 + slot) * rf;
-  };
-  int tpr = 32;   // threads per row: a power of two, tpr * rows <= nthr
-  while (tpr * rows > nthr) tpr >>= 1;
-  if (tid < ((tpr * rows + 31) & ~31)) {   // whole warps, so that shuffles see every lane
-    const int r = tid / tpr, j = tid % tpr;
+  const int d = (tid % kTPR) * 16;
+  for (int r = tid / kTPR; r < rows; r += kRowsPerPass) {
     float m = -INFINITY, l = 0.f;
-    if (r < rows) {
-      for (int k = first + j; k <= last; k += tpr) {
-        const float* rec = rec_of(k);
-        const float mk = __ldcg(rec + ml + r), lk = __ldcg(rec + ml + rows + r);
+    float4 acc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = first; k <= last; ++k) {
+      const int slot = (k == first && g0 != (long long)first * cpc) ? 1 : 0;
+      const float* rec = a.ws_rec + ((size_t)k * 2 + slot) * rf;
+      const float mk = __ldcg(rec + ml + r), lk = __ldcg(rec + ml + rows + r);
+      float4 ok[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        ok[c] = __ldcg(reinterpret_cast<const float4*>(rec + (size_t)r * D + d + 4 * c));
+      if (mk != -INFINITY) {
         const float mn = fmaxf(m, mk);
-        l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + lk * exp2f(mk - mn);
+        const float so = exp2f(m - mn), sn = exp2f(mk - mn);   // so = 0 while m = -inf
+        l = l * so + lk * sn;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          acc[c].x = acc[c].x * so + ok[c].x * sn;
+          acc[c].y = acc[c].y * so + ok[c].y * sn;
+          acc[c].z = acc[c].z * so + ok[c].z * sn;
+          acc[c].w = acc[c].w * so + ok[c].w * sn;
+        }
         m = mn;
       }
     }
-    for (int o = 1; o < tpr; o <<= 1) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m, o);
-      const float lo = __shfl_xor_sync(0xffffffffu, l, o);
-      const float mn = fmaxf(m, mo);
-      if (mn != -INFINITY)
-        l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + (mo == -INFINITY ? 0.f : lo * exp2f(mo - mn));
-      m = mn;
+    const float inv = 1.f / l;
+    uint4 pk[2];
+    uint32_t* w = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      w[2 * c] = pack2<kBF16>(acc[c].x * inv, acc[c].y * inv);
+      w[2 * c + 1] = pack2<kBF16>(acc[c].z * inv, acc[c].w * inv);
     }
-    if (r < rows && j == 0) {
-      s_row[r] = m;
-      s_row[64 + r] = 1.f / l;
-    }
+    uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)i * a.Hq + (size_t)grp * rows + r) * D + d);
+    dst[0] = pk[0];
+    dst[1] = pk[1];
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
-  for (int e = tid; e < rows * (D / 4); e += nthr) {
-    const int r = e / (D / 4);
-    const int d = 4 * (e % (D / 4));
-    const float mx = s_row[r];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = first; k <= last; ++k) {
-      const float* rec = rec_of(k);
-      const float wt = exp2f(__ldcg(rec + ml + r) - mx);
-      const float4 ov = __ldcg(reinterpret_cast<const float4*>(rec + (size_t)r * D + d));
-      acc.x = fmaf(wt, ov.x, acc.x);
-      acc.y = fmaf(wt, ov.y, acc.y);
-      acc.z = fmaf(wt, ov.z, acc.z);
-      acc.w = fmaf(wt, ov.w, acc.w);
-    }
-    const float inv = s_row[64 + r];
-    uint16_t* dst = a.out + ((size_t)i * a.Hq + (size_t)grp * rows + r) * D + d;
-    uint2 pk;
-    pk.x = pack2<kBF16>(acc.x * inv, acc.y * inv);
-    pk.y = pack2<kBF16>(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(dst) = pk;
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");   // s_row is reused by the next merge
 }
 
 // ---------------------------------------------------------------------------
@@ -739,9 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long* const scan_tmp = reinterpret_cast<long long*>(gbase + ctrl_words);
   int* const ctrl = reinterpret_cast<int*>(gbase + ctrl_words + kScanBytes);
   volatile int* const abort_flag = ctrl + 4;
-  float* const s_row = reinterpret_cast<float*>(gbase + ctrl_words + kScanBytes + kCtrlBytes);
-  int* const s_len = reinterpret_cast<int*>(gbase + ctrl_words + kScanBytes + kCtrlBytes +
-                                            kRowScratchBytes);
+  int* const s_len = reinterpret_cast<int*>(gbase + ctrl_words + kScanBytes + kCtrlBytes);
 
   if (tid == 0) {
     ctrl[0] = -1;
@@ -1102,7 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int owed = pm[0];
     for (int k = 0; k < owed; ++k)
       merge_split<D, kBF16>(a, pm[1 + 4 * k], pm[2 + 4 * k], start + pm[3 + 4 * k],
-                            pm[4 + 4 * k], cpc, s_row);
+                            pm[4 + 4 * k], cpc);
   }
 }
 
