@@ -734,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty + 8 * s, kCWarps);
     }
     for (int s = 0; s < kQBufs; ++s) {
-      mbar_init(bar_qfull + 8 * s, 1);
+      mbar_init(bar_qfull + 8 * s, 32);   // one arrival per producer lane
       mbar_init(bar_qempty + 8 * s, kCWarps);
     }
     *abort_flag = 0;
@@ -846,7 +846,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   w0.c = ctrl[2];
   walk_load_seq(w0, a, s_len);
 
-  const int qbytes = a.q_bytes;
   const uint32_t box_bytes = 1u << a.sub_log2;
 
   if (warp == kProducerWarp) {
@@ -886,14 +885,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         {
-          // one bulk copy per query row, into rows q_pitch apart
+          // the rows by 16-byte asynchronous copies into rows q_pitch apart
+          // (one TMA bulk copy per row would queue dozens of small copies in
+          // front of the next chunk's); every lane arrives once its own
+          // copies have landed
+          constexpr int kPR = D * 2 / 16;   // 16-byte pieces per row
           const uint32_t qdst = base + a.q_off + (uint32_t)qb * a.q_stride;
-          const uint16_t* qsrc = a.q + ((size_t)w.i * a.Hq + (size_t)w.g * a.HG * a.G) * D;
-          if (lane == 0) mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)qbytes);
-          __syncwarp();
-          for (int r = lane; r < a.HG * a.G; r += 32)
-            bulk_load(qdst + (uint32_t)(r * q_pitch<D>()), qsrc + (size_t)r * D, D * 2,
-                      bar_qfull + 8 * qb);
+          const char* qsrc = reinterpret_cast<const char*>(
+              a.q + ((size_t)w.i * a.Hq + (size_t)w.g * a.HG * a.G) * D);
+          for (int e = lane; e < a.HG * a.G * kPR; e += 32) {
+            const int r = e / kPR, c = e % kPR;
+            cp_async16(qdst + (uint32_t)(r * q_pitch<D>() + c * 16), qsrc + (size_t)e * 16);
+          }
+          cp_async_arrive_noinc(bar_qfull + 8 * qb);
         }
         __syncwarp();
         ++seg;
