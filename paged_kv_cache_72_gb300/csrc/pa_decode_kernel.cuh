@@ -758,6 +758,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (size_t o = t0; o < sl_bytes; o += step) prefetch_l2(sl + o);
     for (size_t o = t0; o < bt_bytes; o += step) prefetch_l2(bt + o);
     if (kMode != kModeGather) {
+      // the split-context counters: a piece's count waits on its line
+      const char* wc = reinterpret_cast<const char*>(a.ws_count);
+      for (size_t o = t0; o < (size_t)gridDim.x * 4; o += step) prefetch_l2(wc + o);
       const char* qp = reinterpret_cast<const char*>(a.q);
       const size_t q_bytes = (size_t)a.num_seqs * a.Hq * D * 2;
       for (size_t o = t0; o < q_bytes; o += step) prefetch_l2(qp + o);
@@ -1054,12 +1057,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long g0 = start + n - w.c;   // global index of the context's chunk 0
             const int first = (int)(g0 / cpc), last = (int)((g0 + w.nc - 1) / cpc);
             uint32_t* cnt = a.ws_count + last;
-            __threadfence();   // release this CTA's record
             if (*abort_flag) atomicOr(cnt, kPieceAborted);
-            const uint32_t now = atomicAdd(cnt, 1u) + 1u;
+            // releases this CTA's record (ordered before by the barrier) and
+            // acquires those of the pieces counted before it
+            const uint32_t now = atom_add_acq_rel_gpu(cnt, 1u) + 1u;
             if ((now & ~kPieceAborted) == (uint32_t)(last - first + 1)) {
               *cnt = 0u;         // every piece is in: ready for the next call
-              __threadfence();   // acquire the other pieces' records
               if (!(now & kPieceAborted)) {
                 int* pm = ctrl + kCtrlMerges;
                 const int k = pm[0]++;

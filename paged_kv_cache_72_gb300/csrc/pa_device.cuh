@@ -129,6 +129,15 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Atomic add with acquire-release semantics at GPU scope: the caller's
+// earlier writes (and those ordered before it by a CTA barrier) are released
+// with it, and the writes released by earlier adds are acquired.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
