@@ -46,7 +46,24 @@ namespace pa {
 constexpr int kTile = 16;          // tokens per consumer warp per stage
 constexpr int kCWarps = 8;         // consumer warps; stage = kCWarps * 16 token-heads
 constexpr int kProducerWarp = kCWarps;
-constexpr int kThreads = (kCWarps + 1) * 32;
+enum Mode : int { kModeSimt = 0, kModeMma = 1, kModeGather = 2 };
+
+// A block of nine warps has three on one SM sub-partition, which leaves
+// every thread at most 168 registers.  The 16-bit tensor-core consumer needs
+// more: its blocks put the producer in a warpgroup of its own (three more
+// warps that leave at once), and the two warpgroups re-divide the registers
+// the block is launched with (setmaxnreg): the producer's group keeps
+// kProducerRegs per thread, the consumers take kConsumerRegs.  The other
+// consumers run best as they are, in nine-warp blocks.
+constexpr int kLaunchRegs = 168;     // 65536 / 384, rounded down to a multiple of 8
+constexpr int kProducerRegs = 56;
+constexpr int kConsumerRegs = 224;
+static_assert(kCWarps * 32 * kConsumerRegs + 128 * kProducerRegs <= (kCWarps + 4) * 32 * kLaunchRegs,
+              "the register split must fit in what the block is launched with");
+__host__ __device__ constexpr bool split_regs(int mode, bool f8) { return mode == kModeMma && !f8; }
+__host__ __device__ constexpr int block_threads(int mode, bool f8) {
+  return (kCWarps + (split_regs(mode, f8) ? 4 : 1)) * 32;
+}
 constexpr int kQBufs = 2;          // query-row buffers in flight
 // Query rows sit in shared memory at a pitch of one row plus 16 bytes, so
 // that the fragment loads of rows a full row apart fall in different banks.
@@ -65,7 +82,6 @@ constexpr int kCtrlEmpty = 14;     // this CTA owns empty or invalid sequences (
 // counter bit set by a piece whose CTA gave up: the context is left unmerged
 constexpr uint32_t kPieceAborted = 0x80000000u;
 
-enum Mode : int { kModeSimt = 0, kModeMma = 1, kModeGather = 2 };
 
 struct DecodeArgs {
   const uint16_t* q;         // [N][Hq][D]
@@ -146,6 +162,7 @@ __device__ __forceinline__ void walk_advance(Walk& w, const DecodeArgs& a, const
 }
 
 // Block-wide inclusive scan of one value per thread (kThreads threads).
+template <int kThreads>
 __device__ __forceinline__ long long block_scan_incl(long long v, long long* warp_tot,
                                                      long long& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -643,70 +660,121 @@ __device__ __forceinline__ void gather_tile(const DecodeArgs& a, uint32_t kpart,
 // each in record slot 0 except the first CTA's when the context began after
 // that CTA's own first chunk (then it is that CTA's second segment, slot 1):
 //   out = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k.
-// One pass: D / 16 threads share a row, each owning 16 of its head_dim
-// columns, and fold the pieces in with the online rescaling, loading a
-// piece's (m, l) and its 16 o values together, so that a merge waits on L2
-// about once per piece rather than once per step.  Consumer threads only;
-// the records come from other CTAs, so they are read from L2 (ld.global.cg).
+// D / 16 threads share a row, each owning 16 of its head_dim columns, and
+// fold pieces in with the online rescaling, a piece's (m, l) and 16 o values
+// loaded together.  When one set of rows x D / 16 threads leaves room, up to
+// 256 / set sets take every set-th piece in parallel and their partial
+// states are combined through shared memory (scratch: the stage buffers,
+// idle once the loop is done).  Consumer threads only; the records come
+// from other CTAs, so they are read from L2 (ld.global.cg).
 // ---------------------------------------------------------------------------
-template <int D, bool kBF16>
-__device__ __forceinline__ void merge_split(const DecodeArgs& a, int i, int grp, long long g0,
-                                            int nc, long long cpc) {
-  const int tid = threadIdx.x;   // consumer threads 0 .. kCWarps * 32 - 1
-  constexpr int kTPR = D / 16;   // threads per row
-  constexpr int kRowsPerPass = kCWarps * 32 / kTPR;
-  const int first = (int)(g0 / cpc);
-  const int last = (int)((g0 + nc - 1) / cpc);
-  const int rows = a.HG * a.G;
-  const size_t rf = rec_floats(rows, D);
-  const size_t ml = (size_t)rows * D;   // m[] then l[] follow o[][]
-  const int d = (tid % kTPR) * 16;
-  for (int r = tid / kTPR; r < rows; r += kRowsPerPass) {
-    float m = -INFINITY, l = 0.f;
-    float4 acc[4];
+template <int D>
+struct MergeState {
+  float m = -INFINITY, l = 0.f;
+  float4 acc[4];
+  __device__ __forceinline__ MergeState() {
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = first; k <= last; ++k) {
+  }
+  // fold in a partial state (mk, lk, ok) with weight 2^(mk - m*)
+  __device__ __forceinline__ void fold(float mk, float lk, const float4* ok) {
+    if (mk == -INFINITY) return;
+    const float mn = fmaxf(m, mk);
+    const float so = exp2f(m - mn), sn = exp2f(mk - mn);   // so = 0 while m = -inf
+    l = l * so + lk * sn;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      acc[c].x = acc[c].x * so + ok[c].x * sn;
+      acc[c].y = acc[c].y * so + ok[c].y * sn;
+      acc[c].z = acc[c].z * so + ok[c].z * sn;
+      acc[c].w = acc[c].w * so + ok[c].w * sn;
+    }
+    m = mn;
+  }
+};
+
+// Not inlined, with scalar arguments: its registers stay out of the
+// allocation of the kernel's main loop.
+template <int D, bool kBF16>
+__device__ __forceinline__ void merge_split(uint16_t* out, const float* ws_rec, int Hq, int rows,
+                                         int i, int grp, long long g0, int nc, long long cpc,
+                                         float* scratch) {
+  const int tid = threadIdx.x;   // consumer threads 0 .. kCWarps * 32 - 1
+  constexpr int kThr = kCWarps * 32;
+  constexpr int kTPR = D / 16;   // threads per row
+  const int first = (int)(g0 / cpc);
+  const int last = (int)((g0 + nc - 1) / cpc);
+  const size_t rf = rec_floats(rows, D);
+  const size_t ml = (size_t)rows * D;   // m[] then l[] follow o[][]
+  const int set = rows * kTPR;
+  int nsets = set <= kThr ? kThr / set : 1;
+  if (nsets > last - first + 1) nsets = last - first + 1;
+  const int d = (tid % kTPR) * 16;
+  auto fold_pieces = [&](MergeState<D>& st, int r, int k0, int step) {
+    for (int k = k0; k <= last; k += step) {
       const int slot = (k == first && g0 != (long long)first * cpc) ? 1 : 0;
-      const float* rec = a.ws_rec + ((size_t)k * 2 + slot) * rf;
+      const float* rec = ws_rec + ((size_t)k * 2 + slot) * rf;
       const float mk = __ldcg(rec + ml + r), lk = __ldcg(rec + ml + rows + r);
       float4 ok[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         ok[c] = __ldcg(reinterpret_cast<const float4*>(rec + (size_t)r * D + d + 4 * c));
-      if (mk != -INFINITY) {
-        const float mn = fmaxf(m, mk);
-        const float so = exp2f(m - mn), sn = exp2f(mk - mn);   // so = 0 while m = -inf
-        l = l * so + lk * sn;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          acc[c].x = acc[c].x * so + ok[c].x * sn;
-          acc[c].y = acc[c].y * so + ok[c].y * sn;
-          acc[c].z = acc[c].z * so + ok[c].z * sn;
-          acc[c].w = acc[c].w * so + ok[c].w * sn;
-        }
-        m = mn;
-      }
+      st.fold(mk, lk, ok);
     }
-    const float inv = 1.f / l;
+  };
+  auto write_row = [&](const MergeState<D>& st, int r) {
+    const float inv = 1.f / st.l;
     uint4 pk[2];
     uint32_t* w = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      w[2 * c] = pack2<kBF16>(acc[c].x * inv, acc[c].y * inv);
-      w[2 * c + 1] = pack2<kBF16>(acc[c].z * inv, acc[c].w * inv);
+      w[2 * c] = pack2<kBF16>(st.acc[c].x * inv, st.acc[c].y * inv);
+      w[2 * c + 1] = pack2<kBF16>(st.acc[c].z * inv, st.acc[c].w * inv);
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)i * a.Hq + (size_t)grp * rows + r) * D + d);
+    uint4* dst =
+        reinterpret_cast<uint4*>(out + ((size_t)i * Hq + (size_t)grp * rows + r) * D + d);
     dst[0] = pk[0];
     dst[1] = pk[1];
+  };
+  if (nsets <= 1) {
+    for (int r = tid / kTPR; r < rows; r += kThr / kTPR) {
+      MergeState<D> st;
+      fold_pieces(st, r, first, 1);
+      write_row(st, r);
+    }
+    return;
   }
+  // several sets: set q folds pieces first + q, first + q + nsets, ...; its
+  // state for row r goes to scratch[(q * rows + r) * (D + 4)]: o[D], m, l
+  const int q = tid / set, r = (tid % set) / kTPR;
+  if (q < nsets) {
+    MergeState<D> st;
+    fold_pieces(st, r, first + q, nsets);
+    float* sp = scratch + (size_t)(q * rows + r) * (D + 4);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) *reinterpret_cast<float4*>(sp + d + 4 * c) = st.acc[c];
+    if (d == 0) {
+      sp[D] = st.m;
+      sp[D + 1] = st.l;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kThr) : "memory");
+  if (tid < set) {
+    MergeState<D> st;
+    for (int p = 0; p < nsets; ++p) {
+      const float* sp = scratch + (size_t)(p * rows + r) * (D + 4);
+      st.fold(sp[D], sp[D + 1], reinterpret_cast<const float4*>(sp + d));
+    }
+    write_row(st, r);
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kThr) : "memory");   // scratch is reused by the next merge
 }
 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16, int kMode, bool kSwz, bool kHi, bool kF8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(block_threads(kMode, kF8), 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -715,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
 
+  constexpr int kThreads = block_threads(kMode, kF8);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = a.stages;
   const uint32_t bar_full = base + a.ctrl_off;      // S x 8 bytes
@@ -798,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   long long total_nc;
-  const long long my_excl = block_scan_incl(my_nc, scan_tmp, total_nc) - my_nc;
+  const long long my_excl = block_scan_incl<kThreads>(my_nc, scan_tmp, total_nc) - my_nc;
   const long long U = total_nc * a.NGR;
   const long long cpc = (U + gridDim.x - 1) / gridDim.x;
   const long long start = (long long)blockIdx.x * cpc;
@@ -851,7 +920,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t box_bytes = 1u << a.sub_log2;
 
-  if (warp == kProducerWarp) {
+  if (warp >= kCWarps) {
+    if constexpr (split_regs(kMode, kF8)) {
+      setmaxnreg_dec<kProducerRegs>();
+      if (warp != kProducerWarp) return;
+    }
     // ======================= producer =======================
     const uint64_t pol = policy_evict_first();
     Walk w = w0;
@@ -962,6 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= consumers =======================
+  if constexpr (split_regs(kMode, kF8)) setmaxnreg_inc<kConsumerRegs>();
   // out and the workspace may be touched by the preceding kernel
   if (a.early_tables) grid_dep_wait();
   using Mma = typename std::conditional<kF8, MmaConsumerF8<D, kBF16, kSwz, kHi>,
@@ -1092,8 +1166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int* pm = ctrl + kCtrlMerges;
     const int owed = pm[0];
     for (int k = 0; k < owed; ++k)
-      merge_split<D, kBF16>(a, pm[1 + 4 * k], pm[2 + 4 * k], start + pm[3 + 4 * k],
-                            pm[4 + 4 * k], cpc);
+      merge_split<D, kBF16>(a.out, a.ws_rec, a.Hq, a.HG * a.G, pm[1 + 4 * k], pm[2 + 4 * k],
+                            start + pm[3 + 4 * k], pm[4 + 4 * k], cpc,
+                            reinterpret_cast<float*>(gbase));
   }
 }
 

@@ -129,6 +129,18 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Re-divide the registers of a block between warpgroups: every warp of a
+// warpgroup executes the same one.  The increases must fit in what the
+// decreases and the launch left free, or the increasing warps wait.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Atomic add with acquire-release semantics at GPU scope: the caller's
 // earlier writes (and those ordered before it by a CTA barrier) are released
 // with it, and the writes released by earlier adds are acquired.
