@@ -40,6 +40,7 @@ DATASHEET_HBM_GBS = 7900.0   # nominal GB300 HBM3e figure, for context only
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_decode_fp8.cuh", "pa_device.cuh",
                   "pa_decode_variants.cuh", "pa_decode.cu"]
+PREFILL_SOURCES = ["pa_prefill.cu", "pa_device.cuh"]
 
 
 # --------------------------------------------------------------------------
@@ -97,15 +98,16 @@ def measured_peaks(key="hbm_gbs"):
     return (FALLBACK_HBM_GBS if key == "hbm_gbs" else FALLBACK_BF16_TFLOPS), "fallback"
 
 
-def kernel_sha():
+def kernel_sha(sources=KERNEL_SOURCES):
+    """Short hash of the sources of the kernel a traffic record was taken on."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "paged_kv_cache_72_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, prefill=False):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
@@ -114,7 +116,8 @@ def recorded_traffic(workload):
     with open(p) as f:
         d = json.load(f)
     rec = d.get(workload)
-    if not rec or rec.get("kernel_sha") != kernel_sha():
+    sources = PREFILL_SOURCES if prefill else KERNEL_SOURCES
+    if not rec or rec.get("kernel_sha") != kernel_sha(sources):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -379,7 +382,7 @@ def run_gpu(args, rank, world, local_rank):
 
     peak, peak_kind = measured_peaks()
     achieved = nbytes["decode"] / (dms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload, prefill=wl.query_start is not None)
     if wl.query_start is not None:
         # a dense contraction: its roofline is the tensor rate (the kernel
         # timed alone: the burst figure)
