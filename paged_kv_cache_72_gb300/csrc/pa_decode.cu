@@ -380,6 +380,53 @@ int encode_pool_map(CUtensorMap* map, const void* cache, const DecodePlan& p, in
   return encode_kv_map(map, cache, p, Hkv, num_blocks, true);
 }
 
+// One 64-column plane of R rows of one head of one block, 128-byte swizzled:
+// copies of the two planes of a box land apart, so that a stage part holds
+// [plane][row][128 bytes] (the K-major and MN-major operand layouts of the
+// tensor-core prefill).
+int encode_pool_plane_map(CUtensorMap* map, const void* cache, bool bf16, int D, int B, int R,
+                          int Hkv, long long num_blocks) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return PA_ERR_CUDA;
+  const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
+  const cuuint64_t dims[5] = {64, (cuuint64_t)B, (cuuint64_t)(D / 64), (cuuint64_t)Hkv,
+                              (cuuint64_t)num_blocks};
+  const cuuint64_t strides[4] = {row, 128, (cuuint64_t)D * 2, row * B};
+  const cuuint32_t box[5] = {64, (cuuint32_t)R, 1, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   5, const_cast<void*>(cache), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) return PA_OK;
+  note_cuda_error(1000 + (int)r, "cuTensorMapEncodeTiled (pool plane)");
+  return PA_ERR_CUDA;
+}
+
+// The query rows of one work item: BM tokens x the G heads of one KV head, one
+// 64-column plane per copy, landing as [token][head][128 bytes] with a
+// 128-byte swizzle.  Rows past total_q read as zeros.
+int encode_q_tile_map(CUtensorMap* map, const void* q, bool bf16, int D, int G, int Hkv,
+                      long long total_q, int BM) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return PA_ERR_CUDA;
+  const cuuint64_t dims[5] = {64, (cuuint64_t)(D / 64), (cuuint64_t)G, (cuuint64_t)Hkv,
+                              (cuuint64_t)total_q};
+  const cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)G * D * 2,
+                                 (cuuint64_t)Hkv * G * D * 2};
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)G, 1, (cuuint32_t)BM};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   5, const_cast<void*>(q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) return PA_OK;
+  note_cuda_error(1000 + (int)r, "cuTensorMapEncodeTiled (query tile)");
+  return PA_ERR_CUDA;
+}
+
 }  // namespace pa
 
 using namespace pa;

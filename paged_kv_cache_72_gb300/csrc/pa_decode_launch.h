@@ -27,6 +27,11 @@ struct DecodePlan {
 // TMA map over one 16-bit pool (split-row layout) for other kernels.
 int encode_pool_map(CUtensorMap* map, const void* cache, const DecodePlan& p, int Hkv,
                     long long num_blocks);
+// Per-plane pool map and query-tile map of the tensor-core prefill.
+int encode_pool_plane_map(CUtensorMap* map, const void* cache, bool bf16, int D, int B, int R,
+                          int Hkv, long long num_blocks);
+int encode_q_tile_map(CUtensorMap* map, const void* q, bool bf16, int D, int G, int Hkv,
+                      long long total_q, int BM);
 
 // Per-variant occupancy (CTAs per SM) for a given dynamic shared-memory size.
 int decode_ctas_per_sm(const DecodePlan& p, int* ctas);

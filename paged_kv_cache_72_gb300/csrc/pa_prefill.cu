@@ -57,6 +57,7 @@ struct PrefillArgs {
   int sub_log2, hi_log2;        // in a stage part: box j at j << sub_log2, 64-column plane at
                                 // hi << hi_log2, row r at r << 7
   int kv_bytes, stage_bytes, ctrl_off;
+  int q_off, p_off, q_tx;       // tensor-core kernel: query and P buffers, bytes of one query tile
 };
 
 struct Item {
@@ -104,7 +105,8 @@ __device__ __forceinline__ uint32_t swz_chunk(uint32_t row, int j) {
   return row + ((uint32_t)(j ^ (int)((row >> 7) & 7)) << 4);
 }
 
-// Block-wide exclusive scan of one value per thread (kPThreads threads).
+// Block-wide exclusive scan of one value per thread (NT threads).
+template <int NT>
 __device__ __forceinline__ long long scan_excl(long long v, long long* tmp, long long& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   long long x = v;
@@ -118,12 +120,54 @@ __device__ __forceinline__ long long scan_excl(long long v, long long* tmp, long
   long long off = 0;
   total = 0;
 #pragma unroll
-  for (int w = 0; w < kPThreads / 32; ++w) {
+  for (int w = 0; w < NT / 32; ++w) {
     if (w < warp) off += tmp[w];
     total += tmp[w];
   }
   __syncthreads();
   return off + x - v;
+}
+
+// Item offsets: each thread sums the tiles of a run of sequences, one block
+// scan gives toff[] and the item count.  A sequence whose length lies outside
+// its table, or with more new tokens than tokens, is reported and its rows get
+// zeros.  Ends with a block barrier.
+template <int NT, int D>
+__device__ __forceinline__ void item_offsets(const PrefillArgs& a, int* toff, long long* scan_tmp,
+                                             int* total_items_s) {
+  const int tid = threadIdx.x;
+  const int per = (a.num_seqs + NT - 1) / NT;
+  const int run0 = min(a.num_seqs, tid * per), run1 = min(a.num_seqs, run0 + per);
+  long long mine = 0;
+  for (int i = run0; i < run1; ++i) {
+    const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
+    const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
+    const bool ok = L >= 0 && T >= 0 && L <= T;
+    if (ok) mine += (long long)((L + a.BM - 1) / a.BM) * a.Hkv;
+    if ((i % gridDim.x) == blockIdx.x && !ok) {
+      // a length outside its table, or more new tokens than tokens: reported,
+      // and its rows get zeros
+      set_error(a.err, PA_DEVERR_SEQ_LEN);
+      if (L > 0) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(
+            a.out + (size_t)__ldg(a.query_start + i) * a.Hq * D);
+        for (long long e = 0; e < (long long)L * a.Hq * D / 2; ++e) dst[e] = 0u;
+      }
+    }
+  }
+  long long total;
+  long long off = scan_excl<NT>(mine, scan_tmp, total);
+  for (int i = run0; i < run1; ++i) {
+    toff[i] = (int)off;
+    const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
+    const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
+    if (L >= 0 && T >= 0 && L <= T) off += (long long)((L + a.BM - 1) / a.BM) * a.Hkv;
+  }
+  if (tid == 0) {
+    toff[a.num_seqs] = (int)total;
+    *total_items_s = (int)total;
+  }
+  __syncthreads();
 }
 
 template <int D, bool kBF16>
@@ -159,39 +203,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
   grid_dep_wait();
 
-  // ---- item offsets: each thread sums the tiles of a run of sequences
-  const int per = (a.num_seqs + kPThreads - 1) / kPThreads;
-  const int run0 = min(a.num_seqs, tid * per), run1 = min(a.num_seqs, run0 + per);
-  long long mine = 0;
-  for (int i = run0; i < run1; ++i) {
-    const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
-    const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
-    const bool ok = L >= 0 && T >= 0 && L <= T;
-    if (ok) mine += (long long)((L + a.BM - 1) / a.BM) * a.Hkv;
-    if ((i % gridDim.x) == blockIdx.x && !ok) {
-      // a length outside its table, or more new tokens than tokens: reported,
-      // and its rows get zeros
-      set_error(a.err, PA_DEVERR_SEQ_LEN);
-      if (L > 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(
-            a.out + (size_t)__ldg(a.query_start + i) * a.Hq * D);
-        for (long long e = 0; e < (long long)L * a.Hq * D / 2; ++e) dst[e] = 0u;
-      }
-    }
-  }
-  long long total;
-  long long off = scan_excl(mine, scan_tmp, total);
-  for (int i = run0; i < run1; ++i) {
-    toff[i] = (int)off;
-    const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
-    const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
-    if (L >= 0 && T >= 0 && L <= T) off += (long long)((L + a.BM - 1) / a.BM) * a.Hkv;
-  }
-  if (tid == 0) {
-    toff[a.num_seqs] = (int)total;
-    *total_items_s = (int)total;
-  }
-  __syncthreads();
+  item_offsets<kPThreads, D>(a, toff, scan_tmp, total_items_s);
   if (tid == 0) grid_dep_launch();
   const int total_items = *total_items_s;
 
@@ -443,9 +455,464 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core (tcgen05) variant.  The same work items (128 query rows of one
+// KV head) and the same producer walk, with the contraction on the fifth-
+// generation tensor cores and the accumulators in tensor memory:
+//  * warps 0-3 (softmax): thread r owns query row r, which is TMEM lane r.
+//    Per 64-key stage it reads its row of S, masks it, updates the running
+//    maximum and sum, and writes its row of P (16-bit) to shared memory.  The
+//    maximum used for the exponentials moves only when a row's maximum passes
+//    it by more than kTcTau (log2 units): then the row of O is rescaled in
+//    TMEM; otherwise P stays below 2^kTcTau and O, l and the stale maximum
+//    stay consistent (the result is their quotient).  At an item's end it
+//    reads O, divides by l and writes the rows.
+//  * warp 4 (producer): items from the atomic counter; per item the query
+//    tile by TMA (one copy per 64-column plane, [row][128 bytes], 128-byte
+//    swizzle), per stage the K and V planes of the item's KV head, tagged with
+//    the item.
+//  * warp 5 (MMA, one thread): S = Q . K^T (M 128, N 64, K = head_dim) into
+//    one of two S buffers in TMEM, then O += P . V (M 128, N head_dim, K 64,
+//    V as an MN-major operand) for the stage before, so that the tensor core
+//    computes a stage's scores while the softmax works on the previous one.
+// Tensor memory: S buffers at columns 0 and 64, O at 128.  Every wait is
+// bounded; a wait that gives up sets PA_DEVERR_TIMEOUT and the roles leave.
+// ---------------------------------------------------------------------------
+constexpr int kTcWarps = 6;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcProducer = 4;
+constexpr int kTcMma = 5;
+constexpr uint32_t kTcTmemCols = 256;
+constexpr float kTcTau = 8.f;
+constexpr int kTcBars = 12;   // q full/empty, s full/free, p full/empty (two each), o free, done
+
+constexpr int kTcToffBytes = ((4 * (kPMaxSeqs + 1) + 15) / 16) * 16;
+
+// shared-memory control area of the tensor-core kernel (after the P buffers):
+// full/empty barriers, the other barriers, stage tags, TMEM address and
+// flags, item offsets, scan scratch
+__host__ __device__ constexpr int tc_ctrl_bytes(int S) {
+  return 16 * S + 8 * kTcBars + 16 * S + 16 + kTcToffBytes + 8 * (kTcThreads / 32);
+}
+
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                            const __grid_constant__ CUtensorMap tmv,
+                            const __grid_constant__ CUtensorMap tmq, const PrefillArgs a) {
+  constexpr int NP = D / 64;          // 64-column planes of a row
+  constexpr uint32_t kQPlane = 16384; // 128 rows x 128 bytes
+  constexpr uint32_t kKPlane = 8192;  // 64 keys x 128 bytes
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = a.stages;
+  const uint32_t bar_full = base + a.ctrl_off;      // S
+  const uint32_t bar_empty = bar_full + 8 * S;      // S
+  const uint32_t bar_q = bar_empty + 8 * S;         // qfull[2], qempty[2]
+  const uint32_t bar_s = bar_q + 32;                // sfull[2], sfree[2]
+  const uint32_t bar_p = bar_s + 32;                // pfull[2], pempty[2]
+  const uint32_t bar_ofree = bar_p + 32;
+  const uint32_t bar_done = bar_ofree + 8;
+  uint8_t* const cgen = gbase + a.ctrl_off + 16 * S + 8 * kTcBars;
+  int4* const meta = reinterpret_cast<int4*>(cgen);                         // [S]
+  uint32_t* const tslot = reinterpret_cast<uint32_t*>(cgen + 16 * S);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  int* const total_items_s = reinterpret_cast<int*>(tslot + 2);
+  int* const toff = reinterpret_cast<int*>(cgen + 16 * S + 16);             // [N + 1]
+  long long* const scan_tmp = reinterpret_cast<long long*>(cgen + 16 * S + 16 + kTcToffBytes);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);       // one commit of the MMA thread
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_q + 8 * b, 1);           // q full: the producer's expect-tx
+      mbar_init(bar_q + 16 + 8 * b, 1);      // q empty: a commit
+      mbar_init(bar_s + 8 * b, 1);           // s full: a commit
+      mbar_init(bar_s + 16 + 8 * b, 128);    // s free: the softmax threads
+      mbar_init(bar_p + 8 * b, 128);         // p full: the softmax threads
+      mbar_init(bar_p + 16 + 8 * b, 1);      // p empty: a commit
+    }
+    mbar_init(bar_ofree, 128);
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kTcProducer && lane == 0) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+    prefetch_tensormap(&tmq);
+  }
+  if (warp == kTcMma) {
+    tmem_alloc(smem_u32(tslot), kTcTmemCols);
+    tc_fence_before();
+  }
+  grid_dep_wait();
+  item_offsets<kTcThreads, D>(a, toff, scan_tmp, total_items_s);   // ends with a barrier
+  tc_fence_after();
+  if (tid == 0) grid_dep_launch();
+  const int total_items = *total_items_s;
+  const uint32_t tmem = *tslot;
+
+  // a wait whose outcome is the same in every lane of the warp
+  auto wait_warp = [&](uint32_t bar, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag)) != 0;
+  };
+
+  if (warp == kTcProducer) {
+    // ======================= producer =======================
+    // K and V are read again by the sequence's other token tiles: keep them
+    // in L2; a query tile is read once
+    const uint64_t pol_kv = policy_evict_last();
+    const uint64_t pol_q = policy_evict_first();
+    const uint32_t box_bytes = (uint32_t)a.R * 128u;
+    int j = 0, n = 0, nq = 0;   // stages issued, items started, query tiles issued
+    bool stop = false;
+    while (!stop) {
+      int item = 0;
+      if (lane == 0) item = (int)atomicAdd(a.ws, 1u);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      Item it;
+      if (item < total_items) decode_item(item, toff, a, it);
+      else stop = true;
+      const int n_kt = stop ? 1 : it.n_kt;
+      for (int kt = 0; kt < n_kt; ++kt) {
+        const int st = j % S;
+        bool ok_wait = wait_warp(bar_empty + 8 * st, ((uint32_t)(j / S) & 1u) ^ 1u);
+        if (ok_wait && !stop && kt == 0)   // the item's query buffer is free
+          ok_wait = wait_warp(bar_q + 16 + 8 * (n & 1), ((uint32_t)(n >> 1) & 1u) ^ 1u);
+        if (!ok_wait) {
+          if (lane == 0 && !*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
+          if (lane == 0) *abort_flag = 1;
+        }
+        __syncwarp();
+        if (*abort_flag) {   // the other roles leave on the flag
+          stop = true;
+          break;
+        }
+        if (stop) {
+          // tell the others to finish: a stage that carries no item
+          if (lane == 0) {
+            meta[st] = make_int4(-1, 0, 0, 0);
+            mbar_arrive(bar_full + 8 * st);
+          }
+          break;
+        }
+        if (kt == 0) {
+          const int qb = n & 1;
+          const uint32_t qdst = base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane;
+          if (lane == 0) mbar_arrive_expect_tx(bar_q + 8 * qb, (uint32_t)a.q_tx);
+          __syncwarp();
+          if (lane < NP)
+            tma_load_5d(qdst + (uint32_t)lane * kQPlane, &tmq, bar_q + 8 * qb, 0, lane, 0, it.h,
+                        it.q0, pol_q);
+          ++nq;
+        }
+        const int tok0 = kt * kPBN + lane * a.R;
+        int ent = -1;
+        bool ok = false;
+        if (lane < a.nsb && tok0 < it.T) {
+          ent = __ldg(a.bt + (size_t)it.i * a.stride + (tok0 >> a.log2B));
+          ok = ent >= 0 && (long long)ent < a.num_blocks;
+          if (!ok) set_error(a.err, PA_DEVERR_BLOCK_ID);
+        }
+        const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) {
+          meta[st] = make_int4(item, kt, it.n_kt, n);
+          mbar_arrive_expect_tx(bar_full + 8 * st,
+                                (uint32_t)__popc(okmask) * box_bytes * (uint32_t)(2 * NP));
+        }
+        __syncwarp();
+        if (ok) {
+          const uint32_t kdst = base + (uint32_t)st * a.stage_bytes + (uint32_t)lane * box_bytes;
+          const int row_off = tok0 & (a.B - 1);
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            tma_load_5d(kdst + (uint32_t)p * kKPlane, &tmk, bar_full + 8 * st, 0, row_off, p, it.h,
+                        ent, pol_kv);
+            tma_load_5d(kdst + (uint32_t)(a.kv_bytes + p * kKPlane), &tmv, bar_full + 8 * st, 0,
+                        row_off, p, it.h, ent, pol_kv);
+          }
+        }
+        ++j;
+      }
+      if (!stop) ++n;
+    }
+    // after an abort, drain: no TMA write may land in shared memory after the
+    // CTA exits
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+      for (int k = max(0, j - S); k < j; ++k)
+        mbar_wait_bounded(bar_full + 8 * (k % S), (uint32_t)(k / S) & 1u, nullptr);
+      for (int k = max(0, nq - 2); k < nq; ++k)
+        mbar_wait_bounded(bar_q + 8 * (k & 1), (uint32_t)(k >> 1) & 1u, nullptr);
+    }
+  } else if (warp == kTcMma) {
+    // ======================= MMA issue (one thread) =======================
+    if (lane == 0) {
+      constexpr uint32_t id_s = umma_idesc_f16(kBF16, 128, kPBN, false);
+      constexpr uint32_t id_o = umma_idesc_f16(kBF16, 128, D, true);
+      bool ok = true;
+      int j = 0;
+      bool have_prev = false;
+      int pj = 0, pst = 0, pkt = 0, pn = 0;   // the stage whose O += P . V is still to issue
+      // O += P . V of the previous stage: P (128 x 64, K-major) from its
+      // buffer, V (64 keys x D, MN-major: 64-column planes kKPlane apart, 8-key
+      // groups 1024 bytes apart); the first stage of an item overwrites O
+      // once the item before has been written out
+      auto issue_pv = [&]() -> bool {
+        const int pb = pj & 1;
+        if (!mbar_wait_bounded(bar_p + 8 * pb, (uint32_t)(pj >> 1) & 1u, abort_flag)) return false;
+        if (pkt == 0 && pn >= 1 &&
+            !mbar_wait_bounded(bar_ofree, (uint32_t)(pn - 1) & 1u, abort_flag))
+          return false;
+        tc_fence_after();
+        const uint32_t pbuf = base + (uint32_t)a.p_off + (uint32_t)pb * 16384u;
+        const uint32_t vpart = base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes;
+#pragma unroll
+        for (int k = 0; k < kPBN / 16; ++k)
+          umma_f16(tmem + 128, umma_desc_sw128(pbuf + 32u * k, 16, 1024),
+                   umma_desc_sw128(vpart + 2048u * k, kKPlane, 1024), id_o, pkt > 0 || k > 0);
+        umma_commit(bar_p + 16 + 8 * pb);   // P buffer free, O updated
+        umma_commit(bar_empty + 8 * pst);   // the stage's K and V are no longer read
+        return true;
+      };
+      while (true) {
+        const int st = j % S;
+        if (!mbar_wait_bounded(bar_full + 8 * st, (uint32_t)(j / S) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int4 md = meta[st];
+        if (md.x < 0) break;
+        const int kt = md.y, nkt = md.z, n = md.w, qb = n & 1, sb = j & 1;
+        if (kt == 0 && !mbar_wait_bounded(bar_q + 8 * qb, (uint32_t)(n >> 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        // the S buffer's previous scores have been read
+        if (j >= 2 &&
+            !mbar_wait_bounded(bar_s + 16 + 8 * sb, (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // S = Q . K^T: K steps of 16 columns; within a 64-column plane a step
+        // moves the start 32 bytes (the swizzle is applied to the address)
+        const uint32_t qbuf = base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane;
+        const uint32_t kpart = base + (uint32_t)st * a.stage_bytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (uint32_t)(ks & 3) * 32u;
+          umma_f16(tmem + (uint32_t)sb * kPBN,
+                   umma_desc_sw128(qbuf + (uint32_t)(ks >> 2) * kQPlane + off, 16, 1024),
+                   umma_desc_sw128(kpart + (uint32_t)(ks >> 2) * kKPlane + off, 16, 1024), id_s,
+                   ks > 0);
+        }
+        umma_commit(bar_s + 8 * sb);
+        if (kt == nkt - 1) umma_commit(bar_q + 16 + 8 * qb);   // the query tile is free
+        if (have_prev && !issue_pv()) {
+          ok = false;
+          break;
+        }
+        have_prev = true;
+        pj = j;
+        pst = st;
+        pkt = kt;
+        pn = n;
+        ++j;
+      }
+      if (ok && have_prev && !issue_pv()) ok = false;
+      if (!ok) {
+        if (!*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // every MMA issued has completed before the tensor memory is released
+      umma_commit(bar_done);
+      mbar_wait_bounded(bar_done, 0u, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax (warps 0-3) =======================
+    const int r = tid;   // this thread's query row, TMEM lane r
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    const float sl2 = a.scale_log2;
+    Item it{};
+    int prow = -1;         // the row's position (-1: a padding row)
+    bool valid = false;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    int j = 0;
+    while (true) {
+      const int st = j % S, sb = j & 1;
+      if (!wait_warp(bar_full + 8 * st, (uint32_t)(j / S) & 1u)) {
+        ok = false;
+        break;
+      }
+      const int4 md = meta[st];
+      if (md.x < 0) break;
+      const int kt = md.y, nkt = md.z;
+      if (kt == 0) {
+        decode_item(md.x, toff, a, it);
+        const int tok = r / a.G;
+        valid = r < a.BM * a.G && tok < it.ntok;
+        prow = valid ? it.p0 + tok : -1;
+        m_used = -INFINITY;
+        l = 0.f;
+      }
+      // ---- this row of S
+      if (!wait_warp(bar_s + 8 * sb, (uint32_t)(j >> 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[kPBN];
+      tmem_ld32(trow + (uint32_t)sb * kPBN, *reinterpret_cast<uint32_t(*)[32]>(sr));
+      tmem_ld32(trow + (uint32_t)sb * kPBN + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_s + 16 + 8 * sb);   // the S buffer may be overwritten
+      // ---- causal mask (a padding row keeps finite scores against cached
+      // keys), scale, maximum
+      const int tb = kt * kPBN;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kPBN; ++c) {
+        const int t = tb + c;
+        const bool in = prow >= 0 ? t <= prow : t < it.T;
+        const float v = in ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+        sr[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      float alpha = 1.f;
+      if (mx > m_used + kTcTau) {   // the exponentials' reference moves
+        if (m_used != -INFINITY) alpha = exp2f(m_used - mx);
+        m_used = mx;
+      }
+      const float mu = m_used == -INFINITY ? 0.f : m_used;   // no row is masked whole at kt 0
+      // ---- P = 2^(s - m_used), 16-bit, and its row sum
+      uint32_t pk[kPBN / 2];
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kPBN / 2; ++c) {
+        const float p0 = exp2f(__uint_as_float(sr[2 * c]) - mu);
+        const float p1 = exp2f(__uint_as_float(sr[2 * c + 1]) - mu);
+        pk[c] = pack2<kBF16>(p0, p1);
+        const float2 f = unpack2<kBF16>(pk[c]);
+        sum += f.x + f.y;
+      }
+      l = l * alpha + sum;
+      // the P buffer's previous use (two stages back) is done
+      if (j >= 2 && !wait_warp(bar_p + 16 + 8 * sb, (uint32_t)((j >> 1) - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      {
+        // row r of P, K-major with the 128-byte swizzle: 16-byte chunk c at
+        // chunk c ^ (r & 7)
+        const uint32_t prow_addr = base + (uint32_t)a.p_off + (uint32_t)sb * 16384u + (uint32_t)r * 128u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           prow_addr + (uint32_t)((c ^ (r & 7)) << 4)),
+                       "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                       : "memory");
+      }
+      // ---- rescale this warp's rows of O once the previous stage's
+      // O += P . V is done (alpha = 1 leaves a row unchanged)
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!wait_warp(bar_p + 16 + 8 * ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(trow + 128u + (uint32_t)cc, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(trow + 128u + (uint32_t)cc, o);
+        }
+        tmem_wait_st();
+      }
+      // ---- keys past the sequence's end hold no data (NaN, possibly): their
+      // V rows are cleared so that P = 0 multiplies zeros
+      if (tb + kPBN > it.T) {
+        const int z0 = max(0, it.T - tb);
+        const int per_plane = (kPBN - z0) * 8;   // 16-byte pieces
+        const uint32_t vpart = base + (uint32_t)st * a.stage_bytes + (uint32_t)a.kv_bytes;
+        for (int e = tid; e < per_plane * NP; e += 128) {
+          const int p = e / per_plane, rem = e - p * per_plane;
+          const uint32_t addr =
+              vpart + (uint32_t)p * kKPlane + (uint32_t)(z0 + (rem >> 3)) * 128u + (uint32_t)(rem & 7) * 16u;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+        }
+      }
+      fence_proxy_async_smem();   // P and the cleared rows, before the tensor core reads them
+      tc_fence_before();
+      mbar_arrive(bar_p + 8 * sb);
+      if (kt == nkt - 1) {
+        // ---- the item's last stage: out = O / l once O += P . V is done
+        if (!wait_warp(bar_p + 16 + 8 * sb, (uint32_t)(j >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float inv = 1.f / l;
+        uint16_t* orow =
+            a.out + ((size_t)(it.q0 + (valid ? r / a.G : 0)) * a.Hq + (size_t)it.h * a.G + r % a.G) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(trow + 128u + (uint32_t)cc, o);
+          tmem_wait_ld();
+          if (valid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack2<kBF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint4*>(orow + cc + 8 * q4) =
+                  make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_ofree);   // O may be overwritten by the next item
+      }
+      ++j;
+    }
+    if (!ok) {
+      if (lane == 0 && !*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
+      if (lane == 0) *abort_flag = 1;
+    }
+  }
+
+  // ---- teardown: release the tensor memory (every MMA has completed)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kTcMma) tmem_dealloc(tmem, kTcTmemCols);
+  // the last CTA to finish resets the work counters for the next call
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.ws + 1, 1u) == gridDim.x - 1) {
+      a.ws[0] = 0u;
+      a.ws[1] = 0u;
+      __threadfence();
+    }
+  }
+}
+
 struct PrefillPlan {
-  bool bf16;
+  bool bf16, tc;
   int D, G, B, R, nsb, BM, stages, kv_bytes, stage_bytes, ctrl_off, smem_bytes, grid;
+  int q_off, p_off, q_tx;
 };
 
 int ctrl_bytes(int S) { return 32 * S + 4 * (kPMaxSeqs + 1) + 12 + 16 * 8 + 16; }
@@ -458,6 +925,62 @@ int prepare_kernel(const PrefillPlan& p, int smem_optin, int* per_sm) {
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, paged_prefill_kernel<D, BF>,
                                                     kPThreads, p.smem_bytes);
   return launch_status(e, "occupancy query (prefill)");
+}
+
+template <int D, bool BF>
+int prepare_tc_kernel(const PrefillPlan& p, int smem_optin, int* per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel<D, BF>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+  if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute (tensor-core prefill)");
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, paged_prefill_tc_kernel<D, BF>,
+                                                    kTcThreads, p.smem_bytes);
+  return launch_status(e, "occupancy query (tensor-core prefill)");
+}
+
+// Plan of the tensor-core kernel: 64-key stages whose K and V parts are
+// [plane][64 keys][128 bytes]; each 64-column plane of a block's rows is one
+// TMA box of R rows, which must start on 1024 bytes (the 128-byte swizzle), so
+// blocks of fewer than 8 tokens take the warp-level kernel.
+int make_tc_plan(int Hq, int Hkv, int D, int B, int dtype, PrefillPlan* out) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (!is_pow2(B) || B < 8 || B > 256) return PA_ERR_UNSUPPORTED;
+  PrefillPlan p{};
+  p.tc = true;
+  p.bf16 = dtype == PA_BF16;
+  p.D = D;
+  p.G = Hq / Hkv;
+  if (p.G > 16) return PA_ERR_UNSUPPORTED;
+  p.B = B;
+  p.R = B < kPBN ? B : kPBN;
+  p.nsb = kPBN / p.R;
+  p.BM = kPRows / p.G;
+  p.kv_bytes = kPBN * D * 2;
+  p.stage_bytes = 2 * p.kv_bytes;
+  const int qbuf = (D / 64) * 16384;
+  DeviceInfo di;
+  if (int rc = current_device_info(&di)) return rc;
+  int st = (di.smem_per_block - 1024 - 2 * qbuf - 32768 - tc_ctrl_bytes(kPMaxStages)) /
+           p.stage_bytes;
+  if (st > kPMaxStages) st = kPMaxStages;
+  if (st < 2) return PA_ERR_UNSUPPORTED;
+  p.stages = st;
+  p.q_off = st * p.stage_bytes;
+  p.p_off = p.q_off + 2 * qbuf;
+  p.ctrl_off = p.p_off + 32768;
+  p.smem_bytes = 1024 + p.ctrl_off + tc_ctrl_bytes(st);
+  p.q_tx = (D / 64) * 128 * p.G * p.BM;
+  int per_sm = 0;
+  int rc = D == 64 ? (p.bf16 ? prepare_tc_kernel<64, true>(p, di.smem_per_block, &per_sm)
+                             : prepare_tc_kernel<64, false>(p, di.smem_per_block, &per_sm))
+                   : (p.bf16 ? prepare_tc_kernel<128, true>(p, di.smem_per_block, &per_sm)
+                             : prepare_tc_kernel<128, false>(p, di.smem_per_block, &per_sm));
+  if (rc != PA_OK) return rc;
+  if (per_sm < 1) return PA_ERR_UNSUPPORTED;
+  p.grid = di.sm_count * per_sm;
+  *out = p;
+  return PA_OK;
 }
 
 int make_plan(int Hq, int Hkv, int D, int B, int dtype, PrefillPlan* out) {
@@ -519,8 +1042,15 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
                int64_t num_blocks, int32_t dtype, float scale, void* out, void* workspace,
                size_t workspace_bytes, int32_t* err_word, pa_stream stream) {
   if (num_seqs < 0 || total_q < 0 || table_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  // the tensor-core kernel where its staging layout allows (blocks of 8 or
+  // more tokens), else the warp-level one
   PrefillPlan p;
-  if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, &p)) return rc;
+  const int rc_tc = make_tc_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, &p);
+  if (rc_tc == PA_ERR_UNSUPPORTED) {
+    if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, &p)) return rc;
+  } else if (rc_tc != PA_OK) {
+    return rc_tc;
+  }
   if (num_seqs == 0 || total_q == 0) return PA_OK;
   if (num_seqs > kPMaxSeqs) return PA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start || !out ||
@@ -531,16 +1061,27 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
       !aligned16(workspace))
     return PA_ERR_INVALID_ARG;
   if (workspace_bytes < 256) return PA_ERR_WORKSPACE;
-  DecodePlan mp{};
-  mp.bf16 = p.bf16;
-  mp.D = p.D;
-  mp.B = p.B;
-  mp.R = p.R;
-  mp.HG = 1;
-  mp.swz = true;
-  CUtensorMap tk, tv;
-  if (int rc = encode_pool_map(&tk, k_cache, mp, num_kv_heads, num_blocks)) return rc;
-  if (int rc = encode_pool_map(&tv, v_cache, mp, num_kv_heads, num_blocks)) return rc;
+  CUtensorMap tk, tv, tq;
+  if (p.tc) {
+    if (int rc = encode_pool_plane_map(&tk, k_cache, p.bf16, p.D, p.B, p.R, num_kv_heads,
+                                       num_blocks))
+      return rc;
+    if (int rc = encode_pool_plane_map(&tv, v_cache, p.bf16, p.D, p.B, p.R, num_kv_heads,
+                                       num_blocks))
+      return rc;
+    if (int rc = encode_q_tile_map(&tq, q, p.bf16, p.D, p.G, num_kv_heads, total_q, p.BM))
+      return rc;
+  } else {
+    DecodePlan mp{};
+    mp.bf16 = p.bf16;
+    mp.D = p.D;
+    mp.B = p.B;
+    mp.R = p.R;
+    mp.HG = 1;
+    mp.swz = true;
+    if (int rc = encode_pool_map(&tk, k_cache, mp, num_kv_heads, num_blocks)) return rc;
+    if (int rc = encode_pool_map(&tv, v_cache, mp, num_kv_heads, num_blocks)) return rc;
+  }
   PrefillArgs a{};
   a.q = static_cast<const uint16_t*>(q);
   a.out = static_cast<uint16_t*>(out);
@@ -568,9 +1109,23 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
   a.kv_bytes = p.kv_bytes;
   a.stage_bytes = p.stage_bytes;
   a.ctrl_off = p.ctrl_off;
+  a.q_off = p.q_off;
+  a.p_off = p.p_off;
+  a.q_tx = p.q_tx;
   clear_stale_error();
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (p.tc) {
+    const dim3 g(p.grid), b(kTcThreads);
+    const size_t sm = (size_t)p.smem_bytes;
+    if (p.D == 64)
+      e = p.bf16 ? launch_pdl(paged_prefill_tc_kernel<64, true>, g, b, sm, s, tk, tv, tq, a)
+                 : launch_pdl(paged_prefill_tc_kernel<64, false>, g, b, sm, s, tk, tv, tq, a);
+    else
+      e = p.bf16 ? launch_pdl(paged_prefill_tc_kernel<128, true>, g, b, sm, s, tk, tv, tq, a)
+                 : launch_pdl(paged_prefill_tc_kernel<128, false>, g, b, sm, s, tk, tv, tq, a);
+    return launch_status(e, "tensor-core prefill kernel launch");
+  }
   if (p.D == 64)
     e = p.bf16 ? launch_pdl(paged_prefill_kernel<64, true>, dim3(p.grid), dim3(kPThreads),
                             (size_t)p.smem_bytes, s, tk, tv, a)
