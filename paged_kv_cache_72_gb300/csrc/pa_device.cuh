@@ -216,6 +216,13 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 2^x by the SFU's approximation (relative error about 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Re-divide the registers of a block between warpgroups: every warp of a
 // warpgroup executes the same one.  The increases must fit in what the
 // decreases and the launch left free, or the increasing warps wait.

@@ -776,33 +776,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       mbar_arrive(bar_s + 16 + 8 * sb);   // the S buffer may be overwritten
       // ---- causal mask (a padding row keeps finite scores against cached
-      // keys), scale, maximum
+      // keys) and maximum.  A stage wholly at or before the item's first
+      // position needs no mask, and with a positive scale its maximum is
+      // taken on the raw scores; otherwise the scores are scaled first.
       const int tb = kt * kPBN;
-      float mx = -INFINITY;
+      float mx = -INFINITY, f = 1.f;
+      if (tb + kPBN - 1 <= it.p0 && sl2 > 0.f) {
 #pragma unroll
-      for (int c = 0; c < kPBN; ++c) {
-        const int t = tb + c;
-        const bool in = prow >= 0 ? t <= prow : t < it.T;
-        const float v = in ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-        sr[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < kPBN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        mx *= sl2;
+        f = sl2;
+      } else {
+#pragma unroll
+        for (int c = 0; c < kPBN; ++c) {
+          const int t = tb + c;
+          const bool in = prow >= 0 ? t <= prow : t < it.T;
+          const float v = in ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+          sr[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
       }
       float alpha = 1.f;
       if (mx > m_used + kTcTau) {   // the exponentials' reference moves
-        if (m_used != -INFINITY) alpha = exp2f(m_used - mx);
+        if (m_used != -INFINITY) alpha = ex2_approx(m_used - mx);
         m_used = mx;
       }
       const float mu = m_used == -INFINITY ? 0.f : m_used;   // no row is masked whole at kt 0
-      // ---- P = 2^(s - m_used), 16-bit, and its row sum
+      // ---- P = 2^(s f - m_used), one FFMA and one ex2 per score, 16-bit;
+      // its row sum in fp32
       uint32_t pk[kPBN / 2];
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < kPBN / 2; ++c) {
-        const float p0 = exp2f(__uint_as_float(sr[2 * c]) - mu);
-        const float p1 = exp2f(__uint_as_float(sr[2 * c + 1]) - mu);
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), f, -mu));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), f, -mu));
         pk[c] = pack2<kBF16>(p0, p1);
-        const float2 f = unpack2<kBF16>(pk[c]);
-        sum += f.x + f.y;
+        sum += p0 + p1;
       }
       l = l * alpha + sum;
       // the P buffer's previous use (two stages back) is done
