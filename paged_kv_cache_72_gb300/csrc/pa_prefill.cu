@@ -486,13 +486,19 @@ constexpr uint32_t kTcTmemCols = 256;
 constexpr float kTcTau = 8.f;
 constexpr int kTcBars = 12;   // q full/empty, s full/free, p full/empty (two each), o free, done
 
-constexpr int kTcToffBytes = ((4 * (kPMaxSeqs + 1) + 15) / 16) * 16;
+// One query-tile buffer and one P buffer: their shared memory goes to K/V
+// stages instead (a CTA has as many 64-key stages in flight as fit).
+constexpr int kTcQB = 1;
+constexpr int kTcPB = 1;
+__host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
+  return ((4 * (num_seqs + 1) + 15) / 16) * 16;
+}
 
 // shared-memory control area of the tensor-core kernel (after the P buffers):
 // full/empty barriers, the other barriers, stage tags, TMEM address and
 // flags, item offsets, scan scratch
-__host__ __device__ constexpr int tc_ctrl_bytes(int S) {
-  return 16 * S + 8 * kTcBars + 16 * S + 16 + kTcToffBytes + 8 * (kTcThreads / 32);
+__host__ __device__ constexpr int tc_ctrl_bytes(int S, int num_seqs) {
+  return 16 * S + 8 * kTcBars + 16 * S + 16 + tc_toff_bytes(num_seqs) + 8 * (kTcThreads / 32);
 }
 
 template <int D, bool kBF16>
@@ -522,7 +528,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   int* const total_items_s = reinterpret_cast<int*>(tslot + 2);
   int* const toff = reinterpret_cast<int*>(cgen + 16 * S + 16);             // [N + 1]
-  long long* const scan_tmp = reinterpret_cast<long long*>(cgen + 16 * S + 16 + kTcToffBytes);
+  long long* const scan_tmp =
+      reinterpret_cast<long long*>(cgen + 16 * S + 16 + tc_toff_bytes(a.num_seqs));
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -580,11 +587,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (item < total_items) decode_item(item, toff, a, it);
       else stop = true;
       const int n_kt = stop ? 1 : it.n_kt;
+      // block-table entries two stages ahead of their copies (lane l < nsb:
+      // the block of the stage's l-th box), so that the producer does not
+      // wait on each entry's load
+      auto load_ent = [&](int kt) -> int {
+        const int tok0 = kt * kPBN + lane * a.R;
+        return (lane < a.nsb && tok0 < it.T)
+                   ? __ldg(a.bt + (size_t)it.i * a.stride + (tok0 >> a.log2B))
+                   : -1;
+      };
+      int e0 = stop ? -1 : load_ent(0);
+      int e1 = (stop || n_kt < 2) ? -1 : load_ent(1);
       for (int kt = 0; kt < n_kt; ++kt) {
+        const int ent = e0;
+        e0 = e1;
+        e1 = kt + 2 < n_kt ? load_ent(kt + 2) : -1;
         const int st = j % S;
         bool ok_wait = wait_warp(bar_empty + 8 * st, ((uint32_t)(j / S) & 1u) ^ 1u);
         if (ok_wait && !stop && kt == 0)   // the item's query buffer is free
-          ok_wait = wait_warp(bar_q + 16 + 8 * (n & 1), ((uint32_t)(n >> 1) & 1u) ^ 1u);
+          ok_wait = wait_warp(bar_q + 16 + 8 * (n % kTcQB), ((uint32_t)(n / kTcQB) & 1u) ^ 1u);
         if (!ok_wait) {
           if (lane == 0 && !*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
           if (lane == 0) *abort_flag = 1;
@@ -603,7 +624,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         if (kt == 0) {
-          const int qb = n & 1;
+          const int qb = n % kTcQB;
           const uint32_t qdst = base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane;
           if (lane == 0) mbar_arrive_expect_tx(bar_q + 8 * qb, (uint32_t)a.q_tx);
           __syncwarp();
@@ -613,10 +634,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++nq;
         }
         const int tok0 = kt * kPBN + lane * a.R;
-        int ent = -1;
         bool ok = false;
         if (lane < a.nsb && tok0 < it.T) {
-          ent = __ldg(a.bt + (size_t)it.i * a.stride + (tok0 >> a.log2B));
           ok = ent >= 0 && (long long)ent < a.num_blocks;
           if (!ok) set_error(a.err, PA_DEVERR_BLOCK_ID);
         }
@@ -647,85 +666,97 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (__any_sync(0xffffffffu, *abort_flag != 0)) {
       for (int k = max(0, j - S); k < j; ++k)
         mbar_wait_bounded(bar_full + 8 * (k % S), (uint32_t)(k / S) & 1u, nullptr);
-      for (int k = max(0, nq - 2); k < nq; ++k)
-        mbar_wait_bounded(bar_q + 8 * (k & 1), (uint32_t)(k >> 1) & 1u, nullptr);
+      for (int k = max(0, nq - kTcQB); k < nq; ++k)
+        mbar_wait_bounded(bar_q + 8 * (k % kTcQB), (uint32_t)(k / kTcQB) & 1u, nullptr);
     }
   } else if (warp == kTcMma) {
     // ======================= MMA issue (one thread) =======================
+    // An event loop: the next stage's S = Q . K^T is issued as soon as its
+    // K/V have landed (and its query tile, and a free S buffer), and the
+    // oldest pending O += P . V as soon as its P is written, whichever comes
+    // first, so that neither waits on the other's inputs.
     if (lane == 0) {
       constexpr uint32_t id_s = umma_idesc_f16(kBF16, 128, kPBN, false);
       constexpr uint32_t id_o = umma_idesc_f16(kBF16, 128, D, true);
+      int4 info[4];           // (stage slot, kt, item number, -) of stages js-3 .. js-1
+      int js = 0, jp = 0;     // next stage to get its S, next to get its P . V
+      bool s_done = false;    // the stop marker was seen
       bool ok = true;
-      int j = 0;
-      bool have_prev = false;
-      int pj = 0, pst = 0, pkt = 0, pn = 0;   // the stage whose O += P . V is still to issue
-      // O += P . V of the previous stage: P (128 x 64, K-major) from its
-      // buffer, V (64 keys x D, MN-major: 64-column planes kKPlane apart, 8-key
-      // groups 1024 bytes apart); the first stage of an item overwrites O
-      // once the item before has been written out
-      auto issue_pv = [&]() -> bool {
-        const int pb = pj & 1;
-        if (!mbar_wait_bounded(bar_p + 8 * pb, (uint32_t)(pj >> 1) & 1u, abort_flag)) return false;
-        if (pkt == 0 && pn >= 1 &&
-            !mbar_wait_bounded(bar_ofree, (uint32_t)(pn - 1) & 1u, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t pbuf = base + (uint32_t)a.p_off + (uint32_t)pb * 16384u;
-        const uint32_t vpart = base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes;
-#pragma unroll
-        for (int k = 0; k < kPBN / 16; ++k)
-          umma_f16(tmem + 128, umma_desc_sw128(pbuf + 32u * k, 16, 1024),
-                   umma_desc_sw128(vpart + 2048u * k, kKPlane, 1024), id_o, pkt > 0 || k > 0);
-        umma_commit(bar_p + 16 + 8 * pb);   // P buffer free, O updated
-        umma_commit(bar_empty + 8 * pst);   // the stage's K and V are no longer read
-        return true;
-      };
+      long long t_last = clock64();
       while (true) {
-        const int st = j % S;
-        if (!mbar_wait_bounded(bar_full + 8 * st, (uint32_t)(j / S) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const int4 md = meta[st];
-        if (md.x < 0) break;
-        const int kt = md.y, nkt = md.z, n = md.w, qb = n & 1, sb = j & 1;
-        if (kt == 0 && !mbar_wait_bounded(bar_q + 8 * qb, (uint32_t)(n >> 1) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        // the S buffer's previous scores have been read
-        if (j >= 2 &&
-            !mbar_wait_bounded(bar_s + 16 + 8 * sb, (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // S = Q . K^T: K steps of 16 columns; within a 64-column plane a step
-        // moves the start 32 bytes (the swizzle is applied to the address)
-        const uint32_t qbuf = base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane;
-        const uint32_t kpart = base + (uint32_t)st * a.stage_bytes;
+        bool progressed = false;
+        if (!s_done && js - jp < 3) {
+          const int st = js % S, sb = js & 1;
+          if (mbar_test(bar_full + 8 * st, (uint32_t)(js / S) & 1u)) {
+            const int4 md = meta[st];
+            if (md.x < 0) {
+              s_done = true;
+            } else {
+              const int kt = md.y, nkt = md.z, n = md.w, qb = n % kTcQB;
+              const bool q_ok = kt != 0 || mbar_test(bar_q + 8 * qb, (uint32_t)(n / kTcQB) & 1u);
+              // the S buffer's scores of two stages back have been read
+              const bool s_ok =
+                  js < 2 || mbar_test(bar_s + 16 + 8 * sb, (uint32_t)((js >> 1) - 1) & 1u);
+              if (q_ok && s_ok) {
+                tc_fence_after();
+                // K steps of 16 columns; within a 64-column plane a step moves
+                // the start 32 bytes (the swizzle is applied to the address)
+                const uint32_t qbuf = base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane;
+                const uint32_t kpart = base + (uint32_t)st * a.stage_bytes;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (uint32_t)(ks & 3) * 32u;
-          umma_f16(tmem + (uint32_t)sb * kPBN,
-                   umma_desc_sw128(qbuf + (uint32_t)(ks >> 2) * kQPlane + off, 16, 1024),
-                   umma_desc_sw128(kpart + (uint32_t)(ks >> 2) * kKPlane + off, 16, 1024), id_s,
-                   ks > 0);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                  const uint32_t off = (uint32_t)(ks & 3) * 32u;
+                  umma_f16(tmem + (uint32_t)sb * kPBN,
+                           umma_desc_sw128(qbuf + (uint32_t)(ks >> 2) * kQPlane + off, 16, 1024),
+                           umma_desc_sw128(kpart + (uint32_t)(ks >> 2) * kKPlane + off, 16, 1024),
+                           id_s, ks > 0);
+                }
+                umma_commit(bar_s + 8 * sb);
+                if (kt == nkt - 1) umma_commit(bar_q + 16 + 8 * qb);   // the query tile is free
+                info[js & 3] = make_int4(st, kt, n, 0);
+                ++js;
+                progressed = true;
+              }
+            }
+          }
         }
-        umma_commit(bar_s + 8 * sb);
-        if (kt == nkt - 1) umma_commit(bar_q + 16 + 8 * qb);   // the query tile is free
-        if (have_prev && !issue_pv()) {
-          ok = false;
-          break;
+        if (jp < js) {
+          // O += P . V: P (128 x 64, K-major) from its buffer, V (64 keys x D,
+          // MN-major: 64-column planes kKPlane apart, 8-key groups 1024 bytes
+          // apart); an item's first stage overwrites O once the item before
+          // has been written out
+          const int4 pi = info[jp & 3];
+          const int pb = jp % kTcPB;
+          if (mbar_test(bar_p + 8 * pb, (uint32_t)(jp / kTcPB) & 1u) &&
+              (pi.y != 0 || pi.z == 0 || mbar_test(bar_ofree, (uint32_t)(pi.z - 1) & 1u))) {
+            tc_fence_after();
+            const uint32_t pbuf = base + (uint32_t)a.p_off + (uint32_t)pb * 16384u;
+            const uint32_t vpart = base + (uint32_t)pi.x * a.stage_bytes + (uint32_t)a.kv_bytes;
+#pragma unroll
+            for (int k = 0; k < kPBN / 16; ++k)
+              umma_f16(tmem + 128, umma_desc_sw128(pbuf + 32u * k, 16, 1024),
+                       umma_desc_sw128(vpart + 2048u * k, kKPlane, 1024), id_o, pi.y > 0 || k > 0);
+            umma_commit(bar_p + 16 + 8 * pb);   // P buffer free, O updated
+            umma_commit(bar_empty + 8 * pi.x);  // the stage's K and V are no longer read
+            ++jp;
+            progressed = true;
+          }
         }
-        have_prev = true;
-        pj = j;
-        pst = st;
-        pkt = kt;
-        pn = n;
-        ++j;
+        if (s_done && jp == js) break;
+        if (progressed) {
+          t_last = clock64();
+        } else {
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          if (clock64() - t_last > kWaitLimitCycles) {
+            ok = false;
+            break;
+          }
+          __nanosleep(20);   // leave the issue slots to the softmax warp beside it
+        }
       }
-      if (ok && have_prev && !issue_pv()) ok = false;
       if (!ok) {
         if (!*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
@@ -815,14 +846,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       l = l * alpha + sum;
       // the P buffer's previous use (two stages back) is done
-      if (j >= 2 && !wait_warp(bar_p + 16 + 8 * sb, (uint32_t)((j >> 1) - 1) & 1u)) {
+      const int pb = j % kTcPB;
+      if (j >= kTcPB && !wait_warp(bar_p + 16 + 8 * pb, (uint32_t)(j / kTcPB - 1) & 1u)) {
         ok = false;
         break;
       }
       {
         // row r of P, K-major with the 128-byte swizzle: 16-byte chunk c at
         // chunk c ^ (r & 7)
-        const uint32_t prow_addr = base + (uint32_t)a.p_off + (uint32_t)sb * 16384u + (uint32_t)r * 128u;
+        const uint32_t prow_addr = base + (uint32_t)a.p_off + (uint32_t)pb * 16384u + (uint32_t)r * 128u;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
@@ -833,7 +865,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ---- rescale this warp's rows of O once the previous stage's
       // O += P . V is done (alpha = 1 leaves a row unchanged)
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!wait_warp(bar_p + 16 + 8 * ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u)) {
+        if (!wait_warp(bar_p + 16 + 8 * ((j - 1) % kTcPB), (uint32_t)((j - 1) / kTcPB) & 1u)) {
           ok = false;
           break;
         }
@@ -864,10 +896,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       fence_proxy_async_smem();   // P and the cleared rows, before the tensor core reads them
       tc_fence_before();
-      mbar_arrive(bar_p + 8 * sb);
+      mbar_arrive(bar_p + 8 * pb);
       if (kt == nkt - 1) {
         // ---- the item's last stage: out = O / l once O += P . V is done
-        if (!wait_warp(bar_p + 16 + 8 * sb, (uint32_t)(j >> 1) & 1u)) {
+        if (!wait_warp(bar_p + 16 + 8 * pb, (uint32_t)(j / kTcPB) & 1u)) {
           ok = false;
           break;
         }
@@ -950,7 +982,7 @@ int prepare_tc_kernel(const PrefillPlan& p, int smem_optin, int* per_sm) {
 // [plane][64 keys][128 bytes]; each 64-column plane of a block's rows is one
 // TMA box of R rows, which must start on 1024 bytes (the 128-byte swizzle), so
 // blocks of fewer than 8 tokens take the warp-level kernel.
-int make_tc_plan(int Hq, int Hkv, int D, int B, int dtype, PrefillPlan* out) {
+int make_tc_plan(int Hq, int Hkv, int D, int B, int dtype, int num_seqs, PrefillPlan* out) {
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
@@ -970,15 +1002,16 @@ int make_tc_plan(int Hq, int Hkv, int D, int B, int dtype, PrefillPlan* out) {
   const int qbuf = (D / 64) * 16384;
   DeviceInfo di;
   if (int rc = current_device_info(&di)) return rc;
-  int st = (di.smem_per_block - 1024 - 2 * qbuf - 32768 - tc_ctrl_bytes(kPMaxStages)) /
+  int st = (di.smem_per_block - 1024 - kTcQB * qbuf - kTcPB * 16384 -
+            tc_ctrl_bytes(kPMaxStages, num_seqs)) /
            p.stage_bytes;
   if (st > kPMaxStages) st = kPMaxStages;
   if (st < 2) return PA_ERR_UNSUPPORTED;
   p.stages = st;
   p.q_off = st * p.stage_bytes;
-  p.p_off = p.q_off + 2 * qbuf;
-  p.ctrl_off = p.p_off + 32768;
-  p.smem_bytes = 1024 + p.ctrl_off + tc_ctrl_bytes(st);
+  p.p_off = p.q_off + kTcQB * qbuf;
+  p.ctrl_off = p.p_off + kTcPB * 16384;
+  p.smem_bytes = 1024 + p.ctrl_off + tc_ctrl_bytes(st, num_seqs);
   p.q_tx = (D / 64) * 128 * p.G * p.BM;
   int per_sm = 0;
   int rc = D == 64 ? (p.bf16 ? prepare_tc_kernel<64, true>(p, di.smem_per_block, &per_sm)
@@ -1054,7 +1087,8 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
   // the tensor-core kernel where its staging layout allows (blocks of 8 or
   // more tokens), else the warp-level one
   PrefillPlan p;
-  const int rc_tc = make_tc_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, &p);
+  const int rc_tc =
+      make_tc_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_seqs, &p);
   if (rc_tc == PA_ERR_UNSUPPORTED) {
     if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, &p)) return rc;
   } else if (rc_tc != PA_OK) {
