@@ -701,15 +701,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after();
                 // K steps of 16 columns; within a 64-column plane a step moves
                 // the start 32 bytes (the swizzle is applied to the address)
-                const uint32_t qbuf = base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane;
-                const uint32_t kpart = base + (uint32_t)st * a.stage_bytes;
+                // (the descriptors' address field is in 16-byte units: a step
+                // adds its offset / 16 to the base descriptor)
+                const uint64_t da = umma_desc_sw128(
+                    base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane, 16, 1024);
+                const uint64_t db = umma_desc_sw128(base + (uint32_t)st * a.stage_bytes, 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                   const uint32_t off = (uint32_t)(ks & 3) * 32u;
                   umma_f16(tmem + (uint32_t)sb * kPBN,
-                           umma_desc_sw128(qbuf + (uint32_t)(ks >> 2) * kQPlane + off, 16, 1024),
-                           umma_desc_sw128(kpart + (uint32_t)(ks >> 2) * kKPlane + off, 16, 1024),
-                           id_s, ks > 0);
+                           da + (((uint32_t)(ks >> 2) * kQPlane + off) >> 4),
+                           db + (((uint32_t)(ks >> 2) * kKPlane + off) >> 4), id_s, ks > 0);
                 }
                 umma_commit(bar_s + 8 * sb);
                 if (kt == nkt - 1) umma_commit(bar_q + 16 + 8 * qb);   // the query tile is free
@@ -730,12 +732,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (mbar_test(bar_p + 8 * pb, (uint32_t)(jp / kTcPB) & 1u) &&
               (pi.y != 0 || pi.z == 0 || mbar_test(bar_ofree, (uint32_t)(pi.z - 1) & 1u))) {
             tc_fence_after();
-            const uint32_t pbuf = base + (uint32_t)a.p_off + (uint32_t)pb * 16384u;
-            const uint32_t vpart = base + (uint32_t)pi.x * a.stage_bytes + (uint32_t)a.kv_bytes;
+            const uint64_t dp =
+                umma_desc_sw128(base + (uint32_t)a.p_off + (uint32_t)pb * 16384u, 16, 1024);
+            const uint64_t dv = umma_desc_sw128(
+                base + (uint32_t)pi.x * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
 #pragma unroll
             for (int k = 0; k < kPBN / 16; ++k)
-              umma_f16(tmem + 128, umma_desc_sw128(pbuf + 32u * k, 16, 1024),
-                       umma_desc_sw128(vpart + 2048u * k, kKPlane, 1024), id_o, pi.y > 0 || k > 0);
+              umma_f16(tmem + 128, dp + 2u * k, dv + 128u * k, id_o, pi.y > 0 || k > 0);
             umma_commit(bar_p + 16 + 8 * pb);   // P buffer free, O updated
             umma_commit(bar_empty + 8 * pi.x);  // the stage's K and V are no longer read
             ++jp;
