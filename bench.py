@@ -393,7 +393,7 @@ def run_gpu(args, rank, world, local_rank):
             "bound": "tensor", "achieved": round(tach, 1), "peak": tpeak, "unit": "TFLOP/s",
             "frac": round(tach / tpeak, 4), "traffic": traffic,
             "peak_source": tkind + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS bf16 burst)",
-            "kernel": "pa_prefill: paged_prefill_kernel (mma.sync m16n8k16)",
+            "kernel": "pa_prefill: paged_prefill_tc_kernel (tcgen05.mma, TMEM accumulators)",
             "algorithmic_flops_per_launch": flops,
             "kv_gbs": round(achieved, 1),
         }
