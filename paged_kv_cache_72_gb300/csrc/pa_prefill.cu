@@ -671,10 +671,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == kTcMma) {
     // ======================= MMA issue (one thread) =======================
-    // An event loop: the next stage's S = Q . K^T is issued as soon as its
-    // K/V have landed (and its query tile, and a free S buffer), and the
-    // oldest pending O += P . V as soon as its P is written, whichever comes
-    // first, so that neither waits on the other's inputs.
+    // An event loop: the oldest pending O += P . V is issued as soon as its P
+    // is written (first: the softmax waits on it to reuse the P buffer), and
+    // the next stage's S = Q . K^T as soon as its K/V have landed (and its
+    // query tile, and a free S buffer), so that neither waits on the other's
+    // inputs.
     if (lane == 0) {
       constexpr uint32_t id_s = umma_idesc_f16(kBF16, 128, kPBN, false);
       constexpr uint32_t id_o = umma_idesc_f16(kBF16, 128, D, true);
@@ -685,6 +686,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       long long t_last = clock64();
       while (true) {
         bool progressed = false;
+        if (jp < js) {
+          // O += P . V: P (128 x 64, K-major) from its buffer, V (64 keys x D,
+          // MN-major: 64-column planes kKPlane apart, 8-key groups 1024 bytes
+          // apart); an item's first stage overwrites O once the item before
+          // has been written out
+          const int4 pi = info[jp & 3];
+          const int pb = jp % kTcPB;
+          if (mbar_test(bar_p + 8 * pb, (uint32_t)(jp / kTcPB) & 1u) &&
+              (pi.y != 0 || pi.z == 0 || mbar_test(bar_ofree, (uint32_t)(pi.z - 1) & 1u))) {
+            tc_fence_after();
+            const uint64_t dp =
+                umma_desc_sw128(base + (uint32_t)a.p_off + (uint32_t)pb * 16384u, 16, 1024);
+            const uint64_t dv = umma_desc_sw128(
+                base + (uint32_t)pi.x * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
+#pragma unroll
+            for (int k = 0; k < kPBN / 16; ++k)
+              umma_f16(tmem + 128, dp + 2u * k, dv + 128u * k, id_o, pi.y > 0 || k > 0);
+            umma_commit(bar_p + 16 + 8 * pb);   // P buffer free, O updated
+            umma_commit(bar_empty + 8 * pi.x);  // the stage's K and V are no longer read
+            ++jp;
+            progressed = true;
+          }
+        }
         if (!s_done && js - jp < 3) {
           const int st = js % S, sb = js & 1;
           if (mbar_test(bar_full + 8 * st, (uint32_t)(js / S) & 1u)) {
@@ -720,29 +744,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 progressed = true;
               }
             }
-          }
-        }
-        if (jp < js) {
-          // O += P . V: P (128 x 64, K-major) from its buffer, V (64 keys x D,
-          // MN-major: 64-column planes kKPlane apart, 8-key groups 1024 bytes
-          // apart); an item's first stage overwrites O once the item before
-          // has been written out
-          const int4 pi = info[jp & 3];
-          const int pb = jp % kTcPB;
-          if (mbar_test(bar_p + 8 * pb, (uint32_t)(jp / kTcPB) & 1u) &&
-              (pi.y != 0 || pi.z == 0 || mbar_test(bar_ofree, (uint32_t)(pi.z - 1) & 1u))) {
-            tc_fence_after();
-            const uint64_t dp =
-                umma_desc_sw128(base + (uint32_t)a.p_off + (uint32_t)pb * 16384u, 16, 1024);
-            const uint64_t dv = umma_desc_sw128(
-                base + (uint32_t)pi.x * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
-#pragma unroll
-            for (int k = 0; k < kPBN / 16; ++k)
-              umma_f16(tmem + 128, dp + 2u * k, dv + 128u * k, id_o, pi.y > 0 || k > 0);
-            umma_commit(bar_p + 16 + 8 * pb);   // P buffer free, O updated
-            umma_commit(bar_empty + 8 * pi.x);  // the stage's K and V are no longer read
-            ++jp;
-            progressed = true;
           }
         }
         if (s_done && jp == js) break;
