@@ -838,7 +838,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const float mu = m_used == -INFINITY ? 0.f : m_used;   // no row is masked whole at kt 0
       // ---- P = 2^(s f - m_used), one FFMA and one ex2 per score, 16-bit;
-      // its row sum in fp32
+      // its row sum in fp32 over the rounded values that O sums, so that a
+      // row dominated by one key keeps that key's value
       uint32_t pk[kPBN / 2];
       float sum = 0.f;
 #pragma unroll
@@ -846,7 +847,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), f, -mu));
         const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), f, -mu));
         pk[c] = pack2<kBF16>(p0, p1);
-        sum += p0 + p1;
+        const float2 pr = unpack2<kBF16>(pk[c]);
+        sum += pr.x + pr.y;
       }
       l = l * alpha + sum;
       // the P buffer's previous use (two stages back) is done

@@ -109,3 +109,39 @@ def test_llama3_chunked_prefill_sampled(cuda_device):
                                    wl.block_tables[i:i + 1], wl.seq_lens[i:i + 1],
                                    np.array([0, q1 - q0], np.int32), wl.scale)
         assert_close(gpu_out_f64(out[q0:q1]), sub, "llama3 chunked prefill seq %d" % i)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_wide_score_range(cuda_device, D):
+    """q, k ~ N(0, 4^2): scores spread over tens of binary orders, so a row's
+    running maximum moves past the kernel's reference many times and its rows
+    of O are rescaled in tensor memory.
+
+    The tolerance adds what the 16-bit P costs on such peaked rows.  With P_i
+    rounded to p_i (1 + d_i), |d_i| <= 2^-9, the output moves by
+    sum_i p_i d_i (v_i - out) / sum_i p_i, at most 2^-9 * 2 max|v|, and its own
+    rounding adds 2^-9 |out| <= 2^-9 max|v|: 3 * 2^-9 * max|v| in all."""
+    wl = W.random_prefill(150 + D, W.BF16, 16, 4, D, 16, [0, 500, 2000, 63], [300, 129, 64, 70],
+                          garbage="nan", q_sigma=4.0, kv_sigma=4.0)
+    st = GpuState(wl)
+    out, _ = gpu_step(st)
+    ref = OracleState(wl)
+    ref.step()
+    expected = ref.decode()
+    assert pa.pa_get_error(st.err) == 0
+    got = gpu_out_f64(out)
+    assert np.all(np.isfinite(got))
+    vmax = max(float(np.abs(oracle.gather_head(ref.v_cache, wl.dtype, wl.block_tables[i],
+                                                   int(wl.seq_lens[i]), h)).max())
+               for i in range(len(wl.seq_lens)) for h in range(wl.num_kv_heads))
+    bound = 4e-3 + 1e-2 * np.abs(expected) + 3 * 2.0 ** -9 * vmax
+    assert np.all(np.abs(got - expected) <= bound), float(np.abs(got - expected).max())
+
+
+def test_prefill_sequences_ending_on_stage_edges(cuda_device):
+    # lengths at, one past and one short of multiples of the 64-key stage, so
+    # the V rows past the end are cleared in some stages and in none of others
+    prefix = [64 - 5, 128 - 1, 191, 256 - 64, 0, 1]
+    chunk = [5, 1, 2, 64, 64, 63]
+    wl = W.random_prefill(160, W.F16, 8, 2, 128, 16, prefix, chunk, garbage="nan")
+    _parity(wl)

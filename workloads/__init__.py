@@ -455,12 +455,13 @@ def prefill_workload(name, dtype, Hq, H_kv, D, B, num_blocks, prefix_lens, chunk
 
 
 def random_prefill(seed, dtype, Hq, H_kv, D, B, prefix_lens, chunk_lens, spare_blocks=7,
-                   garbage="random"):
+                   garbage="random", q_sigma=1.0, kv_sigma=1.0):
     """A chunked-prefill parity case of any shape."""
     lens = np.asarray(prefix_lens) + np.asarray(chunk_lens)
     need = int(sum(-(-int(T) // B) for T in lens))
     return prefill_workload("random-prefill", dtype, Hq, H_kv, D, B, need + spare_blocks,
-                            prefix_lens, chunk_lens, seed, garbage=garbage, recipe="parity case")
+                            prefix_lens, chunk_lens, seed, q_sigma=q_sigma, kv_sigma=kv_sigma,
+                            garbage=garbage, recipe="parity case")
 
 
 def llama3_8b_chunked_prefill(seed=7, num_seqs=16, chunk=512, garbage="random",
