@@ -814,12 +814,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // keys) and maximum.  A stage wholly at or before the item's first
       // position needs no mask, and with a positive scale its maximum is
       // taken on the raw scores; otherwise the scores are scaled first.
+      // (eight partial maxima and sums: one warp per sub-partition leaves no
+      // other warp to hide a 64-long chain of dependent instructions)
       const int tb = kt * kPBN;
-      float mx = -INFINITY, f = 1.f;
-      if (tb + kPBN - 1 <= it.p0 && sl2 > 0.f) {
+      float mx8[8], f = 1.f;
 #pragma unroll
-        for (int c = 0; c < kPBN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-        mx *= sl2;
+      for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
+      const bool raw = tb + kPBN - 1 <= it.p0 && sl2 > 0.f;
+      if (raw) {
+#pragma unroll
+        for (int c = 0; c < kPBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
         f = sl2;
       } else {
 #pragma unroll
@@ -828,9 +832,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const bool in = prow >= 0 ? t <= prow : t < it.T;
           const float v = in ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
           sr[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          mx8[c & 7] = fmaxf(mx8[c & 7], v);
         }
       }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) mx8[c] = fmaxf(mx8[c], mx8[c + 4]);
+      float mx = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+      if (raw) mx *= sl2;
       float alpha = 1.f;
       if (mx > m_used + kTcTau) {   // the exponentials' reference moves
         if (m_used != -INFINITY) alpha = ex2_approx(m_used - mx);
@@ -841,16 +849,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // its row sum in fp32 over the rounded values that O sums, so that a
       // row dominated by one key keeps that key's value
       uint32_t pk[kPBN / 2];
-      float sum = 0.f;
+      float sum8[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) sum8[c] = 0.f;
 #pragma unroll
       for (int c = 0; c < kPBN / 2; ++c) {
         const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), f, -mu));
         const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), f, -mu));
         pk[c] = pack2<kBF16>(p0, p1);
         const float2 pr = unpack2<kBF16>(pk[c]);
-        sum += pr.x + pr.y;
+        sum8[c & 7] += pr.x + pr.y;
       }
-      l = l * alpha + sum;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sum8[c] += sum8[c + 4];
+      l = l * alpha + ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3]));
       // the P buffer's previous use (two stages back) is done
       const int pb = j % kTcPB;
       if (j >= kTcPB && !wait_warp(bar_p + 16 + 8 * pb, (uint32_t)(j / kTcPB - 1) & 1u)) {
