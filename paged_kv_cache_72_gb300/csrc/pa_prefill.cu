@@ -95,6 +95,43 @@ __device__ __forceinline__ void decode_item(int item, const int* toff, const Pre
   it.n_kt = (it.p0 + it.ntok - 1) / kPBN + 1;
 }
 
+// A work item of the tensor-core kernel: two consecutive token tiles A and B of
+// one sequence and KV head, which share the stream of keys (B's keys; A's are a
+// prefix of them).  Pair number -> (sequence, KV head, pair); toff[i] = Hkv *
+// (pairs of sequences < i); within a sequence the pairs run over KV heads, then
+// from the last pair (most keys) to the first.  Tile B is absent (no tokens)
+// when the sequence has an odd number of tiles and this is its first pair.
+struct Pair {
+  int i, h, q0, ntok_a, ntok_b, p0, T, nkt_a, nkt;   // q0, p0: tile A's first q row and
+                                                     // position; stages of A and of the pair
+};
+
+__device__ __forceinline__ void decode_pair(int item, const int* toff, const PrefillArgs& a,
+                                            Pair& it) {
+  int lo = 0, hi = a.num_seqs;   // the largest i with toff[i] <= item
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (toff[mid] <= item) lo = mid;
+    else hi = mid;
+  }
+  const int i = lo;
+  const int pairs = (toff[i + 1] - toff[i]) / a.Hkv;
+  const int r = item - toff[i];
+  const int pr = pairs - 1 - r % pairs;
+  const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
+  const int T = __ldg(a.seq_lens + i);
+  const int ta = 2 * pr * a.BM;   // tile A's first new token
+  it.i = i;
+  it.h = r / pairs;
+  it.q0 = __ldg(a.query_start + i) + ta;
+  it.ntok_a = min(a.BM, L - ta);
+  it.ntok_b = max(0, min(a.BM, L - ta - a.BM));
+  it.p0 = T - L + ta;
+  it.T = T;
+  it.nkt_a = (it.p0 + it.ntok_a - 1) / kPBN + 1;
+  it.nkt = it.ntok_b > 0 ? (it.p0 + a.BM + it.ntok_b - 1) / kPBN + 1 : it.nkt_a;
+}
+
 __device__ __forceinline__ uint32_t stage_row(uint32_t part, int tt, int hi, const PrefillArgs& a) {
   return part + ((uint32_t)(tt >> a.log2R) << a.sub_log2) + ((uint32_t)hi << a.hi_log2) +
          ((uint32_t)(tt & (a.R - 1)) << 7);
@@ -128,11 +165,11 @@ __device__ __forceinline__ long long scan_excl(long long v, long long* tmp, long
   return off + x - v;
 }
 
-// Item offsets: each thread sums the tiles of a run of sequences, one block
-// scan gives toff[] and the item count.  A sequence whose length lies outside
-// its table, or with more new tokens than tokens, is reported and its rows get
-// zeros.  Ends with a block barrier.
-template <int NT, int D>
+// Item offsets: each thread sums the items (kTPI token tiles each) of a run of
+// sequences, one block scan gives toff[] and the item count.  A sequence whose
+// length lies outside its table, or with more new tokens than tokens, is
+// reported and its rows get zeros.  Ends with a block barrier.
+template <int NT, int D, int kTPI>
 __device__ __forceinline__ void item_offsets(const PrefillArgs& a, int* toff, long long* scan_tmp,
                                              int* total_items_s) {
   const int tid = threadIdx.x;
@@ -143,7 +180,7 @@ __device__ __forceinline__ void item_offsets(const PrefillArgs& a, int* toff, lo
     const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
     const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
     const bool ok = L >= 0 && T >= 0 && L <= T;
-    if (ok) mine += (long long)((L + a.BM - 1) / a.BM) * a.Hkv;
+    if (ok) mine += (long long)(((L + a.BM - 1) / a.BM + kTPI - 1) / kTPI) * a.Hkv;
     if ((i % gridDim.x) == blockIdx.x && !ok) {
       // a length outside its table, or more new tokens than tokens: reported,
       // and its rows get zeros
@@ -161,7 +198,8 @@ __device__ __forceinline__ void item_offsets(const PrefillArgs& a, int* toff, lo
     toff[i] = (int)off;
     const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
     const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
-    if (L >= 0 && T >= 0 && L <= T) off += (long long)((L + a.BM - 1) / a.BM) * a.Hkv;
+    if (L >= 0 && T >= 0 && L <= T)
+      off += (long long)(((L + a.BM - 1) / a.BM + kTPI - 1) / kTPI) * a.Hkv;
   }
   if (tid == 0) {
     toff[a.num_seqs] = (int)total;
@@ -203,7 +241,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
   grid_dep_wait();
 
-  item_offsets<kPThreads, D>(a, toff, scan_tmp, total_items_s);
+  item_offsets<kPThreads, D, 1>(a, toff, scan_tmp, total_items_s);
   if (tid == 0) grid_dep_launch();
   const int total_items = *total_items_s;
 
@@ -456,49 +494,55 @@ __global__ void __launch_bounds__(kPThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core (tcgen05) variant.  The same work items (128 query rows of one
-// KV head) and the same producer walk, with the contraction on the fifth-
-// generation tensor cores and the accumulators in tensor memory:
-//  * warps 0-3 (softmax): thread r owns query row r, which is TMEM lane r.
-//    Per 64-key stage it reads its row of S, masks it, updates the running
-//    maximum and sum, and writes its row of P (16-bit) to shared memory.  The
-//    maximum used for the exponentials moves only when a row's maximum passes
-//    it by more than kTcTau (log2 units): then the row of O is rescaled in
-//    TMEM; otherwise P stays below 2^kTcTau and O, l and the stale maximum
-//    stay consistent (the result is their quotient).  At an item's end it
-//    reads O, divides by l and writes the rows.
-//  * warp 4 (producer): items from the atomic counter; per item the query
-//    tile by TMA (one copy per 64-column plane, [row][128 bytes], 128-byte
+// Tensor-core (tcgen05) variant.  A work item is a pair of consecutive token
+// tiles (A, then B: 128 query rows each) of one sequence and KV head; both
+// read the same stream of keys, so every staged K/V byte serves 256 query
+// rows, and the tensor core works on one tile while the other's softmax runs.
+// The contraction runs on the fifth-generation tensor cores with the
+// accumulators in tensor memory:
+//  * warps 0-3 (softmax of tile A) and 4-7 (tile B): thread r of a warpgroup
+//    owns query row r of its tile, which is TMEM lane r.  Per 64-key stage it
+//    reads its row of S, masks it, updates the running maximum and sum, and
+//    writes its row of P (16-bit) to its tile's P buffer.  The maximum used
+//    for the exponentials moves only when a row's maximum passes it by more
+//    than kTcTau (log2 units): then the row of O is rescaled in TMEM;
+//    otherwise P stays below 2^kTcTau and O, l and the stale maximum stay
+//    consistent (the result is their quotient).  At the tile's last stage it
+//    reads O, divides by l and writes the rows.  Tile A needs at most the
+//    pair's stages; its warpgroup skips the others.
+//  * warp 8 (producer): items from the atomic counter; per item the two query
+//    tiles by TMA (one copy per 64-column plane, [row][128 bytes], 128-byte
 //    swizzle), per stage the K and V planes of the item's KV head, tagged with
 //    the item.
-//  * warp 5 (MMA, one thread): S = Q . K^T (M 128, N 64, K = head_dim) into
-//    one of two S buffers in TMEM, then O += P . V (M 128, N head_dim, K 64,
-//    V as an MN-major operand) for the stage before, so that the tensor core
-//    computes a stage's scores while the softmax works on the previous one.
-// Tensor memory: S buffers at columns 0 and 64, O at 128.  Every wait is
-// bounded; a wait that gives up sets PA_DEVERR_TIMEOUT and the roles leave.
+//  * warp 9 (MMA, one thread): per stage S = Q . K^T (M 128, N 64, K =
+//    head_dim) for each tile that reads it, into one of the tile's two S
+//    buffers, and O += P . V (M 128, N head_dim, K 64, V as an MN-major
+//    operand) for each tile once its P is written.
+// Tensor memory: tile t's S buffers at columns 256 t and 256 t + 64, its O at
+// 256 t + 128.  Every wait is bounded; a wait that gives up sets
+// PA_DEVERR_TIMEOUT and the roles leave.
 // ---------------------------------------------------------------------------
-constexpr int kTcWarps = 6;
+constexpr int kTcWarps = 10;
 constexpr int kTcThreads = kTcWarps * 32;
-constexpr int kTcProducer = 4;
-constexpr int kTcMma = 5;
-constexpr uint32_t kTcTmemCols = 256;
+constexpr int kTcProducer = 8;
+constexpr int kTcMma = 9;
+constexpr uint32_t kTcTmemCols = 512;
 constexpr float kTcTau = 8.f;
-constexpr int kTcBars = 12;   // q full/empty, s full/free, p full/empty (two each), o free, done
+// barriers (8 bytes each): q full, q empty; per tile s full[2], s free[2],
+// p full, p empty, o free (and one spare) = 8; done; one spare
+constexpr int kTcBars = 2 + 2 * 8 + 2;
 
-// One query-tile buffer and one P buffer: their shared memory goes to K/V
-// stages instead (a CTA has as many 64-key stages in flight as fit).
-constexpr int kTcQB = 1;
-constexpr int kTcPB = 1;
 __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
   return ((4 * (num_seqs + 1) + 15) / 16) * 16;
 }
 
 // shared-memory control area of the tensor-core kernel (after the P buffers):
-// full/empty barriers, the other barriers, stage tags, TMEM address and
-// flags, item offsets, scan scratch
+// full/empty/seen barriers, the other barriers, stage tags (two int4 per
+// stage, from a 16-byte boundary), TMEM address and flags, item offsets, scan
+// scratch
+__host__ __device__ constexpr int tc_tags_off(int S) { return (24 * S + 8 * kTcBars + 15) & ~15; }
 __host__ __device__ constexpr int tc_ctrl_bytes(int S, int num_seqs) {
-  return 16 * S + 8 * kTcBars + 16 * S + 16 + tc_toff_bytes(num_seqs) + 8 * (kTcThreads / 32);
+  return tc_tags_off(S) + 32 * S + 16 + tc_toff_bytes(num_seqs) + 8 * (kTcThreads / 32);
 }
 
 template <int D, bool kBF16>
@@ -517,34 +561,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int S = a.stages;
   const uint32_t bar_full = base + a.ctrl_off;      // S
   const uint32_t bar_empty = bar_full + 8 * S;      // S
-  const uint32_t bar_q = bar_empty + 8 * S;         // qfull[2], qempty[2]
-  const uint32_t bar_s = bar_q + 32;                // sfull[2], sfree[2]
-  const uint32_t bar_p = bar_s + 32;                // pfull[2], pempty[2]
-  const uint32_t bar_ofree = bar_p + 32;
-  const uint32_t bar_done = bar_ofree + 8;
-  uint8_t* const cgen = gbase + a.ctrl_off + 16 * S + 8 * kTcBars;
+  // S: every softmax warp has read the stage's tag.  A warpgroup skips the
+  // stages its tile does not read, so the MMA thread can release them without
+  // it; the producer refills a stage only once it is also seen, so that no
+  // warpgroup waits on a stage that has already been refilled.
+  const uint32_t bar_seen = bar_empty + 8 * S;
+  const uint32_t bar_qfull = bar_seen + 8 * S;
+  const uint32_t bar_qempty = bar_qfull + 8;
+  // tile t's barriers: s full[2] at +0, s free[2] at +16, p full at +32,
+  // p empty at +40, o free at +48
+  const uint32_t bar_tile0 = bar_qfull + 16;
+  const uint32_t bar_done = bar_tile0 + 128;
+  uint8_t* const cgen = gbase + a.ctrl_off + tc_tags_off(S);
   int4* const meta = reinterpret_cast<int4*>(cgen);                         // [S]
-  uint32_t* const tslot = reinterpret_cast<uint32_t*>(cgen + 16 * S);
+  int4* const meta2 = reinterpret_cast<int4*>(cgen + 16 * S);               // [S]
+  uint32_t* const tslot = reinterpret_cast<uint32_t*>(cgen + 32 * S);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   int* const total_items_s = reinterpret_cast<int*>(tslot + 2);
-  int* const toff = reinterpret_cast<int*>(cgen + 16 * S + 16);             // [N + 1]
+  int* const toff = reinterpret_cast<int*>(cgen + 32 * S + 16);             // [N + 1]
   long long* const scan_tmp =
-      reinterpret_cast<long long*>(cgen + 16 * S + 16 + tc_toff_bytes(a.num_seqs));
+      reinterpret_cast<long long*>(cgen + 32 * S + 16 + tc_toff_bytes(a.num_seqs));
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);       // one commit of the MMA thread
+      mbar_init(bar_seen + 8 * s, 8);        // one arrival per softmax warp
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_q + 8 * b, 1);           // q full: the producer's expect-tx
-      mbar_init(bar_q + 16 + 8 * b, 1);      // q empty: a commit
-      mbar_init(bar_s + 8 * b, 1);           // s full: a commit
-      mbar_init(bar_s + 16 + 8 * b, 128);    // s free: the softmax threads
-      mbar_init(bar_p + 8 * b, 128);         // p full: the softmax threads
-      mbar_init(bar_p + 16 + 8 * b, 1);      // p empty: a commit
+    mbar_init(bar_qfull, 1);                 // the producer's expect-tx
+    mbar_init(bar_qempty, 1);                // a commit
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t bt = bar_tile0 + 64 * t;
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(bt + 8 * b, 1);            // s full: a commit
+        mbar_init(bt + 16 + 8 * b, 128);     // s free: the warpgroup's threads
+      }
+      mbar_init(bt + 32, 128);               // p full: the warpgroup's threads
+      mbar_init(bt + 40, 1);                 // p empty: a commit
+      mbar_init(bt + 48, 128);               // o free: the warpgroup's threads
     }
-    mbar_init(bar_ofree, 128);
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -559,7 +614,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
   }
   grid_dep_wait();
-  item_offsets<kTcThreads, D>(a, toff, scan_tmp, total_items_s);   // ends with a barrier
+  item_offsets<kTcThreads, D, 2>(a, toff, scan_tmp, total_items_s);   // ends with a barrier
   tc_fence_after();
   if (tid == 0) grid_dep_launch();
   const int total_items = *total_items_s;
@@ -583,10 +638,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int item = 0;
       if (lane == 0) item = (int)atomicAdd(a.ws, 1u);
       item = __shfl_sync(0xffffffffu, item, 0);
-      Item it;
-      if (item < total_items) decode_item(item, toff, a, it);
+      Pair it;
+      if (item < total_items) decode_pair(item, toff, a, it);
       else stop = true;
-      const int n_kt = stop ? 1 : it.n_kt;
+      const int n_kt = stop ? 1 : it.nkt;
       // block-table entries two stages ahead of their copies (lane l < nsb:
       // the block of the stage's l-th box), so that the producer does not
       // wait on each entry's load
@@ -603,9 +658,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         e0 = e1;
         e1 = kt + 2 < n_kt ? load_ent(kt + 2) : -1;
         const int st = j % S;
-        bool ok_wait = wait_warp(bar_empty + 8 * st, ((uint32_t)(j / S) & 1u) ^ 1u);
-        if (ok_wait && !stop && kt == 0)   // the item's query buffer is free
-          ok_wait = wait_warp(bar_q + 16 + 8 * (n % kTcQB), ((uint32_t)(n / kTcQB) & 1u) ^ 1u);
+        bool ok_wait = wait_warp(bar_empty + 8 * st, ((uint32_t)(j / S) & 1u) ^ 1u) &&
+                       wait_warp(bar_seen + 8 * st, ((uint32_t)(j / S) & 1u) ^ 1u);
+        if (ok_wait && !stop && kt == 0)   // the query tiles' buffers are free
+          ok_wait = wait_warp(bar_qempty, ((uint32_t)n & 1u) ^ 1u);
         if (!ok_wait) {
           if (lane == 0 && !*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
           if (lane == 0) *abort_flag = 1;
@@ -624,13 +680,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         if (kt == 0) {
-          const int qb = n % kTcQB;
-          const uint32_t qdst = base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane;
-          if (lane == 0) mbar_arrive_expect_tx(bar_q + 8 * qb, (uint32_t)a.q_tx);
+          // tile A's rows into buffer 0, tile B's (if it has tokens) into 1
+          const int ntiles = it.ntok_b > 0 ? 2 : 1;
+          if (lane == 0) mbar_arrive_expect_tx(bar_qfull, (uint32_t)(a.q_tx * ntiles));
           __syncwarp();
-          if (lane < NP)
-            tma_load_5d(qdst + (uint32_t)lane * kQPlane, &tmq, bar_q + 8 * qb, 0, lane, 0, it.h,
-                        it.q0, pol_q);
+          if (lane < NP * ntiles) {
+            const int t = lane / NP, pl = lane % NP;
+            tma_load_5d(base + (uint32_t)a.q_off + (uint32_t)(t * NP + pl) * kQPlane, &tmq,
+                        bar_qfull, 0, pl, 0, it.h, it.q0 + t * a.BM, pol_q);
+          }
           ++nq;
         }
         const int tok0 = kt * kPBN + lane * a.R;
@@ -641,7 +699,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const unsigned okmask = __ballot_sync(0xffffffffu, ok);
         if (lane == 0) {
-          meta[st] = make_int4(item, kt, it.n_kt, n);
+          meta[st] = make_int4(item, kt, it.nkt, n);
+          meta2[st] = make_int4(it.nkt_a, it.ntok_b > 0 ? 1 : 0, 0, 0);
           mbar_arrive_expect_tx(bar_full + 8 * st,
                                 (uint32_t)__popc(okmask) * box_bytes * (uint32_t)(2 * NP));
         }
@@ -666,87 +725,112 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (__any_sync(0xffffffffu, *abort_flag != 0)) {
       for (int k = max(0, j - S); k < j; ++k)
         mbar_wait_bounded(bar_full + 8 * (k % S), (uint32_t)(k / S) & 1u, nullptr);
-      for (int k = max(0, nq - kTcQB); k < nq; ++k)
-        mbar_wait_bounded(bar_q + 8 * (k % kTcQB), (uint32_t)(k / kTcQB) & 1u, nullptr);
+      if (nq > 0) mbar_wait_bounded(bar_qfull, (uint32_t)(nq - 1) & 1u, nullptr);
     }
   } else if (warp == kTcMma) {
     // ======================= MMA issue (one thread) =======================
-    // An event loop: the oldest pending O += P . V is issued as soon as its P
-    // is written (first: the softmax waits on it to reuse the P buffer), and
-    // the next stage's S = Q . K^T as soon as its K/V have landed (and its
-    // query tile, and a free S buffer), so that neither waits on the other's
-    // inputs.
+    // An event loop: each tile's oldest pending O += P . V is issued as soon
+    // as its P is written (first: the softmax waits on it to reuse the P
+    // buffer), and the next stage's S = Q . K^T products as soon as its K/V
+    // have landed (and the query tiles, and free S buffers of the tiles that
+    // read it).  A stage is released once every tile that reads it has had
+    // its P . V.
     if (lane == 0) {
       constexpr uint32_t id_s = umma_idesc_f16(kBF16, 128, kPBN, false);
       constexpr uint32_t id_o = umma_idesc_f16(kBF16, 128, D, true);
-      int4 info[4];           // (stage slot, kt, item number, -) of stages js-3 .. js-1
-      int js = 0, jp = 0;     // next stage to get its S, next to get its P . V
-      bool s_done = false;    // the stop marker was seen
+      int4 rec[2][4];          // per tile, pending P . V: (stage slot, first of an item, the
+                               // tile's item number, -)
+      int rh[2] = {0, 0}, rt[2] = {0, 0};   // pending records [rh, rt)
+      int ns[2] = {0, 0};      // S products issued per tile
+      int np[2] = {0, 0};      // P . V products issued per tile
+      int ni[2] = {0, 0};      // items started per tile
+      int need[kPMaxStages];   // P . V products a stage still waits for
+      int js = 0;              // next stage to get its S products
+      bool s_done = false;     // the stop marker was seen
       bool ok = true;
       long long t_last = clock64();
       while (true) {
         bool progressed = false;
-        if (jp < js) {
-          // O += P . V: P (128 x 64, K-major) from its buffer, V (64 keys x D,
-          // MN-major: 64-column planes kKPlane apart, 8-key groups 1024 bytes
-          // apart); an item's first stage overwrites O once the item before
-          // has been written out
-          const int4 pi = info[jp & 3];
-          const int pb = jp % kTcPB;
-          if (mbar_test(bar_p + 8 * pb, (uint32_t)(jp / kTcPB) & 1u) &&
-              (pi.y != 0 || pi.z == 0 || mbar_test(bar_ofree, (uint32_t)(pi.z - 1) & 1u))) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (rh[t] == rt[t]) continue;
+          // O += P . V: P (128 x 64, K-major) from the tile's buffer, V (64
+          // keys x D, MN-major: 64-column planes kKPlane apart, 8-key groups
+          // 1024 bytes apart); a tile's first stage of an item overwrites O
+          // once the tile's item before has been written out
+          const int4 pr = rec[t][rh[t] & 3];
+          const uint32_t bt = bar_tile0 + 64 * t;
+          if (mbar_test(bt + 32, (uint32_t)np[t] & 1u) &&
+              (pr.y == 0 || pr.z == 0 || mbar_test(bt + 48, (uint32_t)(pr.z - 1) & 1u))) {
             tc_fence_after();
-            const uint64_t dp =
-                umma_desc_sw128(base + (uint32_t)a.p_off + (uint32_t)pb * 16384u, 16, 1024);
+            const uint64_t dp = umma_desc_sw128(
+                base + (uint32_t)a.p_off + (uint32_t)t * 16384u, 16, 1024);
             const uint64_t dv = umma_desc_sw128(
-                base + (uint32_t)pi.x * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
+                base + (uint32_t)pr.x * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
 #pragma unroll
             for (int k = 0; k < kPBN / 16; ++k)
-              umma_f16(tmem + 128, dp + 2u * k, dv + 128u * k, id_o, pi.y > 0 || k > 0);
-            umma_commit(bar_p + 16 + 8 * pb);   // P buffer free, O updated
-            umma_commit(bar_empty + 8 * pi.x);  // the stage's K and V are no longer read
-            ++jp;
+              umma_f16(tmem + (uint32_t)(256 * t + 128), dp + 2u * k, dv + 128u * k, id_o,
+                       pr.y == 0 || k > 0);
+            umma_commit(bt + 40);                                   // P buffer free, O updated
+            if (--need[pr.x] == 0) umma_commit(bar_empty + 8 * pr.x);   // K, V no longer read
+            ++np[t];
+            ++rh[t];
             progressed = true;
           }
         }
-        if (!s_done && js - jp < 3) {
-          const int st = js % S, sb = js & 1;
+        if (!s_done && rt[0] - rh[0] < 4 && rt[1] - rh[1] < 4) {
+          const int st = js % S;
           if (mbar_test(bar_full + 8 * st, (uint32_t)(js / S) & 1u)) {
             const int4 md = meta[st];
             if (md.x < 0) {
               s_done = true;
+              progressed = true;
             } else {
-              const int kt = md.y, nkt = md.z, n = md.w, qb = n % kTcQB;
-              const bool q_ok = kt != 0 || mbar_test(bar_q + 8 * qb, (uint32_t)(n / kTcQB) & 1u);
-              // the S buffer's scores of two stages back have been read
-              const bool s_ok =
-                  js < 2 || mbar_test(bar_s + 16 + 8 * sb, (uint32_t)((js >> 1) - 1) & 1u);
-              if (q_ok && s_ok) {
+              const int4 m2 = meta2[st];
+              const int kt = md.y, nkt = md.z, n = md.w;
+              const bool act[2] = {kt < m2.x, m2.y != 0 && kt < nkt};
+              bool ready = kt != 0 || mbar_test(bar_qfull, (uint32_t)n & 1u);
+              // a tile's S buffer: its scores of two products back have been read
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+                if (ready && act[t] && ns[t] >= 2)
+                  ready = mbar_test(bar_tile0 + 64 * t + 16 + 8 * (ns[t] & 1),
+                                    (uint32_t)((ns[t] >> 1) - 1) & 1u);
+              if (ready) {
                 tc_fence_after();
-                // K steps of 16 columns; within a 64-column plane a step moves
-                // the start 32 bytes (the swizzle is applied to the address)
-                // (the descriptors' address field is in 16-byte units: a step
-                // adds its offset / 16 to the base descriptor)
-                const uint64_t da = umma_desc_sw128(
-                    base + (uint32_t)a.q_off + (uint32_t)qb * NP * kQPlane, 16, 1024);
+                need[st] = (act[0] ? 1 : 0) + (act[1] ? 1 : 0);
                 const uint64_t db = umma_desc_sw128(base + (uint32_t)st * a.stage_bytes, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                  const uint32_t off = (uint32_t)(ks & 3) * 32u;
-                  umma_f16(tmem + (uint32_t)sb * kPBN,
-                           da + (((uint32_t)(ks >> 2) * kQPlane + off) >> 4),
-                           db + (((uint32_t)(ks >> 2) * kKPlane + off) >> 4), id_s, ks > 0);
+                for (int t = 0; t < 2; ++t) {
+                  if (!act[t]) continue;
+                  // K steps of 16 columns; within a 64-column plane a step
+                  // moves the start 32 bytes (the swizzle is applied to the
+                  // address; the descriptors' address field is in 16-byte
+                  // units: a step adds its offset / 16 to the base descriptor)
+                  const uint64_t da = umma_desc_sw128(
+                      base + (uint32_t)a.q_off + (uint32_t)(t * NP) * kQPlane, 16, 1024);
+                  const int sb = ns[t] & 1;
+#pragma unroll
+                  for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (uint32_t)(ks & 3) * 32u;
+                    umma_f16(tmem + (uint32_t)(256 * t + sb * kPBN),
+                             da + (((uint32_t)(ks >> 2) * kQPlane + off) >> 4),
+                             db + (((uint32_t)(ks >> 2) * kKPlane + off) >> 4), id_s, ks > 0);
+                  }
+                  umma_commit(bar_tile0 + 64 * t + 8 * sb);
+                  rec[t][rt[t] & 3] = make_int4(st, kt == 0 ? 1 : 0, ni[t], 0);
+                  if (kt == 0) ++ni[t];
+                  ++rt[t];
+                  ++ns[t];
                 }
-                umma_commit(bar_s + 8 * sb);
-                if (kt == nkt - 1) umma_commit(bar_q + 16 + 8 * qb);   // the query tile is free
-                info[js & 3] = make_int4(st, kt, n, 0);
+                if (kt == nkt - 1) umma_commit(bar_qempty);   // the query tiles are free
                 ++js;
                 progressed = true;
               }
             }
           }
         }
-        if (s_done && jp == js) break;
+        if (s_done && rh[0] == rt[0] && rh[1] == rt[1]) break;
         if (progressed) {
           t_last = clock64();
         } else {
@@ -758,7 +842,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = false;
             break;
           }
-          __nanosleep(20);   // leave the issue slots to the softmax warp beside it
+          __nanosleep(20);   // leave the issue slots to the softmax warps beside it
         }
       }
       if (!ok) {
@@ -771,35 +855,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= softmax (warps 0-3) =======================
-    const int r = tid;   // this thread's query row, TMEM lane r
-    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    // ======================= softmax (warps 0-7) =======================
+    const int tile = warp >> 2;          // 0: tile A, 1: tile B
+    const int r = tid & 127;             // this thread's query row of the tile, TMEM lane r
+    const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(256 * tile);
+    const uint32_t bt = bar_tile0 + 64 * tile;
+    const uint32_t pbuf = base + (uint32_t)a.p_off + (uint32_t)tile * 16384u;
     const float sl2 = a.scale_log2;
-    Item it{};
+    Pair it{};
+    int q0 = 0, p0 = 0, nkt_t = 0;   // this tile's first q row, first position, stages
     int prow = -1;         // the row's position (-1: a padding row)
     bool valid = false;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    int j = 0;
+    int j = 0;             // stages of the ring seen
+    int nt = 0;            // stages this tile has processed
     while (true) {
-      const int st = j % S, sb = j & 1;
+      const int st = j % S;
       if (!wait_warp(bar_full + 8 * st, (uint32_t)(j / S) & 1u)) {
         ok = false;
         break;
       }
       const int4 md = meta[st];
       if (md.x < 0) break;
-      const int kt = md.y, nkt = md.z;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_seen + 8 * st);   // the tag is read
+      const int kt = md.y;
       if (kt == 0) {
-        decode_item(md.x, toff, a, it);
+        decode_pair(md.x, toff, a, it);
+        const int ntok = tile == 0 ? it.ntok_a : it.ntok_b;
+        q0 = it.q0 + tile * a.BM;
+        p0 = it.p0 + tile * a.BM;
+        nkt_t = tile == 0 ? it.nkt_a : (it.ntok_b > 0 ? it.nkt : 0);
         const int tok = r / a.G;
-        valid = r < a.BM * a.G && tok < it.ntok;
-        prow = valid ? it.p0 + tok : -1;
+        valid = r < a.BM * a.G && tok < ntok;
+        prow = valid ? p0 + tok : -1;
         m_used = -INFINITY;
         l = 0.f;
       }
+      ++j;
+      if (kt >= nkt_t) continue;   // keys past this tile's last position
+      const int sb = nt & 1;
       // ---- this row of S
-      if (!wait_warp(bar_s + 8 * sb, (uint32_t)(j >> 1) & 1u)) {
+      if (!wait_warp(bt + 8 * sb, (uint32_t)(nt >> 1) & 1u)) {
         ok = false;
         break;
       }
@@ -809,9 +907,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_ld32(trow + (uint32_t)sb * kPBN + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar_s + 16 + 8 * sb);   // the S buffer may be overwritten
+      mbar_arrive(bt + 16 + 8 * sb);   // the S buffer may be overwritten
       // ---- causal mask (a padding row keeps finite scores against cached
-      // keys) and maximum.  A stage wholly at or before the item's first
+      // keys) and maximum.  A stage wholly at or before the tile's first
       // position needs no mask, and with a positive scale its maximum is
       // taken on the raw scores; otherwise the scores are scaled first.
       // (eight partial maxima and sums: one warp per sub-partition leaves no
@@ -820,7 +918,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float mx8[8], f = 1.f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
-      const bool raw = tb + kPBN - 1 <= it.p0 && sl2 > 0.f;
+      const bool raw = tb + kPBN - 1 <= p0 && sl2 > 0.f;
       if (raw) {
 #pragma unroll
         for (int c = 0; c < kPBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
@@ -854,25 +952,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < 8; ++c) sum8[c] = 0.f;
 #pragma unroll
       for (int c = 0; c < kPBN / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), f, -mu));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), f, -mu));
-        pk[c] = pack2<kBF16>(p0, p1);
+        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), f, -mu));
+        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), f, -mu));
+        pk[c] = pack2<kBF16>(e0, e1);
         const float2 pr = unpack2<kBF16>(pk[c]);
         sum8[c & 7] += pr.x + pr.y;
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) sum8[c] += sum8[c + 4];
       l = l * alpha + ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3]));
-      // the P buffer's previous use (two stages back) is done
-      const int pb = j % kTcPB;
-      if (j >= kTcPB && !wait_warp(bar_p + 16 + 8 * pb, (uint32_t)(j / kTcPB - 1) & 1u)) {
+      // the P buffer's previous use is done (its O += P . V has completed)
+      if (nt >= 1 && !wait_warp(bt + 40, (uint32_t)(nt - 1) & 1u)) {
         ok = false;
         break;
       }
       {
         // row r of P, K-major with the 128-byte swizzle: 16-byte chunk c at
         // chunk c ^ (r & 7)
-        const uint32_t prow_addr = base + (uint32_t)a.p_off + (uint32_t)pb * 16384u + (uint32_t)r * 128u;
+        const uint32_t prow_addr = pbuf + (uint32_t)r * 128u;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
@@ -881,12 +978,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                        : "memory");
       }
       // ---- rescale this warp's rows of O once the previous stage's
-      // O += P . V is done (alpha = 1 leaves a row unchanged)
+      // O += P . V is done (waited for above; alpha = 1 leaves a row
+      // unchanged)
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!wait_warp(bar_p + 16 + 8 * ((j - 1) % kTcPB), (uint32_t)((j - 1) / kTcPB) & 1u)) {
-          ok = false;
-          break;
-        }
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
@@ -900,12 +994,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_wait_st();
       }
       // ---- keys past the sequence's end hold no data (NaN, possibly): their
-      // V rows are cleared so that P = 0 multiplies zeros
+      // V rows are cleared so that P = 0 multiplies zeros (both warpgroups
+      // may clear the same rows: they write the same zeros)
       if (tb + kPBN > it.T) {
         const int z0 = max(0, it.T - tb);
         const int per_plane = (kPBN - z0) * 8;   // 16-byte pieces
         const uint32_t vpart = base + (uint32_t)st * a.stage_bytes + (uint32_t)a.kv_bytes;
-        for (int e = tid; e < per_plane * NP; e += 128) {
+        for (int e = r; e < per_plane * NP; e += 128) {
           const int p = e / per_plane, rem = e - p * per_plane;
           const uint32_t addr =
               vpart + (uint32_t)p * kKPlane + (uint32_t)(z0 + (rem >> 3)) * 128u + (uint32_t)(rem & 7) * 16u;
@@ -914,17 +1009,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       fence_proxy_async_smem();   // P and the cleared rows, before the tensor core reads them
       tc_fence_before();
-      mbar_arrive(bar_p + 8 * pb);
-      if (kt == nkt - 1) {
-        // ---- the item's last stage: out = O / l once O += P . V is done
-        if (!wait_warp(bar_p + 16 + 8 * pb, (uint32_t)(j / kTcPB) & 1u)) {
+      mbar_arrive(bt + 32);
+      if (kt == nkt_t - 1) {
+        // ---- the tile's last stage: out = O / l once O += P . V is done
+        if (!wait_warp(bt + 40, (uint32_t)nt & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const float inv = 1.f / l;
         uint16_t* orow =
-            a.out + ((size_t)(it.q0 + (valid ? r / a.G : 0)) * a.Hq + (size_t)it.h * a.G + r % a.G) * D;
+            a.out + ((size_t)(q0 + (valid ? r / a.G : 0)) * a.Hq + (size_t)it.h * a.G + r % a.G) * D;
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
           uint32_t o[32];
@@ -942,9 +1037,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(bar_ofree);   // O may be overwritten by the next item
+        mbar_arrive(bt + 48);   // O may be overwritten by the tile's next item
       }
-      ++j;
+      ++nt;
     }
     if (!ok) {
       if (lane == 0 && !*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
@@ -1017,18 +1112,19 @@ int make_tc_plan(int Hq, int Hkv, int D, int B, int dtype, int num_seqs, Prefill
   p.BM = kPRows / p.G;
   p.kv_bytes = kPBN * D * 2;
   p.stage_bytes = 2 * p.kv_bytes;
-  const int qbuf = (D / 64) * 16384;
+  const int qbuf = (D / 64) * 16384;   // one query tile
   DeviceInfo di;
   if (int rc = current_device_info(&di)) return rc;
-  int st = (di.smem_per_block - 1024 - kTcQB * qbuf - kTcPB * 16384 -
+  // two query tiles and two P buffers (the item's tiles A and B)
+  int st = (di.smem_per_block - 1024 - 2 * qbuf - 2 * 16384 -
             tc_ctrl_bytes(kPMaxStages, num_seqs)) /
            p.stage_bytes;
   if (st > kPMaxStages) st = kPMaxStages;
   if (st < 2) return PA_ERR_UNSUPPORTED;
   p.stages = st;
   p.q_off = st * p.stage_bytes;
-  p.p_off = p.q_off + kTcQB * qbuf;
-  p.ctrl_off = p.p_off + kTcPB * 16384;
+  p.p_off = p.q_off + 2 * qbuf;
+  p.ctrl_off = p.p_off + 2 * 16384;
   p.smem_bytes = 1024 + p.ctrl_off + tc_ctrl_bytes(st, num_seqs);
   p.q_tx = (D / 64) * 128 * p.G * p.BM;
   int per_sm = 0;
