@@ -738,13 +738,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = umma_idesc_f16(kBF16, 128, kPBN, false);
       constexpr uint32_t id_o = umma_idesc_f16(kBF16, 128, D, true);
-      int4 rec[2][4];          // per tile, pending P . V: (stage slot, first of an item, the
-                               // tile's item number, -)
+      // All bookkeeping in registers (a dynamically indexed array would live
+      // in local memory, a round trip on this thread's every step):
+      // per tile, a ring of four pending P . V records of 6 bits: stage slot
+      // (bits 0-2), first stage of an item (3), O must be free first (4), the
+      // parity of that wait (5); per stage slot, the P . V products it still
+      // waits for (2 bits).
+      static_assert(kPMaxStages <= 8, "stage slots take 3 bits");
+      uint32_t ring[2] = {0u, 0u};
+      uint32_t need = 0u;
       int rh[2] = {0, 0}, rt[2] = {0, 0};   // pending records [rh, rt)
       int ns[2] = {0, 0};      // S products issued per tile
       int np[2] = {0, 0};      // P . V products issued per tile
       int ni[2] = {0, 0};      // items started per tile
-      int need[kPMaxStages];   // P . V products a stage still waits for
       int js = 0;              // next stage to get its S products
       bool s_done = false;     // the stop marker was seen
       bool ok = true;
@@ -758,21 +764,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // keys x D, MN-major: 64-column planes kKPlane apart, 8-key groups
           // 1024 bytes apart); a tile's first stage of an item overwrites O
           // once the tile's item before has been written out
-          const int4 pr = rec[t][rh[t] & 3];
+          const uint32_t rc = (ring[t] >> (6 * (rh[t] & 3))) & 63u;
+          const int pst = (int)(rc & 7u);
+          const bool first = (rc & 8u) != 0u;
           const uint32_t bt = bar_tile0 + 64 * t;
           if (mbar_test(bt + 32, (uint32_t)np[t] & 1u) &&
-              (pr.y == 0 || pr.z == 0 || mbar_test(bt + 48, (uint32_t)(pr.z - 1) & 1u))) {
+              (!(rc & 16u) || mbar_test(bt + 48, (rc >> 5) & 1u))) {
             tc_fence_after();
             const uint64_t dp = umma_desc_sw128(
                 base + (uint32_t)a.p_off + (uint32_t)t * 16384u, 16, 1024);
             const uint64_t dv = umma_desc_sw128(
-                base + (uint32_t)pr.x * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
+                base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
 #pragma unroll
             for (int k = 0; k < kPBN / 16; ++k)
               umma_f16(tmem + (uint32_t)(256 * t + 128), dp + 2u * k, dv + 128u * k, id_o,
-                       pr.y == 0 || k > 0);
+                       !first || k > 0);
             umma_commit(bt + 40);                                   // P buffer free, O updated
-            if (--need[pr.x] == 0) umma_commit(bar_empty + 8 * pr.x);   // K, V no longer read
+            need -= 1u << (2 * pst);
+            if (((need >> (2 * pst)) & 3u) == 0u)
+              umma_commit(bar_empty + 8 * pst);                     // K, V no longer read
             ++np[t];
             ++rh[t];
             progressed = true;
@@ -798,7 +808,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     (uint32_t)((ns[t] >> 1) - 1) & 1u);
               if (ready) {
                 tc_fence_after();
-                need[st] = (act[0] ? 1 : 0) + (act[1] ? 1 : 0);
+                need = (need & ~(3u << (2 * st))) |
+                       ((uint32_t)((act[0] ? 1 : 0) + (act[1] ? 1 : 0)) << (2 * st));
                 const uint64_t db = umma_desc_sw128(base + (uint32_t)st * a.stage_bytes, 16, 1024);
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
@@ -818,8 +829,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                              db + (((uint32_t)(ks >> 2) * kKPlane + off) >> 4), id_s, ks > 0);
                   }
                   umma_commit(bar_tile0 + 64 * t + 8 * sb);
-                  rec[t][rt[t] & 3] = make_int4(st, kt == 0 ? 1 : 0, ni[t], 0);
-                  if (kt == 0) ++ni[t];
+                  uint32_t rc = (uint32_t)st;
+                  if (kt == 0) {
+                    rc |= 8u;
+                    if (ni[t] > 0) rc |= 16u | ((uint32_t)((ni[t] - 1) & 1) << 5);
+                    ++ni[t];
+                  }
+                  const int sh = 6 * (rt[t] & 3);
+                  ring[t] = (ring[t] & ~(63u << sh)) | (rc << sh);
                   ++rt[t];
                   ++ns[t];
                 }
