@@ -522,14 +522,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // 256 t + 128.  Every wait is bounded; a wait that gives up sets
 // PA_DEVERR_TIMEOUT and the roles leave.
 // ---------------------------------------------------------------------------
-constexpr int kTcWarps = 10;
+constexpr int kTcWarps = 11;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcProducer = 8;
-constexpr int kTcMma = 9;
+constexpr int kTcMma = 9;           // warps 9 and 10: the MMA issuers of tiles A and B
 constexpr uint32_t kTcTmemCols = 512;
 constexpr float kTcTau = 8.f;
 // barriers (8 bytes each): q full, q empty; per tile s full[2], s free[2],
-// p full, p empty, o free (and one spare) = 8; done; one spare
+// p full, p empty, o free (and one spare) = 8; done[2]
 constexpr int kTcBars = 2 + 2 * 8 + 2;
 
 __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
@@ -585,11 +585,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);       // one commit of the MMA thread
+      mbar_init(bar_empty + 8 * s, 2);       // a commit of each MMA issuer
       mbar_init(bar_seen + 8 * s, 8);        // one arrival per softmax warp
     }
     mbar_init(bar_qfull, 1);                 // the producer's expect-tx
-    mbar_init(bar_qempty, 1);                // a commit
+    mbar_init(bar_qempty, 2);                // a commit of each MMA issuer
     for (int t = 0; t < 2; ++t) {
       const uint32_t bt = bar_tile0 + 64 * t;
       for (int b = 0; b < 2; ++b) {
@@ -601,6 +601,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bt + 48, 128);               // o free: the warpgroup's threads
     }
     mbar_init(bar_done, 1);
+    mbar_init(bar_done + 8, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -727,68 +728,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_wait_bounded(bar_full + 8 * (k % S), (uint32_t)(k / S) & 1u, nullptr);
       if (nq > 0) mbar_wait_bounded(bar_qfull, (uint32_t)(nq - 1) & 1u, nullptr);
     }
-  } else if (warp == kTcMma) {
-    // ======================= MMA issue (one thread) =======================
-    // An event loop: each tile's oldest pending O += P . V is issued as soon
-    // as its P is written (first: the softmax waits on it to reuse the P
-    // buffer), and the next stage's S = Q . K^T products as soon as its K/V
-    // have landed (and the query tiles, and free S buffers of the tiles that
-    // read it).  A stage is released once every tile that reads it has had
-    // its P . V.
+  } else if (warp >= kTcMma) {
+    // ======================= MMA issue (one thread per tile) =================
+    // Warp 9 issues tile A's products, warp 10 tile B's: one thread issuing
+    // both tiles' was the bottleneck (an issue takes tens of cycles).  Each
+    // walks every stage.  An event loop: the tile's oldest pending O += P . V
+    // is issued as soon as its P is written (first: the softmax waits on it to
+    // reuse the P buffer), and the next stage's S = Q . K^T as soon as its K/V
+    // have landed (and the query tile, and a free S buffer), once at most one
+    // stage's O += P . V is pending, so that a P . V is never queued behind
+    // score products two stages ahead (the tensor pipe executes in issue
+    // order).  A stage and the query tiles are released by a commit of each
+    // issuer (barriers of count 2), made after its last product that reads
+    // them (at once where its tile does not read the stage).
+    const int t = warp - kTcMma;
     if (lane == 0) {
       constexpr uint32_t id_s = umma_idesc_f16(kBF16, 128, kPBN, false);
       constexpr uint32_t id_o = umma_idesc_f16(kBF16, 128, D, true);
-      // All bookkeeping in registers (a dynamically indexed array would live
-      // in local memory, a round trip on this thread's every step):
-      // per tile, a ring of four pending P . V records of 6 bits: stage slot
-      // (bits 0-2), first stage of an item (3), O must be free first (4), the
-      // parity of that wait (5); per stage slot, the P . V products it still
-      // waits for (2 bits).
+      // Bookkeeping in registers (a dynamically indexed array would live in
+      // local memory, a round trip on this thread's every step): a ring of
+      // four pending P . V records of 6 bits: stage slot (bits 0-2), first
+      // stage of an item (3), O must be free first (4), the parity of that
+      // wait (5).
       static_assert(kPMaxStages <= 8, "stage slots take 3 bits");
-      uint32_t ring[2] = {0u, 0u};
-      uint32_t need = 0u;
-      int rh[2] = {0, 0}, rt[2] = {0, 0};   // pending records [rh, rt)
-      int ns[2] = {0, 0};      // S products issued per tile
-      int np[2] = {0, 0};      // P . V products issued per tile
-      int ni[2] = {0, 0};      // items started per tile
-      int js = 0;              // next stage to get its S products
+      uint32_t ring = 0u;
+      int rh = 0, rt = 0;      // pending records [rh, rt)
+      int ns = 0, np = 0;      // S and P . V products issued
+      int ni = 0;              // items started
+      int js = 0;              // next stage to walk
       bool s_done = false;     // the stop marker was seen
       bool ok = true;
+      const uint32_t bt = bar_tile0 + 64 * t;
+      const uint32_t tcol = tmem + (uint32_t)(256 * t);
+      const uint64_t da = umma_desc_sw128(base + (uint32_t)a.q_off + (uint32_t)(t * NP) * kQPlane,
+                                          16, 1024);
+      const uint64_t dp = umma_desc_sw128(base + (uint32_t)a.p_off + (uint32_t)t * 16384u, 16, 1024);
       long long t_last = clock64();
       while (true) {
         bool progressed = false;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (rh[t] == rt[t]) continue;
+        if (rh != rt) {
           // O += P . V: P (128 x 64, K-major) from the tile's buffer, V (64
           // keys x D, MN-major: 64-column planes kKPlane apart, 8-key groups
-          // 1024 bytes apart); a tile's first stage of an item overwrites O
+          // 1024 bytes apart); the tile's first stage of an item overwrites O
           // once the tile's item before has been written out
-          const uint32_t rc = (ring[t] >> (6 * (rh[t] & 3))) & 63u;
+          const uint32_t rc = (ring >> (6 * (rh & 3))) & 63u;
           const int pst = (int)(rc & 7u);
           const bool first = (rc & 8u) != 0u;
-          const uint32_t bt = bar_tile0 + 64 * t;
-          if (mbar_test(bt + 32, (uint32_t)np[t] & 1u) &&
+          if (mbar_test(bt + 32, (uint32_t)np & 1u) &&
               (!(rc & 16u) || mbar_test(bt + 48, (rc >> 5) & 1u))) {
             tc_fence_after();
-            const uint64_t dp = umma_desc_sw128(
-                base + (uint32_t)a.p_off + (uint32_t)t * 16384u, 16, 1024);
             const uint64_t dv = umma_desc_sw128(
                 base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
 #pragma unroll
             for (int k = 0; k < kPBN / 16; ++k)
-              umma_f16(tmem + (uint32_t)(256 * t + 128), dp + 2u * k, dv + 128u * k, id_o,
-                       !first || k > 0);
-            umma_commit(bt + 40);                                   // P buffer free, O updated
-            need -= 1u << (2 * pst);
-            if (((need >> (2 * pst)) & 3u) == 0u)
-              umma_commit(bar_empty + 8 * pst);                     // K, V no longer read
-            ++np[t];
-            ++rh[t];
+              umma_f16(tcol + 128u, dp + 2u * k, dv + 128u * k, id_o, !first || k > 0);
+            umma_commit(bt + 40);                    // P buffer free, O updated
+            umma_commit(bar_empty + 8 * pst);        // this tile no longer reads K, V
+            ++np;
+            ++rh;
             progressed = true;
           }
         }
-        if (!s_done && rt[0] - rh[0] < 4 && rt[1] - rh[1] < 4) {
+        if (!s_done && rt - rh < 2) {
           const int st = js % S;
           if (mbar_test(bar_full + 8 * st, (uint32_t)(js / S) & 1u)) {
             const int4 md = meta[st];
@@ -798,56 +799,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
               const int4 m2 = meta2[st];
               const int kt = md.y, nkt = md.z, n = md.w;
-              const bool act[2] = {kt < m2.x, m2.y != 0 && kt < nkt};
-              bool ready = kt != 0 || mbar_test(bar_qfull, (uint32_t)n & 1u);
-              // a tile's S buffer: its scores of two products back have been read
-#pragma unroll
-              for (int t = 0; t < 2; ++t)
-                if (ready && act[t] && ns[t] >= 2)
-                  ready = mbar_test(bar_tile0 + 64 * t + 16 + 8 * (ns[t] & 1),
-                                    (uint32_t)((ns[t] >> 1) - 1) & 1u);
-              if (ready) {
-                tc_fence_after();
-                need = (need & ~(3u << (2 * st))) |
-                       ((uint32_t)((act[0] ? 1 : 0) + (act[1] ? 1 : 0)) << (2 * st));
-                const uint64_t db = umma_desc_sw128(base + (uint32_t)st * a.stage_bytes, 16, 1024);
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                  if (!act[t]) continue;
+              const bool act = t == 0 ? kt < m2.x : (m2.y != 0 && kt < nkt);
+              if (!act) {
+                // keys past this tile's last position: nothing to compute
+                umma_commit(bar_empty + 8 * st);
+                if (kt == nkt - 1) umma_commit(bar_qempty);
+                ++js;
+                progressed = true;
+              } else {
+                // the query tile has landed, and the S buffer's scores of two
+                // products back have been read
+                bool ready = kt != 0 || mbar_test(bar_qfull, (uint32_t)n & 1u);
+                if (ready && ns >= 2)
+                  ready = mbar_test(bt + 16 + 8 * (ns & 1), (uint32_t)((ns >> 1) - 1) & 1u);
+                if (ready) {
+                  tc_fence_after();
+                  const uint64_t db =
+                      umma_desc_sw128(base + (uint32_t)st * a.stage_bytes, 16, 1024);
+                  const int sb = ns & 1;
                   // K steps of 16 columns; within a 64-column plane a step
                   // moves the start 32 bytes (the swizzle is applied to the
                   // address; the descriptors' address field is in 16-byte
                   // units: a step adds its offset / 16 to the base descriptor)
-                  const uint64_t da = umma_desc_sw128(
-                      base + (uint32_t)a.q_off + (uint32_t)(t * NP) * kQPlane, 16, 1024);
-                  const int sb = ns[t] & 1;
 #pragma unroll
                   for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (uint32_t)(ks & 3) * 32u;
-                    umma_f16(tmem + (uint32_t)(256 * t + sb * kPBN),
+                    umma_f16(tcol + (uint32_t)(sb * kPBN),
                              da + (((uint32_t)(ks >> 2) * kQPlane + off) >> 4),
                              db + (((uint32_t)(ks >> 2) * kKPlane + off) >> 4), id_s, ks > 0);
                   }
-                  umma_commit(bar_tile0 + 64 * t + 8 * sb);
+                  umma_commit(bt + 8 * sb);
+                  if (kt == nkt - 1) umma_commit(bar_qempty);   // the query tile is free
                   uint32_t rc = (uint32_t)st;
                   if (kt == 0) {
                     rc |= 8u;
-                    if (ni[t] > 0) rc |= 16u | ((uint32_t)((ni[t] - 1) & 1) << 5);
-                    ++ni[t];
+                    if (ni > 0) rc |= 16u | ((uint32_t)((ni - 1) & 1) << 5);
+                    ++ni;
                   }
-                  const int sh = 6 * (rt[t] & 3);
-                  ring[t] = (ring[t] & ~(63u << sh)) | (rc << sh);
-                  ++rt[t];
-                  ++ns[t];
+                  const int sh = 6 * (rt & 3);
+                  ring = (ring & ~(63u << sh)) | (rc << sh);
+                  ++rt;
+                  ++ns;
+                  ++js;
+                  progressed = true;
                 }
-                if (kt == nkt - 1) umma_commit(bar_qempty);   // the query tiles are free
-                ++js;
-                progressed = true;
               }
             }
           }
         }
-        if (s_done && rh[0] == rt[0] && rh[1] == rt[1]) break;
+        if (s_done && rh == rt) break;
         if (progressed) {
           t_last = clock64();
         } else {
@@ -867,8 +867,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *abort_flag = 1;
       }
       // every MMA issued has completed before the tensor memory is released
-      umma_commit(bar_done);
-      mbar_wait_bounded(bar_done, 0u, nullptr);
+      umma_commit(bar_done + 8 * t);
+      mbar_wait_bounded(bar_done + 8 * t, 0u, nullptr);
     }
     __syncwarp();
   } else {
