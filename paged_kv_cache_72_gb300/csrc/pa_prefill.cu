@@ -503,7 +503,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
 //  * warps 0-3 (softmax of tile A) and 4-7 (tile B): thread r of a warpgroup
 //    owns query row r of its tile, which is TMEM lane r.  Per 64-key stage it
 //    reads its row of S, masks it, updates the running maximum and sum, and
-//    writes its row of P (16-bit) to its tile's P buffer.  The maximum used
+//    writes its row of P (16-bit) into one of its tile's two P regions of
+//    tensor memory.  The maximum used
 //    for the exponentials moves only when a row's maximum passes it by more
 //    than kTcTau (log2 units): then the row of O is rescaled in TMEM;
 //    otherwise P stays below 2^kTcTau and O, l and the stale maximum stay
@@ -514,22 +515,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
 //    tiles by TMA (one copy per 64-column plane, [row][128 bytes], 128-byte
 //    swizzle), per stage the K and V planes of the item's KV head, tagged with
 //    the item.
-//  * warp 9 (MMA, one thread): per stage S = Q . K^T (M 128, N 64, K =
-//    head_dim) for each tile that reads it, into one of the tile's two S
-//    buffers, and O += P . V (M 128, N head_dim, K 64, V as an MN-major
-//    operand) for each tile once its P is written.
-// Tensor memory: tile t's S buffers at columns 256 t and 256 t + 64, its O at
+//  * warps 9 and 10 (MMA, one thread each, one per tile): per stage S = Q .
+//    K^T (M 128, N 64, K = head_dim) into the tile's S buffer, and O += P . V
+//    (M 128, N head_dim, K 64; P from tensor memory, V from shared memory as
+//    an MN-major operand) once its P is written.
+// Tensor memory: tile t's S buffer at columns 256 t .. +63, its P regions
+// (64 keys of 16 bits, two to a column) at 256 t + 64 and 256 t + 96, its O at
 // 256 t + 128.  Every wait is bounded; a wait that gives up sets
 // PA_DEVERR_TIMEOUT and the roles leave.
 // ---------------------------------------------------------------------------
+// D[tmem] (+)= A . B with A in tensor memory: M rows in lanes 0..M-1, K along
+// the columns, two 16-bit elements per 32-bit column (the even one in the low
+// half); B from shared memory by its descriptor
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u));
+}
+
 constexpr int kTcWarps = 11;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcProducer = 8;
 constexpr int kTcMma = 9;           // warps 9 and 10: the MMA issuers of tiles A and B
 constexpr uint32_t kTcTmemCols = 512;
 constexpr float kTcTau = 8.f;
-// barriers (8 bytes each): q full, q empty; per tile s full[2], s free[2],
-// p full, p empty, o free (and one spare) = 8; done[2]
+// barriers (8 bytes each): q full, q empty; per tile 8 slots (s full, s free,
+// p full, p empty[2], o free, two unused); done[2]
 constexpr int kTcBars = 2 + 2 * 8 + 2;
 
 __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
@@ -568,8 +581,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t bar_seen = bar_empty + 8 * S;
   const uint32_t bar_qfull = bar_seen + 8 * S;
   const uint32_t bar_qempty = bar_qfull + 8;
-  // tile t's barriers: s full[2] at +0, s free[2] at +16, p full at +32,
-  // p empty at +40, o free at +48
+  // tile t's barriers: s full at +0, s free at +16, p full at +32, p empty of
+  // P region 0 at +40 and of region 1 at +56, o free at +48
   const uint32_t bar_tile0 = bar_qfull + 16;
   const uint32_t bar_done = bar_tile0 + 128;
   uint8_t* const cgen = gbase + a.ctrl_off + tc_tags_off(S);
@@ -592,12 +605,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(bar_qempty, 2);                // a commit of each MMA issuer
     for (int t = 0; t < 2; ++t) {
       const uint32_t bt = bar_tile0 + 64 * t;
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(bt + 8 * b, 1);            // s full: a commit
-        mbar_init(bt + 16 + 8 * b, 128);     // s free: the warpgroup's threads
-      }
+      mbar_init(bt, 1);                      // s full: a commit
+      mbar_init(bt + 16, 128);               // s free: the warpgroup's threads
       mbar_init(bt + 32, 128);               // p full: the warpgroup's threads
-      mbar_init(bt + 40, 1);                 // p empty: a commit
+      mbar_init(bt + 40, 1);                 // p empty, region 0: a commit
+      mbar_init(bt + 56, 1);                 // p empty, region 1: a commit
       mbar_init(bt + 48, 128);               // o free: the warpgroup's threads
     }
     mbar_init(bar_done, 1);
@@ -762,15 +774,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tcol = tmem + (uint32_t)(256 * t);
       const uint64_t da = umma_desc_sw128(base + (uint32_t)a.q_off + (uint32_t)(t * NP) * kQPlane,
                                           16, 1024);
-      const uint64_t dp = umma_desc_sw128(base + (uint32_t)a.p_off + (uint32_t)t * 16384u, 16, 1024);
       long long t_last = clock64();
       while (true) {
         bool progressed = false;
         if (rh != rt) {
-          // O += P . V: P (128 x 64, K-major) from the tile's buffer, V (64
-          // keys x D, MN-major: 64-column planes kKPlane apart, 8-key groups
-          // 1024 bytes apart); the tile's first stage of an item overwrites O
-          // once the tile's item before has been written out
+          // O += P . V: P (128 x 64) from the tile's P region np % 2 in
+          // tensor memory (16 keys = 8 columns per K step), V (64 keys x D,
+          // MN-major: 64-column planes kKPlane apart, 8-key groups 1024 bytes
+          // apart); the tile's first stage of an item overwrites O once the
+          // tile's item before has been written out
           const uint32_t rc = (ring >> (6 * (rh & 3))) & 63u;
           const int pst = (int)(rc & 7u);
           const bool first = (rc & 8u) != 0u;
@@ -779,10 +791,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const uint64_t dv = umma_desc_sw128(
                 base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
+            const uint32_t preg = tcol + 64u + 32u * (uint32_t)(np & 1);
 #pragma unroll
             for (int k = 0; k < kPBN / 16; ++k)
-              umma_f16(tcol + 128u, dp + 2u * k, dv + 128u * k, id_o, !first || k > 0);
-            umma_commit(bt + 40);                    // P buffer free, O updated
+              umma_f16_tmem_a(tcol + 128u, preg + 8u * k, dv + 128u * k, id_o, !first || k > 0);
+            umma_commit(bt + ((np & 1) ? 56 : 40));  // the P region is free, O updated
             umma_commit(bar_empty + 8 * pst);        // this tile no longer reads K, V
             ++np;
             ++rh;
@@ -807,16 +820,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ++js;
                 progressed = true;
               } else {
-                // the query tile has landed, and the S buffer's scores of two
-                // products back have been read
+                // the query tile has landed, and the S buffer's previous
+                // scores have been read
                 bool ready = kt != 0 || mbar_test(bar_qfull, (uint32_t)n & 1u);
-                if (ready && ns >= 2)
-                  ready = mbar_test(bt + 16 + 8 * (ns & 1), (uint32_t)((ns >> 1) - 1) & 1u);
+                if (ready && ns >= 1) ready = mbar_test(bt + 16, (uint32_t)(ns - 1) & 1u);
                 if (ready) {
                   tc_fence_after();
                   const uint64_t db =
                       umma_desc_sw128(base + (uint32_t)st * a.stage_bytes, 16, 1024);
-                  const int sb = ns & 1;
                   // K steps of 16 columns; within a 64-column plane a step
                   // moves the start 32 bytes (the swizzle is applied to the
                   // address; the descriptors' address field is in 16-byte
@@ -824,11 +835,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                   for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (uint32_t)(ks & 3) * 32u;
-                    umma_f16(tcol + (uint32_t)(sb * kPBN),
-                             da + (((uint32_t)(ks >> 2) * kQPlane + off) >> 4),
+                    umma_f16(tcol, da + (((uint32_t)(ks >> 2) * kQPlane + off) >> 4),
                              db + (((uint32_t)(ks >> 2) * kKPlane + off) >> 4), id_s, ks > 0);
                   }
-                  umma_commit(bt + 8 * sb);
+                  umma_commit(bt);
                   if (kt == nkt - 1) umma_commit(bar_qempty);   // the query tile is free
                   uint32_t rc = (uint32_t)st;
                   if (kt == 0) {
@@ -877,7 +887,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int r = tid & 127;             // this thread's query row of the tile, TMEM lane r
     const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(256 * tile);
     const uint32_t bt = bar_tile0 + 64 * tile;
-    const uint32_t pbuf = base + (uint32_t)a.p_off + (uint32_t)tile * 16384u;
     const float sl2 = a.scale_log2;
     Pair it{};
     int q0 = 0, p0 = 0, nkt_t = 0;   // this tile's first q row, first position, stages
@@ -912,19 +921,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       ++j;
       if (kt >= nkt_t) continue;   // keys past this tile's last position
-      const int sb = nt & 1;
       // ---- this row of S
-      if (!wait_warp(bt + 8 * sb, (uint32_t)(nt >> 1) & 1u)) {
+      if (!wait_warp(bt, (uint32_t)nt & 1u)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[kPBN];
-      tmem_ld32(trow + (uint32_t)sb * kPBN, *reinterpret_cast<uint32_t(*)[32]>(sr));
-      tmem_ld32(trow + (uint32_t)sb * kPBN + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      tmem_ld32(trow, *reinterpret_cast<uint32_t(*)[32]>(sr));
+      tmem_ld32(trow + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bt + 16 + 8 * sb);   // the S buffer may be overwritten
+      mbar_arrive(bt + 16);   // the S buffer may be overwritten
       // ---- causal mask (a padding row keeps finite scores against cached
       // keys) and maximum.  A stage wholly at or before the tile's first
       // position needs no mask, and with a positive scale its maximum is
@@ -978,26 +986,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) sum8[c] += sum8[c + 4];
       l = l * alpha + ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3]));
-      // the P buffer's previous use is done (its O += P . V has completed)
-      if (nt >= 1 && !wait_warp(bt + 40, (uint32_t)(nt - 1) & 1u)) {
+      // the P region's previous use (two stages back) is done: its O += P . V
+      // has completed
+      const uint32_t pe = bt + ((nt & 1) ? 56 : 40);
+      if (nt >= 2 && !wait_warp(pe, (uint32_t)((nt >> 1) - 1) & 1u)) {
         ok = false;
         break;
       }
-      {
-        // row r of P, K-major with the 128-byte swizzle: 16-byte chunk c at
-        // chunk c ^ (r & 7)
-        const uint32_t prow_addr = pbuf + (uint32_t)r * 128u;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           prow_addr + (uint32_t)((c ^ (r & 7)) << 4)),
-                       "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                       : "memory");
-      }
+      tc_fence_after();
+      // row r of P into the tile's P region nt % 2 (lane r, two keys a column)
+      tmem_st32(trow + 64u + 32u * (uint32_t)(nt & 1), *reinterpret_cast<uint32_t(*)[32]>(pk));
       // ---- rescale this warp's rows of O once the previous stage's
-      // O += P . V is done (waited for above; alpha = 1 leaves a row
-      // unchanged)
+      // O += P . V is done (alpha = 1 leaves a row unchanged)
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        if (nt >= 1 && !wait_warp(bt + ((nt & 1) ? 40 : 56), (uint32_t)((nt - 1) >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
@@ -1024,12 +1029,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
         }
       }
-      fence_proxy_async_smem();   // P and the cleared rows, before the tensor core reads them
+      tmem_wait_st();
+      fence_proxy_async_smem();   // the cleared rows, before the tensor core reads them
       tc_fence_before();
       mbar_arrive(bt + 32);
       if (kt == nkt_t - 1) {
         // ---- the tile's last stage: out = O / l once O += P . V is done
-        if (!wait_warp(bt + 40, (uint32_t)nt & 1u)) {
+        if (!wait_warp(pe, (uint32_t)(nt >> 1) & 1u)) {
           ok = false;
           break;
         }
@@ -1132,16 +1138,15 @@ int make_tc_plan(int Hq, int Hkv, int D, int B, int dtype, int num_seqs, Prefill
   const int qbuf = (D / 64) * 16384;   // one query tile
   DeviceInfo di;
   if (int rc = current_device_info(&di)) return rc;
-  // two query tiles and two P buffers (the item's tiles A and B)
-  int st = (di.smem_per_block - 1024 - 2 * qbuf - 2 * 16384 -
-            tc_ctrl_bytes(kPMaxStages, num_seqs)) /
+  // two query tiles (the item's tiles A and B); P lives in tensor memory
+  int st = (di.smem_per_block - 1024 - 2 * qbuf - tc_ctrl_bytes(kPMaxStages, num_seqs)) /
            p.stage_bytes;
   if (st > kPMaxStages) st = kPMaxStages;
   if (st < 2) return PA_ERR_UNSUPPORTED;
   p.stages = st;
   p.q_off = st * p.stage_bytes;
-  p.p_off = p.q_off + 2 * qbuf;
-  p.ctrl_off = p.p_off + 2 * 16384;
+  p.p_off = p.q_off + 2 * qbuf;   // (unused by the tensor-core kernel)
+  p.ctrl_off = p.p_off;
   p.smem_bytes = 1024 + p.ctrl_off + tc_ctrl_bytes(st, num_seqs);
   p.q_tx = (D / 64) * 128 * p.G * p.BM;
   int per_sm = 0;
