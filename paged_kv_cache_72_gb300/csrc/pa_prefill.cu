@@ -504,9 +504,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
 //    owns query row r of its tile, which is TMEM lane r.  Per 64-key stage it
 //    reads its row of S, masks it, updates the running maximum and sum, and
 //    writes its row of P (16-bit) into one of its tile's two P regions of
-//    tensor memory.  The maximum used
-//    for the exponentials moves only when a row's maximum passes it by more
-//    than kTcTau (log2 units): then the row of O is rescaled in TMEM;
+//    tensor memory.  The maximum used for the exponentials moves only when a
+//    row's maximum passes it by more than kTcTau (log2 units): then the row
+//    of O is rescaled in TMEM;
 //    otherwise P stays below 2^kTcTau and O, l and the stale maximum stay
 //    consistent (the result is their quotient).  At the tile's last stage it
 //    reads O, divides by l and writes the rows.  Tile A needs at most the
@@ -549,7 +549,7 @@ __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
   return ((4 * (num_seqs + 1) + 15) / 16) * 16;
 }
 
-// shared-memory control area of the tensor-core kernel (after the P buffers):
+// shared-memory control area of the tensor-core kernel (after the query tiles):
 // full/empty/seen barriers, the other barriers, stage tags (two int4 per
 // stage, from a 16-byte boundary), TMEM address and flags, item offsets, scan
 // scratch
@@ -746,8 +746,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // both tiles' was the bottleneck (an issue takes tens of cycles).  Each
     // walks every stage.  An event loop: the tile's oldest pending O += P . V
     // is issued as soon as its P is written (first: the softmax waits on it to
-    // reuse the P buffer), and the next stage's S = Q . K^T as soon as its K/V
-    // have landed (and the query tile, and a free S buffer), once at most one
+    // reuse the P region and to rescale O), and the next stage's S = Q . K^T
+    // as soon as its K/V have landed (and the query tile, and the S buffer's
+    // previous scores have been read), once at most one
     // stage's O += P . V is pending, so that a P . V is never queued behind
     // score products two stages ahead (the tensor pipe executes in issue
     // order).  A stage and the query tiles are released by a commit of each
