@@ -57,7 +57,7 @@ struct PrefillArgs {
   int sub_log2, hi_log2;        // in a stage part: box j at j << sub_log2, 64-column plane at
                                 // hi << hi_log2, row r at r << 7
   int kv_bytes, stage_bytes, ctrl_off;
-  int q_off, p_off, q_tx;       // tensor-core kernel: query and P buffers, bytes of one query tile
+  int q_off, q_tx;              // tensor-core kernel: query tiles, bytes of one query tile
 };
 
 struct Item {
@@ -1090,7 +1090,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 struct PrefillPlan {
   bool bf16, tc;
   int D, G, B, R, nsb, BM, stages, kv_bytes, stage_bytes, ctrl_off, smem_bytes, grid;
-  int q_off, p_off, q_tx;
+  int q_off, q_tx;
 };
 
 int ctrl_bytes(int S) { return 32 * S + 4 * (kPMaxSeqs + 1) + 12 + 16 * 8 + 16; }
@@ -1146,8 +1146,7 @@ int make_tc_plan(int Hq, int Hkv, int D, int B, int dtype, int num_seqs, Prefill
   if (st < 2) return PA_ERR_UNSUPPORTED;
   p.stages = st;
   p.q_off = st * p.stage_bytes;
-  p.p_off = p.q_off + 2 * qbuf;   // (unused by the tensor-core kernel)
-  p.ctrl_off = p.p_off;
+  p.ctrl_off = p.q_off + 2 * qbuf;
   p.smem_bytes = 1024 + p.ctrl_off + tc_ctrl_bytes(st, num_seqs);
   p.q_tx = (D / 64) * 128 * p.G * p.BM;
   int per_sm = 0;
@@ -1290,7 +1289,6 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
   a.stage_bytes = p.stage_bytes;
   a.ctrl_off = p.ctrl_off;
   a.q_off = p.q_off;
-  a.p_off = p.p_off;
   a.q_tx = p.q_tx;
   clear_stale_error();
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
