@@ -743,17 +743,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp >= kTcMma) {
     // ======================= MMA issue (one thread per tile) =================
     // Warp 9 issues tile A's products, warp 10 tile B's: one thread issuing
-    // both tiles' was the bottleneck (an issue takes tens of cycles).  Each
-    // walks every stage.  An event loop: the tile's oldest pending O += P . V
-    // is issued as soon as its P is written (first: the softmax waits on it to
-    // reuse the P region and to rescale O), and the next stage's S = Q . K^T
-    // as soon as its K/V have landed (and the query tile, and the S buffer's
-    // previous scores have been read), once at most one
-    // stage's O += P . V is pending, so that a P . V is never queued behind
-    // score products two stages ahead (the tensor pipe executes in issue
-    // order).  A stage and the query tiles are released by a commit of each
-    // issuer (barriers of count 2), made after its last product that reads
-    // them (at once where its tile does not read the stage).
+    // both tiles' was the bottleneck (an issue returns after about a hundred
+    // cycles).  Each walks every stage.  An event loop: the tile's oldest
+    // pending O += P . V is issued as soon as its P is written (first: the
+    // softmax waits on it to reuse the P region and to rescale O), and the
+    // next stage's S = Q . K^T as soon as its K/V have landed, the query tile
+    // has, and the S buffer's previous scores have been read -- once at most
+    // one stage's O += P . V is pending, so that a P . V is never queued
+    // behind score products two stages ahead (the tensor pipe executes in
+    // issue order).  A stage and the query tiles are released by a commit of
+    // each issuer (barriers of count 2), made after its last product that
+    // reads them (at once where its tile does not read the stage).
     const int t = warp - kTcMma;
     if (lane == 0) {
       constexpr uint32_t id_s = umma_idesc_f16(kBF16, 128, kPBN, false);
