@@ -116,6 +116,25 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, in
                    pa_stream stream);
 
 /*
+ * pa_cache_write_mapped -- pa_slot_mapping and pa_cache_write in one launch.
+ * [P1] "How is vLLM's KV cache paged?", bullet "Writing": each new token at
+ * position t of sequence i is stored at slot block_table[i][t / B] * B + t % B.
+ * Arguments as in those two calls: block_tables int32 [num_seqs][table_stride],
+ * token_seq / token_pos int32 [num_tokens], k, v [num_tokens][num_kv_heads]
+ * [head_dim] contiguous in the pool dtype (PA_F16 or PA_BF16).  slot_mapping,
+ * int64 [num_tokens], receives the slots when not NULL.  A token with a bad
+ * sequence index or position (PA_DEVERR_POSITION) or table entry
+ * (PA_DEVERR_BLOCK_ID) gets slot -1 and writes nothing.  The pools and
+ * err_word end as after pa_slot_mapping followed by pa_cache_write.
+ */
+int pa_cache_write_mapped(const void* k, const void* v, const int32_t* block_tables,
+                          int32_t table_stride, int32_t num_seqs, const int32_t* token_seq,
+                          const int32_t* token_pos, int64_t num_tokens, void* k_cache,
+                          void* v_cache, int64_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                          int64_t* slot_mapping, int32_t* err_word, pa_stream stream);
+
+/*
  * pa_copy_blocks -- copy-on-write block copies.
  * [P1] "What operations can cause memory fragmentation, and how does vLLM avoid
  * it?", bullet "Sharing instead of copying": a shared block is copied only when

@@ -42,6 +42,8 @@ SIGNATURES = {
     "pa_slot_mapping": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp]),
     "pa_cache_write": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _i32,
                                       _vp, _vp]),
+    "pa_cache_write_mapped": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _i64, _vp, _vp,
+                                             _i64, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "pa_copy_blocks": (ctypes.c_int, [_vp, _i32, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp, _vp]),
     "pa_swap_blocks": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32,
                                       _i32, _i32, _vp, _vp]),

@@ -71,6 +71,63 @@ __global__ void cache_write_kernel(const uint4* __restrict__ k, const uint4* __r
   }
 }
 
+// Slot mapping and cache write in one launch: one CTA per new token.  Thread
+// 0 finds the token's slot from its (sequence, position) and the block table,
+// with the checks of slot_mapping_kernel, and writes it to slots when given;
+// meanwhile every thread loads its first vectors of the token's K and V rows,
+// which are then stored at the slot.  Saves the second kernel's start and its
+// read of the slots.
+__global__ void cache_write_mapped_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                          const int32_t* __restrict__ bt, int stride, int num_seqs,
+                                          const int32_t* __restrict__ tok_seq,
+                                          const int32_t* __restrict__ tok_pos, int log2B,
+                                          long long num_blocks, int vecs_per_row,
+                                          uint4* __restrict__ kc, uint4* __restrict__ vc,
+                                          int64_t* __restrict__ slots, int32_t* err) {
+  __shared__ long long s_slot;
+  grid_dep_wait();
+  grid_dep_launch();
+  const long long tok = blockIdx.x;
+  const uint4* ks = k + tok * vecs_per_row;
+  const uint4* vs = v + tok * vecs_per_row;
+  const int e0 = threadIdx.x;
+  uint4 a0 = make_uint4(0u, 0u, 0u, 0u), b0 = a0;
+  if (e0 < vecs_per_row) {
+    a0 = __ldg(ks + e0);
+    b0 = __ldg(vs + e0);
+  }
+  if (threadIdx.x == 0) {
+    const int i = tok_seq[tok];
+    const int t = tok_pos[tok];
+    long long sl = -1;
+    if (i < 0 || i >= num_seqs || t < 0 || (long long)t >= ((long long)stride << log2B)) {
+      set_error(err, PA_DEVERR_POSITION);
+    } else {
+      const int p = bt[(size_t)i * stride + (t >> log2B)];
+      if (p < 0 || (long long)p >= num_blocks) {
+        set_error(err, PA_DEVERR_BLOCK_ID);
+      } else {
+        sl = ((long long)p << log2B) + (t & ((1 << log2B) - 1));
+      }
+    }
+    if (slots) slots[tok] = sl;
+    s_slot = sl;
+  }
+  __syncthreads();
+  const long long sl = s_slot;
+  if (sl < 0) return;
+  uint4* kd = kc + sl * vecs_per_row;
+  uint4* vd = vc + sl * vecs_per_row;
+  if (e0 < vecs_per_row) {
+    kd[e0] = a0;
+    vd[e0] = b0;
+  }
+  for (int e = e0 + blockDim.x; e < vecs_per_row; e += blockDim.x) {
+    kd[e] = __ldg(ks + e);
+    vd[e] = __ldg(vs + e);
+  }
+}
+
 // E4M3 cache write: one block per new token; each thread turns 8 16-bit
 // elements (16 bytes) of the token's K and V rows into 8 codes (8 bytes).
 template <bool kBF16>
@@ -229,6 +286,34 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, in
                                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                   err_word),
                        "cache write launch");
+}
+
+int pa_cache_write_mapped(const void* k, const void* v, const int32_t* block_tables,
+                          int32_t table_stride, int32_t num_seqs, const int32_t* token_seq,
+                          const int32_t* token_pos, int64_t num_tokens, void* k_cache,
+                          void* v_cache, int64_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                          int64_t* slot_mapping, int32_t* err_word, pa_stream stream) {
+  if (num_tokens < 0 || num_seqs < 0 || table_stride < 0 || num_blocks < 0)
+    return PA_ERR_INVALID_ARG;
+  if (!shape_ok(block_size, num_kv_heads, head_dim, dtype)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (num_tokens > 0x7fffffffLL) return PA_ERR_INVALID_ARG;
+  if (!k || !v || !block_tables || !token_seq || !token_pos || !k_cache || !v_cache)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const int vecs = num_kv_heads * head_dim * 2 / 16;
+  const int threads = vecs >= 256 ? 256 : (vecs >= 128 ? 128 : 64);
+  clear_stale_error();
+  return launch_status(
+      launch_pdl(cache_write_mapped_kernel, dim3((unsigned)num_tokens), dim3(threads), 0,
+                 static_cast<cudaStream_t>(stream), static_cast<const uint4*>(k),
+                 static_cast<const uint4*>(v), block_tables, (int)table_stride, (int)num_seqs,
+                 token_seq, token_pos, ilog2(block_size), (long long)num_blocks, vecs,
+                 static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping,
+                 err_word),
+      "slot-mapped cache write launch");
 }
 
 int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cache, void* v_cache,

@@ -105,6 +105,38 @@ def pa_cache_write(k, v, slot_mapping, k_cache, v_cache, err=None):
                             _stream()), "pa_cache_write")
 
 
+def pa_cache_write_mapped(k, v, block_tables, token_seq, token_pos, k_cache, v_cache,
+                          slot_mapping=None, err=None):
+    """pa_slot_mapping and pa_cache_write in one launch: store k[n], v[n]
+    ([n_tok, H_kv, D]) at slot block_tables[seq][pos // B] * B + pos % B of
+    new token n; the int64 slots go to slot_mapping when given."""
+    L = _lib.load()
+    nb, B, H, D = _pool_shape(k_cache, v_cache)
+    for t, n in ((block_tables, "block_tables"), (token_seq, "token_seq"), (token_pos, "token_pos")):
+        _cuda(t, n)
+        if t.dtype != torch.int32:
+            raise TypeError("%s must be int32" % n)
+    _cuda(k, "k")
+    _cuda(v, "v")
+    n_tok = token_seq.numel()
+    if token_pos.numel() != n_tok:
+        raise ValueError("token_seq and token_pos differ in length")
+    if k.shape != (n_tok, H, D) or v.shape != (n_tok, H, D):
+        raise ValueError("k, v must be [num_tokens, H_kv, D]")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype:
+        raise TypeError("k, v and the pools must share a dtype")
+    if slot_mapping is not None:
+        _cuda(slot_mapping, "slot_mapping")
+        if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != n_tok:
+            raise ValueError("slot_mapping must be int64 [num_tokens]")
+    _check(L.pa_cache_write_mapped(_ptr(k), _ptr(v), _ptr(block_tables), block_tables.shape[1],
+                                   block_tables.shape[0], _ptr(token_seq), _ptr(token_pos), n_tok,
+                                   _ptr(k_cache), _ptr(v_cache), nb, B, H, D,
+                                   _dtype_code(k_cache), _ptr(slot_mapping), _ptr(err), _stream()),
+           "pa_cache_write_mapped")
+    return slot_mapping
+
+
 def pa_copy_blocks(pairs, k_cache, v_cache, err=None):
     """Copy pool block src -> dst (K and V) for each row (src, dst) of pairs.
 

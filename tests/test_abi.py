@@ -86,4 +86,14 @@ def test_host_checks_need_no_device(lib):
     # missing pointers and negative sizes
     assert lib.pa_cache_write(None, None, None, 3, None, None, 10, 16, 8, 128, 0, None, None) == 1
     assert lib.pa_cache_write(None, None, None, -1, None, None, 10, 16, 8, 128, 0, None, None) == 1
+    # the slot-mapped cache write: no tokens is a no-op, missing inputs or a
+    # negative count are refused, E4M3 pools are not its dtype
+    assert lib.pa_cache_write_mapped(None, None, None, 4, 2, None, None, 0, None, None, 10, 16, 8,
+                                     128, 0, None, None, None) == 0
+    assert lib.pa_cache_write_mapped(None, None, None, 4, 2, None, None, 3, None, None, 10, 16, 8,
+                                     128, 0, None, None, None) == 1
+    assert lib.pa_cache_write_mapped(None, None, None, 4, 2, None, None, -1, None, None, 10, 16, 8,
+                                     128, 0, None, None, None) == 1
+    assert lib.pa_cache_write_mapped(None, None, None, 4, 2, None, None, 3, None, None, 10, 16, 8,
+                                     128, 2, None, None, None) == 2
     assert lib.pa_get_error(None, None, None) == 1

@@ -112,3 +112,53 @@ def test_empty_calls_are_no_ops(cuda_device):
                       torch.zeros((0, 2, 64), dtype=torch.float16, device="cuda"),
                       torch.zeros(0, dtype=torch.int64, device="cuda"), kc, kc.clone())
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("make", [W.tiny, W.shared_prefix,
+                                  lambda: W.random_workload(44, W.BF16, 32, 8, 128, 16,
+                                                            [1, 16, 17, 300, 777])])
+def test_slot_mapped_cache_write_is_bit_exact(cuda_device, make):
+    # the one-launch slot mapping + cache write stores the same bytes and
+    # returns the same slots as the oracle's scatter ("vLLM Framework and
+    # Inference Engine Design", "How is vLLM's KV cache paged?", "Writing")
+    wl = make()
+    st = GpuState(wl)
+    ref = OracleState(wl)
+    ref.step()
+    if st.pairs.numel():
+        pa.pa_copy_blocks(st.pairs, st.k_cache, st.v_cache, err=st.err)
+    slots = torch.full((wl.new_seq.size,), 7, dtype=torch.int64, device="cuda")
+    pa.pa_cache_write_mapped(st.k_new, st.v_new, st.block_tables, st.new_seq, st.new_pos,
+                             st.k_cache, st.v_cache, slot_mapping=slots, err=st.err)
+    assert np.array_equal(slots.cpu().numpy(), ref.slots)
+    assert np.array_equal(bits_of(st.k_cache), ref.k_cache)
+    assert np.array_equal(bits_of(st.v_cache), ref.v_cache)
+    assert pa.pa_get_error(st.err) == 0
+
+
+def test_slot_mapped_cache_write_flags_bad_tokens(cuda_device):
+    # bad sequence index, position or table entry: slot -1, nothing written,
+    # the same error bits as the slot mapping
+    H, D, B, nb = 2, 64, 4, 4
+    bt = torch.tensor([[3, 1], [0, 9]], dtype=torch.int32, device="cuda")
+    seq = torch.tensor([0, 1, 2, 0, 1], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([5, 1, 0, -1, 6], dtype=torch.int32, device="cuda")
+    k = torch.randn(5, H, D, device="cuda").to(torch.float16)
+    v = torch.randn(5, H, D, device="cuda").to(torch.float16)
+    kc = torch.zeros(nb, B, H, D, dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.zeros(5, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_cache_write_mapped(k, v, bt, seq, pos, kc, vc, slot_mapping=slots, err=err)
+    assert slots.cpu().tolist() == [5, 1, -1, -1, -1]
+    assert pa.pa_get_error(err) == pa.PA_DEVERR_POSITION | pa.PA_DEVERR_BLOCK_ID
+    kf, vf = kc.view(nb * B, H, D), vc.view(nb * B, H, D)
+    assert torch.equal(kf[5], k[0]) and torch.equal(vf[5], v[0])
+    assert torch.equal(kf[1], k[1]) and torch.equal(vf[1], v[1])
+    written = torch.zeros(nb * B, dtype=torch.bool)
+    written[[1, 5]] = True
+    assert not kf[~written.cuda()].any() and not vf[~written.cuda()].any()
+    # without a slot output the pools end the same
+    kc2, vc2 = torch.zeros_like(kc), torch.zeros_like(vc)
+    pa.pa_cache_write_mapped(k, v, bt, seq, pos, kc2, vc2)
+    assert torch.equal(kc2, kc) and torch.equal(vc2, vc)
