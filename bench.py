@@ -237,22 +237,20 @@ class Step:
         self.decode_ms = []
 
     def launches_per_step(self):
-        # copy-on-write (if any), the slot-mapped cache write (a slot mapping
-        # and a quantizing write for an E4M3 cache), decode (split contexts are
-        # merged inside the decode grid)
-        return (1 if self.pairs.numel() else 0) + (2 if self.wl.fp8 else 1) + 1
+        # copy-on-write (if any), the slot-mapped cache write, decode (split
+        # contexts are merged inside the decode grid)
+        return (1 if self.pairs.numel() else 0) + 1 + 1
 
     def write_phase(self):
         pa, wl = self.pa, self.wl
         if self.pairs.numel():
             pa.pa_copy_blocks(self.pairs, self.k_cache, self.v_cache, err=self.err)
+        # slot mapping and cache write in one launch
         if wl.fp8:
-            pa.pa_slot_mapping(self.block_tables, self.new_seq, self.new_pos, wl.block_size,
-                               wl.num_blocks, out=self.slots, err=self.err)
-            pa.pa_cache_write_fp8(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
-                                  wl.k_scale, wl.v_scale, err=self.err)
+            pa.pa_cache_write_fp8_mapped(self.k_new, self.v_new, self.block_tables, self.new_seq,
+                                         self.new_pos, self.k_cache, self.v_cache, wl.k_scale,
+                                         wl.v_scale, slot_mapping=self.slots, err=self.err)
         else:
-            # slot mapping and cache write in one launch
             pa.pa_cache_write_mapped(self.k_new, self.v_new, self.block_tables, self.new_seq,
                                      self.new_pos, self.k_cache, self.v_cache,
                                      slot_mapping=self.slots, err=self.err)

@@ -200,6 +200,22 @@ int pa_cache_write_fp8(const void* k, const void* v, int32_t src_dtype,
                        int32_t* err_word, pa_stream stream);
 
 /*
+ * pa_cache_write_fp8_mapped -- pa_slot_mapping and pa_cache_write_fp8 in one
+ * launch.  [P1] "How is vLLM's KV cache paged?", bullet "Writing" (the slots);
+ * the E4M3 reading of pa_cache_write_fp8 (the codes).  Arguments as in those
+ * two calls; slot_mapping, int64 [num_tokens], receives the slots when not
+ * NULL.  A bad token gets slot -1 and writes nothing, with the error bits of
+ * pa_slot_mapping.  The pools and err_word end as after the two calls.
+ */
+int pa_cache_write_fp8_mapped(const void* k, const void* v, int32_t src_dtype,
+                              const int32_t* block_tables, int32_t table_stride, int32_t num_seqs,
+                              const int32_t* token_seq, const int32_t* token_pos,
+                              int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                              int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                              float k_scale, float v_scale, int64_t* slot_mapping,
+                              int32_t* err_word, pa_stream stream);
+
+/*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
  * this shape on the current device: a fixed region of PA_DECODE_MAX_CTAS
  * 32-bit piece counters, then the partial softmax states of contexts split

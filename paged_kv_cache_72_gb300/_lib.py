@@ -49,6 +49,9 @@ SIGNATURES = {
                                       _i32, _i32, _vp, _vp]),
     "pa_cache_write_fp8": (ctypes.c_int, [_vp, _vp, _i32, _vp, _i64, _vp, _vp, _i64, _i32, _i32,
                                           _i32, ctypes.c_float, ctypes.c_float, _vp, _vp]),
+    "pa_cache_write_fp8_mapped": (ctypes.c_int, [_vp, _vp, _i32, _vp, _i32, _i32, _vp, _vp, _i64,
+                                                 _vp, _vp, _i64, _i32, _i32, _i32, ctypes.c_float,
+                                                 ctypes.c_float, _vp, _vp, _vp]),
     "pa_decode_workspace_size": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                                 ctypes.POINTER(_sz)]),
     "pa_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i64,

@@ -71,6 +71,26 @@ __global__ void cache_write_kernel(const uint4* __restrict__ k, const uint4* __r
   }
 }
 
+// The slot of new token tok, with the checks of slot_mapping_kernel: -1 (and
+// an error bit) for a bad sequence index, position or table entry.
+__device__ __forceinline__ long long token_slot(const int32_t* __restrict__ bt, int stride,
+                                                int num_seqs, const int32_t* __restrict__ tok_seq,
+                                                const int32_t* __restrict__ tok_pos, long long tok,
+                                                int log2B, long long num_blocks, int32_t* err) {
+  const int i = tok_seq[tok];
+  const int t = tok_pos[tok];
+  if (i < 0 || i >= num_seqs || t < 0 || (long long)t >= ((long long)stride << log2B)) {
+    set_error(err, PA_DEVERR_POSITION);
+    return -1;
+  }
+  const int p = bt[(size_t)i * stride + (t >> log2B)];
+  if (p < 0 || (long long)p >= num_blocks) {
+    set_error(err, PA_DEVERR_BLOCK_ID);
+    return -1;
+  }
+  return ((long long)p << log2B) + (t & ((1 << log2B) - 1));
+}
+
 // Slot mapping and cache write in one launch: one CTA per new token.  Thread
 // 0 finds the token's slot from its (sequence, position) and the block table,
 // with the checks of slot_mapping_kernel, and writes it to slots when given;
@@ -97,19 +117,8 @@ __global__ void cache_write_mapped_kernel(const uint4* __restrict__ k, const uin
     b0 = __ldg(vs + e0);
   }
   if (threadIdx.x == 0) {
-    const int i = tok_seq[tok];
-    const int t = tok_pos[tok];
-    long long sl = -1;
-    if (i < 0 || i >= num_seqs || t < 0 || (long long)t >= ((long long)stride << log2B)) {
-      set_error(err, PA_DEVERR_POSITION);
-    } else {
-      const int p = bt[(size_t)i * stride + (t >> log2B)];
-      if (p < 0 || (long long)p >= num_blocks) {
-        set_error(err, PA_DEVERR_BLOCK_ID);
-      } else {
-        sl = ((long long)p << log2B) + (t & ((1 << log2B) - 1));
-      }
-    }
+    const long long sl = token_slot(bt, stride, num_seqs, tok_seq, tok_pos, tok, log2B,
+                                    num_blocks, err);
     if (slots) slots[tok] = sl;
     s_slot = sl;
   }
@@ -160,6 +169,58 @@ __global__ void cache_write_fp8_kernel(const uint4* __restrict__ k, const uint4*
   uint2* kd = kc + s * vecs_per_row;
   uint2* vd = vc + s * vecs_per_row;
   for (int e = threadIdx.x; e < vecs_per_row; e += blockDim.x) {
+    kd[e] = quantize8(__ldg(ks + e), k_scale);
+    vd[e] = quantize8(__ldg(vs + e), v_scale);
+  }
+}
+
+// The E4M3 cache write with its slot mapping in one launch, as
+// cache_write_mapped_kernel does for 16-bit pools.
+template <bool kBF16>
+__global__ void cache_write_fp8_mapped_kernel(
+    const uint4* __restrict__ k, const uint4* __restrict__ v, const int32_t* __restrict__ bt,
+    int stride, int num_seqs, const int32_t* __restrict__ tok_seq,
+    const int32_t* __restrict__ tok_pos, int log2B, long long num_blocks, int vecs_per_row,
+    uint2* __restrict__ kc, uint2* __restrict__ vc, float k_scale, float v_scale,
+    int64_t* __restrict__ slots, int32_t* err) {
+  __shared__ long long s_slot;
+  grid_dep_wait();
+  grid_dep_launch();
+  const long long tok = blockIdx.x;
+  const uint4* ks = k + tok * vecs_per_row;
+  const uint4* vs = v + tok * vecs_per_row;
+  const int e0 = threadIdx.x;
+  uint4 a0 = make_uint4(0u, 0u, 0u, 0u), b0 = a0;
+  if (e0 < vecs_per_row) {
+    a0 = __ldg(ks + e0);
+    b0 = __ldg(vs + e0);
+  }
+  if (threadIdx.x == 0) {
+    const long long sl = token_slot(bt, stride, num_seqs, tok_seq, tok_pos, tok, log2B,
+                                    num_blocks, err);
+    if (slots) slots[tok] = sl;
+    s_slot = sl;
+  }
+  __syncthreads();
+  const long long sl = s_slot;
+  if (sl < 0) return;
+  auto quantize8 = [](const uint4 x, float scale) -> uint2 {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack2<kBF16>(w[i]);
+      c[i] = f32x2_to_e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  };
+  uint2* kd = kc + sl * vecs_per_row;
+  uint2* vd = vc + sl * vecs_per_row;
+  if (e0 < vecs_per_row) {
+    kd[e0] = quantize8(a0, k_scale);
+    vd[e0] = quantize8(b0, v_scale);
+  }
+  for (int e = e0 + blockDim.x; e < vecs_per_row; e += blockDim.x) {
     kd[e] = quantize8(__ldg(ks + e), k_scale);
     vd[e] = quantize8(__ldg(vs + e), v_scale);
   }
@@ -405,6 +466,46 @@ int pa_cache_write_fp8(const void* k, const void* v, int32_t src_dtype,
                        static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), k_scale,
                        v_scale, err_word);
   return launch_status(e, "E4M3 cache write launch");
+}
+
+int pa_cache_write_fp8_mapped(const void* k, const void* v, int32_t src_dtype,
+                              const int32_t* block_tables, int32_t table_stride, int32_t num_seqs,
+                              const int32_t* token_seq, const int32_t* token_pos,
+                              int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                              int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                              float k_scale, float v_scale, int64_t* slot_mapping,
+                              int32_t* err_word, pa_stream stream) {
+  if (num_tokens < 0 || num_seqs < 0 || table_stride < 0 || num_blocks < 0)
+    return PA_ERR_INVALID_ARG;
+  if (!shape_ok(block_size, num_kv_heads, head_dim, src_dtype)) return PA_ERR_UNSUPPORTED;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale > 3.0e38f || v_scale > 3.0e38f)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (num_tokens > 0x7fffffffLL) return PA_ERR_INVALID_ARG;
+  if (!k || !v || !block_tables || !token_seq || !token_pos || !k_cache || !v_cache)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const int vecs = num_kv_heads * head_dim / 8;   // 16-byte input vectors per row
+  const int threads = vecs >= 256 ? 256 : (vecs >= 128 ? 128 : 64);
+  clear_stale_error();
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int log2B = ilog2(block_size);
+  cudaError_t e =
+      src_dtype == PA_BF16
+          ? launch_pdl(cache_write_fp8_mapped_kernel<true>, dim3((unsigned)num_tokens),
+                       dim3(threads), 0, s, static_cast<const uint4*>(k),
+                       static_cast<const uint4*>(v), block_tables, (int)table_stride,
+                       (int)num_seqs, token_seq, token_pos, log2B, (long long)num_blocks, vecs,
+                       static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), k_scale,
+                       v_scale, slot_mapping, err_word)
+          : launch_pdl(cache_write_fp8_mapped_kernel<false>, dim3((unsigned)num_tokens),
+                       dim3(threads), 0, s, static_cast<const uint4*>(k),
+                       static_cast<const uint4*>(v), block_tables, (int)table_stride,
+                       (int)num_seqs, token_seq, token_pos, log2B, (long long)num_blocks, vecs,
+                       static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), k_scale,
+                       v_scale, slot_mapping, err_word);
+  return launch_status(e, "slot-mapped E4M3 cache write launch");
 }
 
 }  // extern "C"

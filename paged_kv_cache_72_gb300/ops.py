@@ -201,6 +201,40 @@ def pa_cache_write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, e
                                 float(v_scale), _ptr(err), _stream()), "pa_cache_write_fp8")
 
 
+def pa_cache_write_fp8_mapped(k, v, block_tables, token_seq, token_pos, k_cache, v_cache,
+                              k_scale, v_scale, slot_mapping=None, err=None):
+    """pa_slot_mapping and pa_cache_write_fp8 in one launch: E4M3 codes of
+    k[n] / k_scale and v[n] / v_scale ([n_tok, H_kv, D], float16 / bfloat16)
+    stored at slot block_tables[seq][pos // B] * B + pos % B of new token n;
+    the int64 slots go to slot_mapping when given."""
+    L = _lib.load()
+    nb, B, H, D = _pool_shape(k_cache, v_cache)
+    for t, n in ((block_tables, "block_tables"), (token_seq, "token_seq"), (token_pos, "token_pos")):
+        _cuda(t, n)
+        if t.dtype != torch.int32:
+            raise TypeError("%s must be int32" % n)
+    _cuda(k, "k")
+    _cuda(v, "v")
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("E4M3 pools are uint8 codes")
+    n_tok = token_seq.numel()
+    if token_pos.numel() != n_tok:
+        raise ValueError("token_seq and token_pos differ in length")
+    if k.shape != (n_tok, H, D) or v.shape != (n_tok, H, D) or k.dtype != v.dtype:
+        raise ValueError("k, v must be [num_tokens, H_kv, D] of one dtype")
+    if slot_mapping is not None:
+        _cuda(slot_mapping, "slot_mapping")
+        if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != n_tok:
+            raise ValueError("slot_mapping must be int64 [num_tokens]")
+    _check(L.pa_cache_write_fp8_mapped(_ptr(k), _ptr(v), _dtype_code(k), _ptr(block_tables),
+                                       block_tables.shape[1], block_tables.shape[0],
+                                       _ptr(token_seq), _ptr(token_pos), n_tok, _ptr(k_cache),
+                                       _ptr(v_cache), nb, B, H, D, float(k_scale), float(v_scale),
+                                       _ptr(slot_mapping), _ptr(err), _stream()),
+           "pa_cache_write_fp8_mapped")
+    return slot_mapping
+
+
 def pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, block_size, dtype,
                              flags=PA_DECODE_AUTO, num_ctas=0):
     L = _lib.load()

@@ -96,4 +96,10 @@ def test_host_checks_need_no_device(lib):
                                      128, 0, None, None, None) == 1
     assert lib.pa_cache_write_mapped(None, None, None, 4, 2, None, None, 3, None, None, 10, 16, 8,
                                      128, 2, None, None, None) == 2
+    assert lib.pa_cache_write_fp8_mapped(None, None, 1, None, 4, 2, None, None, 0, None, None, 10,
+                                         16, 8, 128, 1.0, 1.0, None, None, None) == 0
+    assert lib.pa_cache_write_fp8_mapped(None, None, 1, None, 4, 2, None, None, 3, None, None, 10,
+                                         16, 8, 128, 1.0, 1.0, None, None, None) == 1
+    assert lib.pa_cache_write_fp8_mapped(None, None, 1, None, 4, 2, None, None, 3, None, None, 10,
+                                         16, 8, 128, 0.0, 1.0, None, None, None) == 1
     assert lib.pa_get_error(None, None, None) == 1

@@ -52,6 +52,35 @@ def test_fp8_cache_write_is_bit_exact_with_saturation_and_ties(cuda_device):
         assert np.any((codes & 0x7F) == 0x7E)
 
 
+def test_fp8_slot_mapped_cache_write_is_bit_exact(cuda_device):
+    # the one-launch slot mapping + quantizing write gives the oracle's slots
+    # and codes (saturation included) and leaves the pools as the two calls do
+    for dtype, scales in ((W.BF16, (0.004, 0.0021)), (W.F16, (2.0 ** -7, 0.05))):
+        wl = W.random_workload(52, dtype, 8, 8, 128, 16, [3, 40, 129], fp8_scales=scales)
+        st = GpuState(wl)
+        ref = OracleState(wl)
+        ref.step()
+        slots = torch.full((wl.new_seq.size,), 7, dtype=torch.int64, device="cuda")
+        pa.pa_cache_write_fp8_mapped(st.k_new, st.v_new, st.block_tables, st.new_seq, st.new_pos,
+                                     st.k_cache, st.v_cache, wl.k_scale, wl.v_scale,
+                                     slot_mapping=slots, err=st.err)
+        assert np.array_equal(slots.cpu().numpy(), ref.slots)
+        assert np.array_equal(st.k_cache.cpu().numpy(), ref.k_cache)
+        assert np.array_equal(st.v_cache.cpu().numpy(), ref.v_cache)
+        assert pa.pa_get_error(st.err) == 0
+    # a bad table entry: slot -1, nothing written, the block-id bit
+    bt = torch.tensor([[9]], dtype=torch.int32, device="cuda")
+    one = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k = torch.ones(1, 2, 64, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 4, 2, 64, dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.zeros(1, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_cache_write_fp8_mapped(k, k, bt, one, one, kc, vc, 1.0, 1.0, slot_mapping=slots, err=err)
+    assert slots.item() == -1 and not kc.any() and not vc.any()
+    assert pa.pa_get_error(err) == pa.PA_DEVERR_BLOCK_ID
+
+
 CASES = [
     # q dtype, Hq, Hkv, D, B
     (W.BF16, 8, 8, 128, 16),     # G = 1: CUDA-core kernel
