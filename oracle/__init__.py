@@ -63,11 +63,11 @@ def lib():
         L.or_gather_bits.argtypes = [u16p, i32p, ctypes.c_int64, ctypes.c_int32,
                                      ctypes.c_int32, ctypes.c_int32, u16p]
         L.or_attention_1q.argtypes = [f64p, f64p, f64p, ctypes.c_int64, ctypes.c_int32,
-                                      ctypes.c_double, f64p, f64p]
+                                      ctypes.c_double, f64p, f64p, f64p]
         L.or_paged_decode.argtypes = [u16p, u16p, u16p, ctypes.c_int, i32p, ctypes.c_int64,
                                       i32p, i32p, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                      ctypes.c_double, f64p, ctypes.c_int]
+                                      ctypes.c_double, f64p, f64p, ctypes.c_int]
         L.or_paged_decode.restype = ctypes.c_int
         L.or_contiguous_decode.argtypes = [f64p, f64p, f64p, ctypes.c_int64, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_double, f64p]
@@ -89,19 +89,19 @@ def lib():
                                           ctypes.c_double, i32p, ctypes.c_int64, i32p, i32p,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_double, f64p,
-                                          ctypes.c_int]
+                                          f64p, ctypes.c_int]
         L.or_paged_decode_fp8.restype = ctypes.c_int
         L.or_paged_decode_window.argtypes = [u16p, u16p, u16p, ctypes.c_int, i32p,
                                              ctypes.c_int64, i32p, ctypes.c_int32, i32p,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
-                                             f64p, ctypes.c_int]
+                                             f64p, f64p, ctypes.c_int]
         L.or_paged_decode_window.restype = ctypes.c_int
         L.or_swap_blocks.argtypes = [u8p, u8p, u8p, u8p, i32p, ctypes.c_int64, ctypes.c_int64]
         L.or_paged_prefill.argtypes = [u16p, u16p, u16p, ctypes.c_int, i32p, ctypes.c_int64,
                                        i32p, i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_double, f64p,
-                                       ctypes.c_int]
+                                       f64p, ctypes.c_int]
         L.or_paged_prefill.restype = ctypes.c_int
         L.or_max_threads.restype = ctypes.c_int
         _lib = L
@@ -110,6 +110,11 @@ def lib():
 
 def _p(a, ctype):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _opt(a):
+    """fp64 array pointer, or NULL for None."""
+    return ctypes.POINTER(ctypes.c_double)() if a is None else _p(a, ctypes.c_double)
 
 
 def _u16(a):
@@ -234,27 +239,32 @@ def gather_head(cache, dtype, table_row, T, h):
 # Attention   [P1 "What is the essence of vLLM's PagedAttention?"]
 # --------------------------------------------------------------------------
 
-def attention_1q(q, K, V, scale):
-    """softmax(scale * q.K^T) . V for one query: q [D], K, V [T, D] (fp64)."""
+def attention_1q(q, K, V, scale, spread=False):
+    """softmax(scale * q.K^T) . V for one query: q [D], K, V [T, D] (fp64).
+
+    With spread=True returns (out, spread), spread[d] = sum_t w_t |V[t, d] -
+    out[d]| (the weighted mean absolute deviation about the output)."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     K = np.ascontiguousarray(K, dtype=np.float64)
     V = np.ascontiguousarray(V, dtype=np.float64)
     T, D = K.shape
     out = np.empty(D, dtype=np.float64)
     scratch = np.empty(max(T, 1), dtype=np.float64)
+    sp = np.empty(D, dtype=np.float64) if spread else None
     lib().or_attention_1q(_p(q, ctypes.c_double), _p(K, ctypes.c_double),
                           _p(V, ctypes.c_double), T, D, float(scale),
-                          _p(out, ctypes.c_double), _p(scratch, ctypes.c_double))
-    return out
+                          _p(out, ctypes.c_double), _p(scratch, ctypes.c_double), _opt(sp))
+    return (out, sp) if spread else out
 
 
 def paged_decode(q, k_cache, v_cache, dtype, block_tables, seq_lens, scale,
-                 seq_ids=None, threads=0):
+                 seq_ids=None, threads=0, spread=False):
     """fp64 decode output [len(seq_ids), Hq, D].
 
     q: uint16 [N, Hq, D]; pools uint16 [num_blocks, B, H_kv, D];
     block_tables int32 [N, stride]; seq_lens int32 [N].  Query head hq reads KV
-    head hq // (Hq // H_kv).
+    head hq // (Hq // H_kv).  With spread=True returns (out, spread), spread
+    as in attention_1q, per output element.
     """
     q = _u16(q)
     k_cache = _u16(k_cache)
@@ -266,18 +276,19 @@ def paged_decode(q, k_cache, v_cache, dtype, block_tables, seq_lens, scale,
     sl = _i32(seq_lens)
     ids = _i32(np.arange(N) if seq_ids is None else seq_ids)
     out = np.empty((ids.size, Hq, D), dtype=np.float64)
+    sp = np.empty_like(out) if spread else None
     rc = lib().or_paged_decode(_p(q, ctypes.c_uint16), _p(k_cache, ctypes.c_uint16),
                                _p(v_cache, ctypes.c_uint16), int(dtype), _p(bt, ctypes.c_int32),
                                bt.shape[1], _p(sl, ctypes.c_int32), _p(ids, ctypes.c_int32),
                                ids.size, Hq, H_kv, D, B, float(scale),
-                               _p(out, ctypes.c_double), int(threads))
+                               _p(out, ctypes.c_double), _opt(sp), int(threads))
     if rc != 0:
         raise MemoryError("oracle decode could not allocate its gather buffers")
-    return out
+    return (out, sp) if spread else out
 
 
 def paged_decode_window(q, k_cache, v_cache, dtype, block_tables, seq_lens, window, scale,
-                        seq_ids=None, threads=0):
+                        seq_ids=None, threads=0, spread=False):
     """Sliding-window decode [P1 "How does it support prompts of arbitrary
     length? Does it have a sliding window?"]: the query of position T - 1
     attends to tokens [max(0, T - window), T); table entries before the window
@@ -292,18 +303,20 @@ def paged_decode_window(q, k_cache, v_cache, dtype, block_tables, seq_lens, wind
     sl = _i32(seq_lens)
     ids = _i32(np.arange(N) if seq_ids is None else seq_ids)
     out = np.empty((ids.size, Hq, D), dtype=np.float64)
+    sp = np.empty_like(out) if spread else None
     rc = lib().or_paged_decode_window(_p(q, ctypes.c_uint16), _p(k_cache, ctypes.c_uint16),
                                       _p(v_cache, ctypes.c_uint16), int(dtype),
                                       _p(bt, ctypes.c_int32), bt.shape[1], _p(sl, ctypes.c_int32),
                                       int(window), _p(ids, ctypes.c_int32), ids.size, Hq, H_kv, D,
-                                      B, float(scale), _p(out, ctypes.c_double), int(threads))
+                                      B, float(scale), _p(out, ctypes.c_double), _opt(sp),
+                                      int(threads))
     if rc != 0:
         raise MemoryError("oracle decode could not allocate its gather buffers")
-    return out
+    return (out, sp) if spread else out
 
 
 def paged_prefill(q, k_cache, v_cache, dtype, block_tables, seq_lens, query_start, scale,
-                  threads=0):
+                  threads=0, spread=False):
     """Multi-query paged attention (chunked prefill; decode is L_i = 1):
     fp64 out [total_q, Hq, D].  Sequence i's new tokens are q rows
     [query_start[i], query_start[i+1]), sitting at the end of its seq_lens[i]
@@ -319,14 +332,15 @@ def paged_prefill(q, k_cache, v_cache, dtype, block_tables, seq_lens, query_star
     qs = _i32(query_start)
     assert qs.size == sl.size + 1 and qs[-1] == total
     out = np.zeros((total, Hq, D), dtype=np.float64)
+    sp = np.zeros_like(out) if spread else None
     rc = lib().or_paged_prefill(_p(q, ctypes.c_uint16), _p(k_cache, ctypes.c_uint16),
                                 _p(v_cache, ctypes.c_uint16), int(dtype), _p(bt, ctypes.c_int32),
                                 bt.shape[1], _p(sl, ctypes.c_int32), _p(qs, ctypes.c_int32),
                                 sl.size, Hq, H_kv, D, B, float(scale), _p(out, ctypes.c_double),
-                                int(threads))
+                                _opt(sp), int(threads))
     if rc != 0:
         raise MemoryError("oracle prefill could not allocate its gather buffers")
-    return out
+    return (out, sp) if spread else out
 
 
 def contiguous_decode(q, K, V, scale):
@@ -401,8 +415,9 @@ def gather_head_fp8(cache, scale, table_row, T, h):
 
 
 def paged_decode_fp8(q, k_cache, v_cache, q_dtype, k_scale, v_scale, block_tables, seq_lens,
-                     scale, seq_ids=None, threads=0):
-    """fp64 decode output [len(seq_ids), Hq, D] over E4M3 pools (uint8)."""
+                     scale, seq_ids=None, threads=0, spread=False):
+    """fp64 decode output [len(seq_ids), Hq, D] over E4M3 pools (uint8);
+    with spread=True returns (out, spread) as paged_decode does."""
     q = _u16(q)
     k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
     v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
@@ -413,15 +428,17 @@ def paged_decode_fp8(q, k_cache, v_cache, q_dtype, k_scale, v_scale, block_table
     sl = _i32(seq_lens)
     ids = _i32(np.arange(N) if seq_ids is None else seq_ids)
     out = np.empty((ids.size, Hq, D), dtype=np.float64)
+    sp = np.empty_like(out) if spread else None
     rc = lib().or_paged_decode_fp8(_p(q, ctypes.c_uint16), _p(k_cache, ctypes.c_uint8),
                                    _p(v_cache, ctypes.c_uint8), int(q_dtype),
                                    float(np.float32(k_scale)), float(np.float32(v_scale)),
                                    _p(bt, ctypes.c_int32), bt.shape[1], _p(sl, ctypes.c_int32),
                                    _p(ids, ctypes.c_int32), ids.size, Hq, H_kv, D, B,
-                                   float(scale), _p(out, ctypes.c_double), int(threads))
+                                   float(scale), _p(out, ctypes.c_double), _opt(sp),
+                                   int(threads))
     if rc != 0:
         raise MemoryError("oracle decode could not allocate its gather buffers")
-    return out
+    return (out, sp) if spread else out
 
 
 # --------------------------------------------------------------------------

@@ -191,10 +191,19 @@ void or_gather_bits(const uint16_t* cache, const int32_t* table_row, int64_t T,
  *   s_t = scale * sum_d q_d K_td;  w_t = exp(s_t - max s) / sum exp(s - max s)
  *   out_d = sum_t w_t V_td
  * scratch must hold T doubles.
+ *
+ * If spread is not NULL it receives, per output element, the weighted mean
+ * absolute deviation of the values about the output,
+ *   spread_d = sum_t w_t |V_td - out_d|.
+ * It is not part of the method: it is the scale of the error that perturbing
+ * every weight w_t by a relative amount of at most u can cause in out_d (the
+ * perturbed output is again a weighted mean, and moves by at most about
+ * u * spread_d), which the tests use to bound a kernel's rounding of the
+ * weights.
  * ------------------------------------------------------------------------- */
 void or_attention_1q(const double* q, const double* K, const double* V,
                      int64_t T, int32_t D, double scale, double* out,
-                     double* scratch) {
+                     double* scratch, double* spread) {
     double m = -INFINITY;
     for (int64_t t = 0; t < T; ++t) {
         double dot = 0.0;
@@ -212,6 +221,13 @@ void or_attention_1q(const double* q, const double* K, const double* V,
         for (int64_t t = 0; t < T; ++t) acc += scratch[t] * V[t * D + d];
         out[d] = acc / z;
     }
+    if (spread) {
+        for (int32_t d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; ++t) acc += scratch[t] * fabs(V[t * D + d] - out[d]);
+            spread[d] = acc / z;
+        }
+    }
 }
 
 /* ---------------------------------------------------------------------------
@@ -220,6 +236,8 @@ void or_attention_1q(const double* q, const double* K, const double* V,
  *   pools    [num_blocks][B][H_kv][D]    (16-bit, dtype)
  *   block_tables [num_seqs][table_stride] int32, seq_lens[num_seqs] int32
  *   seq_ids  the n_ids sequences to evaluate; out[n_ids][Hq][D] fp64.
+ *   spread   NULL, or [n_ids][Hq][D] fp64: each element's weighted mean
+ *            absolute deviation (or_attention_1q); zero for a zero-length row.
  * Query head hq reads KV head floor(hq / G), G = Hq / H_kv (contiguous query
  * groups: our reading of grouped-query attention, which the pages name in
  * "How big the KV cache is: a formula and a real measurement" without giving
@@ -230,7 +248,7 @@ int or_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* 
                     int dtype, const int32_t* block_tables, int64_t table_stride,
                     const int32_t* seq_lens, const int32_t* seq_ids, int32_t n_ids,
                     int32_t Hq, int32_t H_kv, int32_t D, int32_t B, double scale,
-                    double* out, int threads) {
+                    double* out, double* spread, int threads) {
     int32_t G = Hq / H_kv;
     int64_t n_work = (int64_t)n_ids * H_kv;
     int failed = 0;
@@ -246,7 +264,10 @@ int or_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* 
         double* o = out + (int64_t)idx * Hq * D;
         if (T <= 0) {
             for (int32_t g = 0; g < G; ++g)
-                for (int32_t d = 0; d < D; ++d) o[(int64_t)(h * G + g) * D + d] = 0.0;
+                for (int32_t d = 0; d < D; ++d) {
+                    o[(int64_t)(h * G + g) * D + d] = 0.0;
+                    if (spread) spread[((int64_t)idx * Hq + h * G + g) * D + d] = 0.0;
+                }
             continue;
         }
         const int32_t* row = block_tables + (int64_t)i * table_stride;
@@ -266,7 +287,8 @@ int or_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* 
                 int32_t hq = h * G + g;
                 const uint16_t* qrow = q + ((int64_t)i * Hq + hq) * D;
                 for (int32_t d = 0; d < D; ++d) qv[d] = or_decode(qrow[d], dtype);
-                or_attention_1q(qv, K, V, T, D, scale, o + (int64_t)hq * D, s);
+                or_attention_1q(qv, K, V, T, D, scale, o + (int64_t)hq * D, s,
+                                spread ? spread + ((int64_t)idx * Hq + hq) * D : NULL);
             }
         }
         free(K);
@@ -292,7 +314,7 @@ int or_paged_decode_window(const uint16_t* q, const uint16_t* k_cache, const uin
                            int dtype, const int32_t* block_tables, int64_t table_stride,
                            const int32_t* seq_lens, int32_t window, const int32_t* seq_ids,
                            int32_t n_ids, int32_t Hq, int32_t H_kv, int32_t D, int32_t B,
-                           double scale, double* out, int threads) {
+                           double scale, double* out, double* spread, int threads) {
     int32_t G = Hq / H_kv;
     int64_t n_work = (int64_t)n_ids * H_kv;
     int failed = 0;
@@ -308,7 +330,10 @@ int or_paged_decode_window(const uint16_t* q, const uint16_t* k_cache, const uin
         double* o = out + (int64_t)idx * Hq * D;
         if (T <= 0) {
             for (int32_t g = 0; g < G; ++g)
-                for (int32_t d = 0; d < D; ++d) o[(int64_t)(h * G + g) * D + d] = 0.0;
+                for (int32_t d = 0; d < D; ++d) {
+                    o[(int64_t)(h * G + g) * D + d] = 0.0;
+                    if (spread) spread[((int64_t)idx * Hq + h * G + g) * D + d] = 0.0;
+                }
             continue;
         }
         int64_t s0 = (window > 0 && T > window) ? T - window : 0;
@@ -337,7 +362,8 @@ int or_paged_decode_window(const uint16_t* q, const uint16_t* k_cache, const uin
                 int32_t hq = h * G + g;
                 const uint16_t* qrow = q + ((int64_t)i * Hq + hq) * D;
                 for (int32_t d = 0; d < D; ++d) qv[d] = or_decode(qrow[d], dtype);
-                or_attention_1q(qv, K, V, n, D, scale, o + (int64_t)hq * D, s);
+                or_attention_1q(qv, K, V, n, D, scale, o + (int64_t)hq * D, s,
+                                spread ? spread + ((int64_t)idx * Hq + hq) * D : NULL);
             }
         }
         free(K);
@@ -365,7 +391,7 @@ int or_paged_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t*
                      int dtype, const int32_t* block_tables, int64_t table_stride,
                      const int32_t* seq_lens, const int32_t* query_start, int32_t num_seqs,
                      int32_t Hq, int32_t H_kv, int32_t D, int32_t B, double scale,
-                     double* out, int threads) {
+                     double* out, double* spread, int threads) {
     int32_t G = Hq / H_kv;
     int64_t n_work = (int64_t)num_seqs * H_kv;
     int failed = 0;
@@ -398,7 +424,8 @@ int or_paged_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t*
                     int32_t hq = h * G + g;
                     const uint16_t* qrow = q + ((q0 + j) * Hq + hq) * D;
                     for (int32_t d = 0; d < D; ++d) qv[d] = or_decode(qrow[d], dtype);
-                    or_attention_1q(qv, K, V, p + 1, D, scale, out + ((q0 + j) * Hq + hq) * D, s);
+                    or_attention_1q(qv, K, V, p + 1, D, scale, out + ((q0 + j) * Hq + hq) * D, s,
+                                    spread ? spread + ((q0 + j) * Hq + hq) * D : NULL);
                 }
             }
         }
@@ -411,8 +438,10 @@ int or_paged_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t*
 }
 
 /* The same single-query attention over a contiguous (unpaged) cache
- * K[T][H_kv][D] (fp64), used to check that paging changes only the addressing
- * ("the attention kernel is the only part of the model that has to change"). */
+ * K[T][H_kv][D] (fp64), used to check that paging changes only the addressing:
+ * "vLLM Framework and Inference Engine Design", section "What is the essence
+ * of vLLM's PagedAttention?", has the attention computation as the one place
+ * that must learn about blocks, the rest of the model being untouched. */
 void or_contiguous_decode(const double* q /*[Hq][D]*/, const double* K, const double* V,
                           int64_t T, int32_t Hq, int32_t H_kv, int32_t D, double scale,
                           double* out /*[Hq][D]*/) {
@@ -428,7 +457,8 @@ void or_contiguous_decode(const double* q /*[Hq][D]*/, const double* K, const do
             }
         for (int32_t g = 0; g < G; ++g) {
             int32_t hq = h * G + g;
-            or_attention_1q(q + (int64_t)hq * D, Kh, Vh, T, D, scale, out + (int64_t)hq * D, s);
+            or_attention_1q(q + (int64_t)hq * D, Kh, Vh, T, D, scale, out + (int64_t)hq * D, s,
+                            NULL);
         }
     }
     free(Kh);
@@ -542,7 +572,7 @@ int or_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t
                         const int32_t* block_tables, int64_t table_stride,
                         const int32_t* seq_lens, const int32_t* seq_ids, int32_t n_ids,
                         int32_t Hq, int32_t H_kv, int32_t D, int32_t B, double scale,
-                        double* out, int threads) {
+                        double* out, double* spread, int threads) {
     int32_t G = Hq / H_kv;
     int64_t n_work = (int64_t)n_ids * H_kv;
     int failed = 0;
@@ -558,7 +588,10 @@ int or_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t
         double* o = out + (int64_t)idx * Hq * D;
         if (T <= 0) {
             for (int32_t g = 0; g < G; ++g)
-                for (int32_t d = 0; d < D; ++d) o[(int64_t)(h * G + g) * D + d] = 0.0;
+                for (int32_t d = 0; d < D; ++d) {
+                    o[(int64_t)(h * G + g) * D + d] = 0.0;
+                    if (spread) spread[((int64_t)idx * Hq + h * G + g) * D + d] = 0.0;
+                }
             continue;
         }
         const int32_t* row = block_tables + (int64_t)i * table_stride;
@@ -578,7 +611,8 @@ int or_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t
                 int32_t hq = h * G + g;
                 const uint16_t* qrow = q + ((int64_t)i * Hq + hq) * D;
                 for (int32_t d = 0; d < D; ++d) qv[d] = or_decode(qrow[d], q_dtype);
-                or_attention_1q(qv, K, V, T, D, scale, o + (int64_t)hq * D, s);
+                or_attention_1q(qv, K, V, T, D, scale, o + (int64_t)hq * D, s,
+                                spread ? spread + ((int64_t)idx * Hq + hq) * D : NULL);
             }
         }
         free(K);

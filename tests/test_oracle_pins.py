@@ -202,6 +202,64 @@ def test_attention_invariances():
     np.testing.assert_allclose(oracle.attention_1q(2 * q, K, V, 0.15), base, atol=1e-13)
 
 
+def test_attention_spread_closed_forms():
+    # spread_d = sum_t w_t |V_td - out_d| (the scale of the output error that
+    # relative errors in the weights can cause; the GPU tests bound a kernel's
+    # rounding of the weights by it)
+    rng = np.random.default_rng(15)
+    D = 16
+    K = rng.standard_normal((9, D))
+    V = rng.standard_normal((9, D))
+    q = rng.standard_normal(D)
+    # one token: the output is that row, with no deviation
+    _, sp = oracle.attention_1q(q, K[:1], V[:1], 0.25, spread=True)
+    assert np.array_equal(sp, np.zeros(D))
+    # two tokens with equal weights (zero query): half their distance
+    out, sp = oracle.attention_1q(np.zeros(D), K[:2], V[:2], 0.25, spread=True)
+    np.testing.assert_allclose(sp, np.abs(V[0] - V[1]) / 2, rtol=1e-15, atol=0)
+    # three equal weights on values 0, 1, 5: mean 2, deviations 2, 1, 3 -> 2
+    V3 = np.array([[0.0], [1.0], [5.0]])
+    out, sp = oracle.attention_1q(np.zeros(1), np.zeros((3, 1)), V3, 1.0, spread=True)
+    assert out[0] == 2.0 and abs(sp[0] - 2.0) < 1e-15
+    # weights 1/4, 3/4 (scores 0 and ln 3) on values 0 and 4: out 3, spread
+    # 1/4 * 3 + 3/4 * 1 = 3/2
+    K2 = np.array([[0.0], [math.log(3.0)]])
+    out, sp = oracle.attention_1q(np.ones(1), K2, np.array([[0.0], [4.0]]), 1.0, spread=True)
+    assert abs(out[0] - 3.0) < 1e-14 and abs(sp[0] - 1.5) < 1e-14
+    # equal value rows: no deviation
+    _, sp = oracle.attention_1q(q, K, np.tile(V[:1], (9, 1)), 0.25, spread=True)
+    assert np.all(sp < 1e-15)
+
+
+def test_attention_spread_invariances_and_perturbation_bound():
+    rng = np.random.default_rng(16)
+    T, D = 50, 24
+    q = rng.standard_normal(D)
+    K = rng.standard_normal((T, D))
+    V = rng.standard_normal((T, D))
+    out, sp = oracle.attention_1q(q, K, V, 0.4, spread=True)
+    # a shift of every value row leaves it unchanged; a factor a scales it by |a|
+    c = rng.standard_normal(D)
+    np.testing.assert_allclose(oracle.attention_1q(q, K, V + c, 0.4, spread=True)[1], sp,
+                               rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(oracle.attention_1q(q, K, -3.0 * V, 0.4, spread=True)[1],
+                               3.0 * sp, rtol=1e-12, atol=1e-13)
+    # the property the GPU tests rely on: weights perturbed by relative
+    # errors of at most u give a weighted mean within u * spread / (1 - u) of
+    # the output; the worst signs (those of V - out) come close to it
+    s = 0.4 * (K @ q)
+    w = np.exp(s - s.max())
+    w /= w.sum()
+    u = 2.0 ** -8
+    for trial in range(20):
+        eps = rng.uniform(-u, u, (T, D)) if trial else u * np.sign(V - out)
+        wp = w[:, None] * (1 + eps)
+        moved = np.abs((wp * V).sum(0) / wp.sum(0) - out)
+        assert np.all(moved <= u * sp / (1 - u) + 1e-15)
+        if trial == 0:
+            assert np.all(moved >= 0.99 * u * sp / (1 + u))
+
+
 # --------------------------------------------------------- paged decode
 
 def _bf16_bits(x):
