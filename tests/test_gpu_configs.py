@@ -1,12 +1,13 @@
 """The five workloads end to end on the GPU (copy-on-write, slot mapping,
-cache write, decode) against the oracle; at full size, in the launch
-configuration the benchmark times."""
+cache write, decode) against the oracle, at full size, each as separate
+eager calls (the benchmark's own graph-captured step is checked in
+test_gpu_bench_step.py)."""
 import numpy as np
 import pytest
 
 import paged_kv_cache_72_gb300 as pa
 import workloads as W
-from harness import GpuState, OracleState, assert_close, bits_of, gpu_out_f64, gpu_step
+from harness import GpuState, OracleState, bits_of, check_parity, gpu_step
 
 pytestmark = pytest.mark.gpu
 
@@ -18,12 +19,9 @@ def _run(wl, seq_ids=None):
     ref = OracleState(wl)
     ref.step()
     assert np.array_equal(slots.cpu().numpy(), ref.slots)
-    expected = ref.decode(seq_ids=seq_ids)
-    got = gpu_out_f64(out)
-    if seq_ids is not None:
-        got = got[seq_ids]
-    err = assert_close(got, expected, wl.name)
-    return st, ref, err
+    expected, spread = ref.decode(seq_ids=seq_ids, spread=True)
+    rep = check_parity(out, wl, expected, spread, wl.name, rows=seq_ids)
+    return st, ref, rep["max_abs"]
 
 
 def test_tiny():

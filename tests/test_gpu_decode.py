@@ -11,8 +11,8 @@ import torch
 import oracle
 import paged_kv_cache_72_gb300 as pa
 import workloads as W
-from harness import (GpuState, OracleState, assert_close, bits_of, gpu_out_f64, gpu_step,
-                     to_dev)
+from harness import (GpuState, OracleState, assert_close, bits_of, check_parity, gpu_out_f64,
+                     gpu_step, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,10 +24,11 @@ def _parity(wl, flags=pa.PA_DECODE_AUTO, num_ctas=0):
     out, _ = gpu_step(st, flags=flags, num_ctas=num_ctas)
     ref = OracleState(wl)
     ref.step()
-    expected = ref.decode()
-    err = assert_close(gpu_out_f64(out), expected, "%s flags=%d ctas=%d" % (wl.name, flags, num_ctas))
+    expected, spread = ref.decode(spread=True)
+    rep = check_parity(out, wl, expected, spread,
+                       "%s flags=%d ctas=%d" % (wl.name, flags, num_ctas), flags=flags)
     assert pa.pa_get_error(st.err) == 0
-    return out, err
+    return out, rep["max_abs"]
 
 
 def test_tiny_config(cuda_device):

@@ -13,7 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_72_gb300 as pa
 import workloads as W
-from harness import GpuState, OracleState, assert_close, gpu_out_f64, gpu_step
+from harness import GpuState, OracleState, assert_close, check_parity, gpu_out_f64, gpu_step
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +26,8 @@ def _parity(wl):
     out, _ = gpu_step(st)
     ref = OracleState(wl)
     ref.step()
-    err = assert_close(gpu_out_f64(out), ref.decode(), wl.name)
+    expected, spread = ref.decode(spread=True)
+    check_parity(out, wl, expected, spread, wl.name)
     assert pa.pa_get_error(st.err) == 0
     return st, out
 
@@ -105,10 +106,10 @@ def test_llama3_chunked_prefill_sampled(cuda_device):
     order = np.argsort(wl.seq_lens)
     for i in (int(order[0]), int(order[-1])):
         q0, q1 = wl.query_start[i], wl.query_start[i + 1]
-        sub = oracle.paged_prefill(wl.q[q0:q1], ref.k_cache, ref.v_cache, wl.dtype,
-                                   wl.block_tables[i:i + 1], wl.seq_lens[i:i + 1],
-                                   np.array([0, q1 - q0], np.int32), wl.scale)
-        assert_close(gpu_out_f64(out[q0:q1]), sub, "llama3 chunked prefill seq %d" % i)
+        sub, sp = oracle.paged_prefill(wl.q[q0:q1], ref.k_cache, ref.v_cache, wl.dtype,
+                                       wl.block_tables[i:i + 1], wl.seq_lens[i:i + 1],
+                                       np.array([0, q1 - q0], np.int32), wl.scale, spread=True)
+        check_parity(out[q0:q1], wl, sub, sp, "llama3 chunked prefill seq %d" % i)
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -117,10 +118,12 @@ def test_prefill_wide_score_range(cuda_device, D):
     running maximum moves past the kernel's reference many times and its rows
     of O are rescaled in tensor memory.
 
-    The tolerance adds what the 16-bit P costs on such peaked rows.  With P_i
-    rounded to p_i (1 + d_i), |d_i| <= 2^-9, the output moves by
-    sum_i p_i d_i (v_i - out) / sum_i p_i, at most 2^-9 * 2 max|v|, and its own
-    rounding adds 2^-9 |out| <= 2^-9 max|v|: 3 * 2^-9 * max|v| in all."""
+    On such peaked rows the 16-bit P costs more than the plain decode
+    tolerance allows.  With P_i rounded to p_i (1 + d_i), |d_i| <= 2^-8
+    (bfloat16), the output moves by sum_i p_i d_i (v_i - out) / sum_i p_i, at
+    most 2^-8 * 2 max|v|, and its own rounding adds at most 2^-8 |out|: the
+    coarse bound below.  The rounding bound (the same terms per element, with
+    the oracle's weighted deviation in place of 2 max|v|) must hold too."""
     wl = W.random_prefill(150 + D, W.BF16, 16, 4, D, 16, [0, 500, 2000, 63], [300, 129, 64, 70],
                           garbage="nan", q_sigma=4.0, kv_sigma=4.0)
     st = GpuState(wl)
@@ -134,8 +137,10 @@ def test_prefill_wide_score_range(cuda_device, D):
     vmax = max(float(np.abs(oracle.gather_head(ref.v_cache, wl.dtype, wl.block_tables[i],
                                                    int(wl.seq_lens[i]), h)).max())
                for i in range(len(wl.seq_lens)) for h in range(wl.num_kv_heads))
-    bound = 4e-3 + 1e-2 * np.abs(expected) + 3 * 2.0 ** -9 * vmax
+    bound = 4e-3 + 1e-2 * np.abs(expected) + 3 * 2.0 ** -8 * vmax
     assert np.all(np.abs(got - expected) <= bound), float(np.abs(got - expected).max())
+    _, spread = ref.decode(spread=True)
+    check_parity(out, wl, expected, spread, "wide score range D=%d" % D, allclose=False)
 
 
 def test_prefill_sequences_ending_on_stage_edges(cuda_device):

@@ -15,7 +15,7 @@ import torch
 import oracle
 import paged_kv_cache_72_gb300 as pa
 import workloads as W
-from harness import GpuState, OracleState, assert_close, gpu_out_f64, gpu_step
+from harness import GpuState, OracleState, assert_close, check_parity, gpu_out_f64, gpu_step
 
 pytestmark = pytest.mark.gpu
 
@@ -27,10 +27,11 @@ def _parity(wl, flags=pa.PA_DECODE_AUTO, num_ctas=0):
     out, _ = gpu_step(st, flags=flags, num_ctas=num_ctas)
     ref = OracleState(wl)
     ref.step()
-    err = assert_close(gpu_out_f64(out), ref.decode(),
-                       "window %d flags=%d ctas=%d" % (wl.window, flags, num_ctas))
+    expected, spread = ref.decode(spread=True)
+    rep = check_parity(out, wl, expected, spread,
+                       "window %d flags=%d ctas=%d" % (wl.window, flags, num_ctas), flags=flags)
     assert pa.pa_get_error(st.err) == 0
-    return err
+    return rep["max_abs"]
 
 
 @pytest.mark.parametrize("window", [1, 7, 16, 17, 100, 128, 129, 1000, 5000])
