@@ -350,12 +350,16 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
  * are those of pa_decode.  The workspace is a fixed array of
  * PA_NOALLOC_SCRATCH_BYTES in the library's own device memory, held by every
  * GPU that loads the library until the process exits; this call allocates
- * nothing.  The first call on a device looks the array's device address up
- * (cudaGetSymbolAddress) with that device current, so make that first call
- * before any stream capture.  A shape whose workspace
- * (pa_decode_workspace_size) exceeds the array returns PA_ERR_WORKSPACE.  All
- * calls share the one array: calls that overlap on the GPU (for instance on two
- * streams) race and must be serialized by the caller.
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).  The
+ * first call on a device (and the first after that device's context was reset)
+ * looks the array's device address up (cudaGetSymbolAddress) with that device
+ * current, so make that first call before any stream capture.  Every call
+ * first clears the array's split-context counters on `stream` (one
+ * cudaMemsetAsync of 64 KiB), so nothing a previous call left in the array,
+ * including one that gave up with PA_DEVERR_TIMEOUT, reaches the next.  A
+ * shape whose workspace (pa_decode_workspace_size) exceeds the array returns
+ * PA_ERR_WORKSPACE.  All calls share the one array: calls that overlap on the
+ * GPU (for instance on two streams) race and must be serialized by the caller.
  */
 #define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
