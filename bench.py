@@ -38,6 +38,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 DATASHEET_HBM_GBS = 7900.0   # nominal GB300 HBM3e figure, for context only
 L2_FLUSH_BYTES = 512 << 20
+CLOCK_SOAK_S = 0.5   # untimed replays of the step under the clock sampler before timing
 KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_decode_fp8.cuh", "pa_device.cuh",
                   "pa_decode_variants.cuh", "pa_decode.cu"]
 PREFILL_SOURCES = ["pa_prefill.cu", "pa_device.cuh"]
@@ -131,7 +132,8 @@ def l2_flush(buf, k):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 20 ms, read-only queries) of SM clock and
+    throttle reasons, each stamped with the host time it arrived."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -146,7 +148,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -159,9 +161,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
-    def stop(self):
+    def stop(self, region=None):
+        """Summary of the samples; region = (t0, t1) host times of the timed
+        region, whose samples are counted separately."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -170,9 +174,9 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, mx, reasons = [], [], set()
+        sm, mx, reasons, in_region = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for t, line in self.lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 6:
                 continue
@@ -181,13 +185,20 @@ class ClockSampler:
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
+            if region and region[0] <= t <= region[1]:
+                in_region.append(sm[-1])
             for n, v in zip(names, parts[2:6]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "samples_in_timed_region": len(in_region),
+                "sm_mhz_in_timed_region": statistics.median(in_region) if in_region else None,
+                "reasons": sorted(reasons),
+                "window": "every 20 ms over an untimed soak of the same step (about %.1f s, "
+                          "graph replays with the L2 flush) running straight into the timed "
+                          "region, and the timed region itself" % CLOCK_SOAK_S}
 
 
 # --------------------------------------------------------------------------
@@ -323,8 +334,20 @@ def run_gpu(args, rank, world, local_rank):
 
     clocks = ClockSampler(local_rank)
     clocks.start()
+    # keep the GPU under the step's load while the sampler collects samples
+    # (a timed region of a few steps lasts milliseconds, shorter than the
+    # sampling period)
+    t_soak = time.perf_counter()
+    k = 0
+    while time.perf_counter() - t_soak < CLOCK_SOAK_S:
+        l2_flush(flush, k)
+        st.g_step.replay()
+        k += 1
+        if k % 64 == 0:
+            torch.cuda.synchronize()
     _barrier(world)
     torch.cuda.synchronize()
+    t_region0 = time.perf_counter()
     # timed region: K steps (one graph each), then K decode phases alone for
     # the decode kernels' own duration; L2 flushed before each, untimed
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -339,8 +362,9 @@ def run_gpu(args, rank, world, local_rank):
         st.g_decode.replay()
         ev[k][3].record()
     torch.cuda.synchronize()
+    t_region1 = time.perf_counter()
     _barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop(region=(t_region0, t_region1))
     flags = pa.pa_get_error(st.err)
     if flags:
         raise RuntimeError("kernel reported error bits 0x%x" % flags)
