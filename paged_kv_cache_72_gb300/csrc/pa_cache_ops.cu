@@ -226,68 +226,170 @@ __global__ void cache_write_fp8_mapped_kernel(
   }
 }
 
-// One block per (pair, K or V).  A pair is copied only if it is in range, its
-// dst appears once among the dsts and is no pair's src.
-__global__ void copy_blocks_kernel(const int32_t* __restrict__ pairs, int num_pairs,
-                                   long long num_blocks, int vecs_per_block,
-                                   uint4* __restrict__ kc, uint4* __restrict__ vc, int32_t* err) {
+// Pair validation for the block copy and the block swap, in time linear in
+// the number of pairs.  Each thread block owns a contiguous range of at most
+// kPairsPerCta pairs.  It puts its own pairs' dst blocks in a hash table in
+// shared memory (key and local index in one 64-bit word, open addressing),
+// then reads every pair of the list once and looks its src and its dst up:
+//   * a dst that is some pair's src (block copy only: both sides address the
+//     same pool) makes the owning pair invalid;
+//   * a dst that is another pair's dst makes both invalid;
+//   * a src or dst outside its pool makes the pair invalid.
+// The grid is bounded by a small multiple of the SM count, so the whole check
+// reads the list once per thread block: O(num_pairs) per block, with no
+// device memory beyond the inputs.
+constexpr int kPairsPerCta = 512;
+constexpr int kPairHash = 1024;              // table slots (power of two, twice the pairs)
+constexpr unsigned long long kHashEmpty = ~0ull;
+
+__device__ __forceinline__ unsigned pair_hash(int key) {
+  return ((unsigned)key * 2654435761u) >> (32 - 10);   // kPairHash = 2^10
+}
+
+// Marks bad[i] for the invalid pairs among the m pairs from p0; the caller
+// syncs after.  table: kPairHash words of shared memory.
+__device__ __forceinline__ void validate_pairs(const int32_t* __restrict__ pairs, int num_pairs,
+                                               int p0, int m, long long src_blocks,
+                                               long long dst_blocks, bool dst_may_be_src,
+                                               unsigned long long* table, unsigned char* bad) {
+  for (int i = threadIdx.x; i < kPairHash; i += blockDim.x) table[i] = kHashEmpty;
+  for (int i = threadIdx.x; i < m; i += blockDim.x) bad[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const int src = pairs[2 * (p0 + i)], dst = pairs[2 * (p0 + i) + 1];
+    if (src < 0 || (long long)src >= src_blocks || dst < 0 || (long long)dst >= dst_blocks) {
+      bad[i] = 1;
+      continue;
+    }
+    const unsigned long long word = ((unsigned long long)(unsigned)dst << 32) | (unsigned)i;
+    for (unsigned h = pair_hash(dst);; h = (h + 1) & (kPairHash - 1)) {
+      const unsigned long long prev = atomicCAS(&table[h], kHashEmpty, word);
+      if (prev == kHashEmpty) break;
+      if ((int)(prev >> 32) == dst) {   // two own pairs share a dst
+        bad[i] = 1;
+        bad[(unsigned)prev] = 1;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  auto find = [&](int key) -> int {   // local index of the own pair with dst == key, or -1
+    for (unsigned h = pair_hash(key);; h = (h + 1) & (kPairHash - 1)) {
+      const unsigned long long w = table[h];
+      if (w == kHashEmpty) return -1;
+      if ((int)(w >> 32) == key) return (int)(unsigned)w;
+    }
+  };
+  for (int j = threadIdx.x; j < num_pairs; j += blockDim.x) {
+    const int sj = pairs[2 * j], dj = pairs[2 * j + 1];
+    if (dst_may_be_src) {
+      const int a = find(sj);   // an own dst that is pair j's src
+      if (a >= 0) bad[a] = 1;
+    }
+    const int b = find(dj);     // an own dst that is pair j's dst too
+    if (b >= 0 && p0 + b != j) bad[b] = 1;
+  }
+}
+
+// Copies the valid pairs among the m pairs from p0, K and V blocks, in 16-byte
+// vectors, four loads in flight per thread.
+__device__ __forceinline__ void copy_valid_pairs(const int32_t* __restrict__ pairs, int p0, int m,
+                                                 int vecs_per_block, const unsigned char* bad,
+                                                 const uint4* src_k, const uint4* src_v,
+                                                 uint4* dst_k, uint4* dst_v) {
+  for (int i = 0; i < m; ++i) {
+    if (bad[i]) continue;
+    const long long src = pairs[2 * (p0 + i)], dst = pairs[2 * (p0 + i) + 1];
+    const uint4* sk = src_k + src * vecs_per_block;
+    const uint4* sv = src_v + src * vecs_per_block;
+    uint4* dk = dst_k + dst * vecs_per_block;
+    uint4* dv = dst_v + dst * vecs_per_block;
+    const int n = 2 * vecs_per_block;
+    int e = threadIdx.x;
+    for (; e + 3 * (int)blockDim.x < n; e += 4 * blockDim.x) {
+      uint4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int f = e + u * blockDim.x;
+        x[u] = f < vecs_per_block ? sk[f] : sv[f - vecs_per_block];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int f = e + u * blockDim.x;
+        if (f < vecs_per_block) dk[f] = x[u];
+        else dv[f - vecs_per_block] = x[u];
+      }
+    }
+    for (; e < n; e += blockDim.x) {
+      if (e < vecs_per_block) dk[e] = sk[e];
+      else dv[e - vecs_per_block] = sv[e - vecs_per_block];
+    }
+  }
+}
+
+// Copy-on-write block copy: thread block b owns pairs [b * per_cta, ...).  A
+// pair is copied only if it is in range, its dst appears once among the dsts
+// and is no pair's src.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restrict__ pairs,
+                                                          int num_pairs, int per_cta,
+                                                          long long num_blocks, int vecs_per_block,
+                                                          uint4* kc, uint4* vc, int32_t* err) {
   grid_dep_wait();
   grid_dep_launch();
-  const int p = blockIdx.x;
-  const int which = blockIdx.y;  // 0 = K, 1 = V
-  const int src = pairs[2 * p], dst = pairs[2 * p + 1];
-  __shared__ int bad;
-  if (threadIdx.x == 0) bad = 0;
+  __shared__ unsigned long long table[kPairHash];
+  __shared__ unsigned char bad[kPairsPerCta];
+  __shared__ int any_bad;
+  const int p0 = blockIdx.x * per_cta;
+  const int m = min(per_cta, num_pairs - p0);
+  if (m <= 0) return;
+  validate_pairs(pairs, num_pairs, p0, m, num_blocks, num_blocks, true, table, bad);
+  if (threadIdx.x == 0) any_bad = 0;
   __syncthreads();
-  int mine = (src < 0 || (long long)src >= num_blocks || dst < 0 || (long long)dst >= num_blocks);
-  for (int j = threadIdx.x; j < num_pairs && !mine; j += blockDim.x) {
-    const int sj = pairs[2 * j], dj = pairs[2 * j + 1];
-    if (sj == dst || (j != p && dj == dst)) mine = 1;
-  }
-  if (mine) atomicOr(&bad, 1);
+  for (int i = threadIdx.x; i < m; i += blockDim.x)
+    if (bad[i]) any_bad = 1;
   __syncthreads();
-  if (bad) {
-    if (threadIdx.x == 0 && which == 0) set_error(err, PA_DEVERR_COPY_PAIR);
-    return;
-  }
-  uint4* base = which ? vc : kc;
-  const uint4* s = base + (long long)src * vecs_per_block;
-  uint4* d = base + (long long)dst * vecs_per_block;
-  for (int e = threadIdx.x; e < vecs_per_block; e += blockDim.x) d[e] = s[e];
+  if (threadIdx.x == 0 && any_bad) set_error(err, PA_DEVERR_COPY_PAIR);
+  copy_valid_pairs(pairs, p0, m, vecs_per_block, bad, kc, vc, kc, vc);
 }
 
 // Block swap between the device pool and a pinned host pool ("vLLM anatomy",
 // section "Memory Pressure and Preemption": swapping moves physical blocks from
-// GPU memory to the CPU's memory and back).  One CTA per (pair, K or V) copies
-// a block in 16-byte vectors; the host pool is addressed through its mapped
-// device address, so any number of blocks moves in one launch (over
-// NVLink-C2C on a Grace-Blackwell node).  A pair is copied only if both
-// blocks are in range and its dst appears once among the dsts.
-__global__ void swap_blocks_kernel(const int32_t* __restrict__ pairs, int num_pairs,
-                                   long long src_blocks, long long dst_blocks, int vecs_per_block,
-                                   const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
-                                   uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
-                                   int32_t* err) {
+// GPU memory to the CPU's memory and back).  Thread block b owns pairs
+// [b * per_cta, ...) and copies them in 16-byte vectors; the host pool is
+// addressed through its mapped device address, so any number of blocks moves
+// in one launch (over NVLink-C2C on a Grace-Blackwell node).  A pair is copied
+// only if both blocks are in range and its dst appears once among the dsts.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(
+    const int32_t* __restrict__ pairs, int num_pairs, int per_cta, long long src_blocks,
+    long long dst_blocks, int vecs_per_block, const uint4* __restrict__ src_k,
+    const uint4* __restrict__ src_v, uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+    int32_t* err) {
   grid_dep_wait();
   grid_dep_launch();
-  const int p = blockIdx.x;
-  const int which = blockIdx.y;  // 0 = K, 1 = V
-  const int src = pairs[2 * p], dst = pairs[2 * p + 1];
-  __shared__ int bad;
-  if (threadIdx.x == 0) bad = 0;
+  __shared__ unsigned long long table[kPairHash];
+  __shared__ unsigned char bad[kPairsPerCta];
+  __shared__ int any_bad;
+  const int p0 = blockIdx.x * per_cta;
+  const int m = min(per_cta, num_pairs - p0);
+  if (m <= 0) return;
+  validate_pairs(pairs, num_pairs, p0, m, src_blocks, dst_blocks, false, table, bad);
+  if (threadIdx.x == 0) any_bad = 0;
   __syncthreads();
-  int mine = (src < 0 || (long long)src >= src_blocks || dst < 0 || (long long)dst >= dst_blocks);
-  for (int j = threadIdx.x; j < num_pairs && !mine; j += blockDim.x)
-    if (j != p && pairs[2 * j + 1] == dst) mine = 1;
-  if (mine) atomicOr(&bad, 1);
+  for (int i = threadIdx.x; i < m; i += blockDim.x)
+    if (bad[i]) any_bad = 1;
   __syncthreads();
-  if (bad) {
-    if (threadIdx.x == 0 && which == 0) set_error(err, PA_DEVERR_COPY_PAIR);
-    return;
-  }
-  const uint4* s = (which ? src_v : src_k) + (long long)src * vecs_per_block;
-  uint4* d = (which ? dst_v : dst_k) + (long long)dst * vecs_per_block;
-  for (int e = threadIdx.x; e < vecs_per_block; e += blockDim.x) d[e] = s[e];
+  if (threadIdx.x == 0 && any_bad) set_error(err, PA_DEVERR_COPY_PAIR);
+  copy_valid_pairs(pairs, p0, m, vecs_per_block, bad, src_k, src_v, dst_k, dst_v);
+}
+
+// Pairs per thread block for a list of n pairs: at most kPairsPerCta, and
+// enough blocks (two per SM) to keep the copies spread over the GPU.
+static int pairs_per_cta(int n, int sm_count) {
+  const int target_ctas = 2 * sm_count;
+  int per = (n + target_ctas - 1) / target_ctas;
+  if (per < 1) per = 1;
+  if (per > kPairsPerCta) per = kPairsPerCta;
+  return per;
 }
 
 static bool shape_ok(int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
@@ -389,11 +491,14 @@ int pa_copy_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, void* k_cach
   const int eb = dtype == PA_FP8_E4M3 ? 1 : 2;
   const long long vecs = (long long)block_size * num_kv_heads * head_dim * eb / 16;
   if (vecs > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-  dim3 grid((unsigned)num_pairs, 2);
+  DeviceInfo di;
+  if (int rc = current_device_info(&di)) return rc;
+  const int per = pairs_per_cta(num_pairs, di.sm_count);
+  const unsigned ctas = (unsigned)((num_pairs + per - 1) / per);
   clear_stale_error();
-  return launch_status(launch_pdl(copy_blocks_kernel, grid, dim3(256), 0,
+  return launch_status(launch_pdl(copy_blocks_kernel, dim3(ctas), dim3(256), 0,
                                   static_cast<cudaStream_t>(stream), src_dst_pairs,
-                                  (int)num_pairs, (long long)num_blocks, (int)vecs,
+                                  (int)num_pairs, per, (long long)num_blocks, (int)vecs,
                                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                   err_word),
                        "block copy launch");
@@ -424,10 +529,14 @@ int pa_swap_blocks(const int32_t* src_dst_pairs, int32_t num_pairs, int32_t dire
   const long long vecs = (long long)block_size * num_kv_heads * head_dim * eb / 16;
   if (vecs > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   const bool out = direction == PA_SWAP_OUT;
+  DeviceInfo di;
+  if (int rc = current_device_info(&di)) return rc;
+  const int per = pairs_per_cta(num_pairs, di.sm_count);
+  const unsigned ctas = (unsigned)((num_pairs + per - 1) / per);
   clear_stale_error();
   const cudaError_t e = launch_pdl(
-      swap_blocks_kernel, dim3((unsigned)num_pairs, 2), dim3(256), 0,
-      static_cast<cudaStream_t>(stream), src_dst_pairs, (int)num_pairs,
+      swap_blocks_kernel, dim3(ctas), dim3(256), 0,
+      static_cast<cudaStream_t>(stream), src_dst_pairs, (int)num_pairs, per,
       (long long)(out ? dev_num_blocks : host_num_blocks),
       (long long)(out ? host_num_blocks : dev_num_blocks), (int)vecs,
       static_cast<const uint4*>(out ? dev_k : hk), static_cast<const uint4*>(out ? dev_v : hv),

@@ -162,3 +162,65 @@ def test_slot_mapped_cache_write_flags_bad_tokens(cuda_device):
     kc2, vc2 = torch.zeros_like(kc), torch.zeros_like(vc)
     pa.pa_cache_write_mapped(k, v, bt, seq, pos, kc2, vc2)
     assert torch.equal(kc2, kc) and torch.equal(vc2, vc)
+
+
+def _valid_pairs(pairs, nb):
+    """The pairs the block copy must apply: in range, dst unique among the
+    dsts and no pair's src (the rules stated for pa_copy_blocks)."""
+    src, dst = pairs[:, 0], pairs[:, 1]
+    ok = (src >= 0) & (src < nb) & (dst >= 0) & (dst < nb)
+    uniq, counts = np.unique(dst, return_counts=True)
+    dup = set(uniq[counts > 1].tolist())
+    srcs = set(src.tolist())
+    ok &= np.array([d not in dup and d not in srcs for d in dst.tolist()])
+    return pairs[ok]
+
+
+def test_copy_blocks_4096_pairs_with_conflicts_far_apart(cuda_device):
+    # a fork of many samples: 4,096 pairs, handled by many thread blocks; the
+    # conflicting pairs sit far apart in the list, in other blocks' ranges
+    rng = np.random.default_rng(45)
+    n, nb, B, H, D = 4096, 9000, 16, 2, 64
+    kc = rng.integers(0, 65535, size=(nb, B, H, D), dtype=np.uint16)
+    vc = rng.integers(0, 65535, size=(nb, B, H, D), dtype=np.uint16)
+    perm = rng.permutation(nb).astype(np.int32)
+    pairs = np.stack([perm[:n], perm[n:2 * n]], 1).astype(np.int32)
+    pairs[10, 1] = pairs[4000, 1]      # one dst twice: both dropped
+    pairs[20, 1] = pairs[3000, 0]      # a dst that another pair reads: dropped
+    pairs[30, 0] = nb + 5              # out of range: dropped
+    pairs[2000, 1] = pairs[2000, 0]    # a block onto itself (its dst is a src): dropped
+    valid = _valid_pairs(pairs, nb)
+    assert valid.shape[0] == n - 5
+    dk = torch.from_numpy(kc.view(np.int16)).cuda().view(torch.float16)
+    dv = torch.from_numpy(vc.view(np.int16)).cuda().view(torch.float16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_copy_blocks(torch.from_numpy(pairs).cuda(), dk, dv, err=err)
+    assert pa.pa_get_error(err) == pa.PA_DEVERR_COPY_PAIR
+    oracle.copy_blocks(kc, vc, valid)
+    assert np.array_equal(bits_of(dk), kc) and np.array_equal(bits_of(dv), vc)
+
+
+def test_copy_blocks_time_grows_linearly_with_pairs(cuda_device):
+    # each thread block validates its own pairs against one pass over the list,
+    # so the call's time grows with the number of pairs, not with its square
+    nb, B, H, D = 17000, 16, 1, 64
+    kc = torch.zeros((nb, B, H, D), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    perm = np.random.default_rng(46).permutation(nb).astype(np.int32)
+    times = {}
+    for n in (512, 2048, 8192):
+        pairs = torch.from_numpy(np.stack([perm[:n], perm[n:2 * n]], 1).copy()).cuda()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ms = []
+        for rep in range(9):
+            ev[0].record()
+            pa.pa_copy_blocks(pairs, kc, vc, err=err)
+            ev[1].record()
+            torch.cuda.synchronize()
+            if rep >= 2:
+                ms.append(ev[0].elapsed_time(ev[1]))
+        times[n] = sorted(ms)[len(ms) // 2]
+    assert pa.pa_get_error(err) == 0
+    # 16 times the pairs: a quadratic check would take over 100 times as long
+    assert times[8192] < 16 * times[512] + 0.05, times
