@@ -484,10 +484,10 @@ class OracleStep:
     """The fp64 oracle's step (cache write of the sampled sequences' new tokens
     + decode of all their query heads) on the host cores."""
 
-    def __init__(self, wl):
+    def __init__(self, wl, threads=0):
         import oracle
         self.oracle, self.wl = oracle, wl
-        self.cores = cores()
+        self.cores = threads if threads > 0 else cores()
         self.kc, self.vc = wl.k_cache.copy(), wl.v_cache.copy()
         self.slots = oracle.slot_mapping(wl.block_tables, wl.new_seq, wl.new_pos, wl.block_size)
 
@@ -526,9 +526,10 @@ class OracleStep:
         return int(min(self.wl.num_seqs, max(1, budget_s / per_seq)))
 
 
-def oracle_rate(wl, budget_s):
-    """Sequence-steps per second of the oracle over about budget_s seconds."""
-    os_ = OracleStep(wl)
+def oracle_rate(wl, budget_s, threads=0):
+    """Sequence-steps per second of the oracle over about budget_s seconds
+    (threads: host threads, 0 for every core the process may use)."""
+    os_ = OracleStep(wl, threads)
     n = os_.sample_size(min(budget_s, 2.0))
     done, t_total, reps = 0, 0.0, 0
     while t_total < budget_s and reps < 1000:
@@ -665,6 +666,8 @@ def main():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads of the oracle's CPU baseline (0: every available core)")
     ap.add_argument("--pool-blocks", type=int, default=None,
                     help="smaller pool for the Llama-3-8B workload (profiling captures)")
     ap.add_argument("--mode", default="step", choices=["step", "swap"],
@@ -690,7 +693,8 @@ def main():
     wl = res["wl"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, sample, _, n_cores = oracle_rate(wl, budget_s=args.cpu_baseline_seconds)
+        r, sample, _, n_cores = oracle_rate(wl, budget_s=args.cpu_baseline_seconds,
+                                            threads=args.cpu_threads)
         cpu = {"value": round(r, 2), "unit": UNIT, "cores": n_cores, "kind": "oracle",
                "sample": sample}
     if rank == 0:

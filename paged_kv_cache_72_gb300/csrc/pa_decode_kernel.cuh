@@ -29,7 +29,8 @@
 //  * Eight consumer warps: warp w takes 16 tokens (tile w % TPH, TPH = 8 / HG)
 //    of head w / TPH of every chunk and keeps its own online-softmax state in
 //    fp32.  The tensor-core consumer computes S = Q.K^T and O += P.V with
-//    m16n8k16 MMAs (query heads on M, tokens / head_dim on N); the CUDA-core
+//    m16n8k16 MMAs (query heads on M, tokens / head_dim on N; P enters as a
+//    pair of 16-bit values whose sum carries it to 16 bits); the CUDA-core
 //    consumer (group size 1) uses per-lane head_dim slices and warp shuffles.
 //    When a warp owns its head alone (HG = 8) it writes its result directly;
 //    otherwise the TPH warps of a head merge through shared memory.
@@ -298,8 +299,14 @@ struct MmaConsumer {
       const uint32_t ra = row_addr(vpart, tt, cidx >> 3, a);
       ldmatrix_x4_trans(chunk_addr<kSwz>(ra, cidx & 7), vb[j][0], vb[j][1], vb[j][2], vb[j][3]);
     }
-    // online softmax, in the log2 domain, per query-head row
-    uint32_t pa[4];
+    // online softmax, in the log2 domain, per query-head row.  P goes to the
+    // P . V products as a pair of 16-bit values, hi = round(P) and
+    // lo = round(P - hi) (P - hi is exact in fp32), so that hi + lo is within
+    // 2^-16 (bfloat16) or 2^-22 (binary16) of P; the normaliser l sums the
+    // fp32 values.  One 16-bit P would move the output by up to the unit
+    // roundoff times the values' spread, many ulps of a small output; the
+    // second product costs about 1% of the decode, whose consumers have slack.
+    uint32_t pa[4], pl[4];
 #pragma unroll
     for (int hr = 0; hr < (kHi ? 2 : 1); ++hr) {
       float v[4];
@@ -317,10 +324,14 @@ struct MmaConsumer {
       const float mn = fmaxf(m[hr], mt);
       const float alpha = exp2f(m[hr] - mn);
       m[hr] = mn;
-      const uint32_t p01 = pack2<kBF16>(exp2f(v[0] - mn), exp2f(v[1] - mn));
-      const uint32_t p23 = pack2<kBF16>(exp2f(v[2] - mn), exp2f(v[3] - mn));
+      const float e0 = exp2f(v[0] - mn), e1 = exp2f(v[1] - mn);
+      const float e2 = exp2f(v[2] - mn), e3 = exp2f(v[3] - mn);
+      const uint32_t p01 = pack2<kBF16>(e0, e1);
+      const uint32_t p23 = pack2<kBF16>(e2, e3);
       const float2 f01 = unpack2<kBF16>(p01), f23 = unpack2<kBF16>(p23);
-      l[hr] = l[hr] * alpha + ((f01.x + f01.y) + (f23.x + f23.y));
+      pl[hr] = pack2<kBF16>(e0 - f01.x, e1 - f01.y);
+      pl[hr + 2] = pack2<kBF16>(e2 - f23.x, e3 - f23.y);
+      l[hr] = l[hr] * alpha + ((e0 + e1) + (e2 + e3));
       // once the running maximum settles, alpha is exactly 1 in every lane
       // and the rescale is skipped (multiplying by 1 changes nothing)
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -333,7 +344,7 @@ struct MmaConsumer {
       pa[hr] = p01;       // row gid (+8): tokens 2tig, 2tig+1
       pa[hr + 2] = p23;   // tokens 8 + 2tig, 9 + 2tig
     }
-    if (!kHi) { pa[1] = 0u; pa[3] = 0u; }
+    if (!kHi) { pa[1] = 0u; pa[3] = 0u; pl[1] = 0u; pl[3] = 0u; }
     if (nv < kTile || lo > 0) {
       // zero the V values of tokens outside [lo, nv) (the low 16 bits of a
       // fragment register hold token 2tig (+8), the high bits token 2tig+1)
@@ -353,6 +364,8 @@ struct MmaConsumer {
     for (int j = 0; j < D / 16; ++j) {
       mma_16816<kBF16>(o[2 * j], pa[0], pa[1], pa[2], pa[3], vb[j][0], vb[j][1]);
       mma_16816<kBF16>(o[2 * j + 1], pa[0], pa[1], pa[2], pa[3], vb[j][2], vb[j][3]);
+      mma_16816<kBF16>(o[2 * j], pl[0], pl[1], pl[2], pl[3], vb[j][0], vb[j][1]);
+      mma_16816<kBF16>(o[2 * j + 1], pl[0], pl[1], pl[2], pl[3], vb[j][2], vb[j][3]);
     }
   }
 

@@ -146,17 +146,20 @@ def unit_roundoff(dtype):
 
 
 def weight_roundoff(wl, flags=0):
-    """Relative rounding of the softmax weights P on the path that runs wl:
-    the tensor-core kernels feed P to their P.V products in 16 bits (the
-    cache dtype; binary16 for an E4M3 cache), the CUDA-core decode (group
-    size 1 unless the tensor-core kernel is forced) keeps P in fp32."""
+    """Relative rounding of the softmax weights P on the path that runs wl.
+    The CUDA-core decode (group size 1 unless the tensor-core kernel is
+    forced) keeps P in fp32.  The 16-bit tensor-core decode feeds P to its
+    P.V products as a pair hi = round(P), lo = round(P - hi) of 16-bit values,
+    whose sum carries P to within 2^-16 (bfloat16) or 2^-22 (binary16); 2^-15
+    bounds both.  The E4M3 decode feeds binary16 P (2^-11), the prefill P in
+    the model dtype."""
     G = wl.num_q_heads // wl.num_kv_heads
     if wl.query_start is not None:
         return unit_roundoff(wl.dtype)
     mma = (flags & 0xff) == pa.PA_DECODE_MMA or ((flags & 0xff) == pa.PA_DECODE_AUTO and G > 1)
     if not mma:
         return 0.0
-    return 2.0 ** -11 if wl.fp8 else unit_roundoff(wl.dtype)
+    return 2.0 ** -11 if wl.fp8 else 2.0 ** -15
 
 
 def _f64_to_f32_round_to_odd(x):
