@@ -223,3 +223,23 @@ def test_gather_is_bit_exact(cuda_device, flags, B, D, dtype):
         o = offs[i]
         assert np.array_equal(kg[o:o + T], oracle.gather_bits(wl.k_cache, wl.block_tables[i], T))
         assert np.array_equal(vg[o:o + T], oracle.gather_bits(wl.v_cache, wl.block_tables[i], T))
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8", "window"])
+def test_more_sequences_than_the_length_cache(cuda_device, kind):
+    # the decode keeps the first 1,024 lengths in shared memory and reads the
+    # others from global memory: 2,500 short sequences cross that line, with
+    # the lengths and tables read before the grid-dependency wait
+    rng = np.random.default_rng(2500)
+    lens = rng.integers(1, 80, size=2500)
+    lens[[0, 1023, 1024, 1025, 2499]] = [1, 17, 33, 1, 79]
+    kw = {"fp8": {"fp8_scales": (2.0 ** -6, 2.0 ** -6)}, "window": {"window": 20}}.get(kind, {})
+    wl = W.random_workload(2500, W.BF16, 8, 2, 64, 16, lens, kv_sigma=0.7, garbage="nan", **kw)
+    flags = pa.PA_DECODE_TABLES_READY
+    st = GpuState(wl)
+    out, _ = gpu_step(st, flags=flags)
+    assert pa.pa_get_error(st.err) == 0
+    ref = OracleState(wl)
+    ref.step()
+    expected, spread = ref.decode(spread=True)
+    check_parity(out, wl, expected, spread, "%s, 2,500 sequences" % kind, flags=flags)

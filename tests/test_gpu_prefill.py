@@ -14,6 +14,7 @@ import oracle
 import paged_kv_cache_72_gb300 as pa
 import workloads as W
 from harness import GpuState, OracleState, assert_close, check_parity, gpu_out_f64, gpu_step
+from paged_kv_cache_72_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
 
@@ -150,3 +151,25 @@ def test_prefill_sequences_ending_on_stage_edges(cuda_device):
     chunk = [5, 1, 2, 64, 64, 63]
     wl = W.random_prefill(160, W.F16, 8, 2, 128, 16, prefix, chunk, garbage="nan")
     _parity(wl)
+
+
+def test_prefill_at_the_sequence_limit(cuda_device):
+    # every sequence's item offset sits in shared memory, up to 4,096
+    # sequences: a batch of 4,096, mostly single decode tokens with a chunk in
+    # every 97th, and one sequence more is refused
+    rng = np.random.default_rng(4096)
+    n = 4096
+    prefix = rng.integers(0, 60, size=n)
+    chunk = np.ones(n, dtype=np.int64)
+    chunk[::97] = rng.integers(2, 40, size=chunk[::97].size)
+    wl = W.random_prefill(4096, W.BF16, 8, 2, 64, 16, prefix, chunk, garbage="nan")
+    _parity(wl)
+    st = GpuState(wl)
+    extra_lens = torch.cat([st.seq_lens, st.seq_lens[:1]])
+    extra_qs = torch.cat([st.query_start, st.query_start[-1:] + 1])
+    q = torch.zeros((int(wl.query_start[-1]) + 1,) + tuple(st.q.shape[1:]), dtype=st.q.dtype,
+                    device="cuda")
+    bt = torch.cat([st.block_tables, st.block_tables[:1]])
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_prefill(q, st.k_cache, st.v_cache, bt, extra_lens, extra_qs, wl.scale, err=st.err)
+    assert e.value.status == _lib.PA_ERR_UNSUPPORTED
