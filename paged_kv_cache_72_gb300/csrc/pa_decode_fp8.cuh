@@ -43,14 +43,6 @@ namespace pa {
 // Tokens per warp per chunk of this consumer (the 16-bit consumers take 16).
 constexpr int kTileF8 = 32;
 
-// 8x8 transpose of 16-bit elements held in the m8n8 fragment layout (lane
-// 4 gid + tig holds row gid, columns 2 tig and 2 tig + 1).
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
-  return r;
-}
-
 template <int D, bool kBF16, bool kSwz, bool kHi>
 struct MmaConsumerF8 {
   static constexpr int KS = D / 16;        // k-steps of S^T over head_dim

@@ -28,10 +28,12 @@
 //    and shared by the G query heads of its KV head.
 //  * Eight consumer warps: warp w takes 16 tokens (tile w % TPH, TPH = 8 / HG)
 //    of head w / TPH of every chunk and keeps its own online-softmax state in
-//    fp32.  The tensor-core consumer computes S = Q.K^T and O += P.V with
-//    m16n8k16 MMAs (query heads on M, tokens / head_dim on N; P enters as a
-//    pair of 16-bit values whose sum carries it to 16 bits); the CUDA-core
-//    consumer (group size 1) uses per-lane head_dim slices and warp shuffles.
+//    fp32.  The tensor-core consumers use m16n8k16 MMAs; for groups of up to
+//    8 query heads they compute the transposed products S^T = K.Q^T and
+//    O^T += V^T.P^T (tokens / head_dim on M, the heads on N), for larger
+//    groups S = Q.K^T and O += P.V (heads on M); P enters as a pair of 16-bit
+//    values whose sum carries it to 16 bits.  The CUDA-core consumer (group
+//    size 1) uses per-lane head_dim slices and warp shuffles.
 //    When a warp owns its head alone (HG = 8) it writes its result directly;
 //    otherwise the TPH warps of a head merge through shared memory.
 //  * Every wait is bounded; a wait that gives up sets PA_DEVERR_TIMEOUT and the
@@ -50,20 +52,23 @@ constexpr int kProducerWarp = kCWarps;
 enum Mode : int { kModeSimt = 0, kModeMma = 1, kModeGather = 2 };
 
 // A block of nine warps has three on one SM sub-partition, which leaves
-// every thread at most 168 registers.  The 16-bit tensor-core consumer needs
-// more: its blocks put the producer in a warpgroup of its own (three more
-// warps that leave at once), and the two warpgroups re-divide the registers
-// the block is launched with (setmaxnreg): the producer's group keeps
-// kProducerRegs per thread, the consumers take kConsumerRegs.  The other
-// consumers run best as they are, in nine-warp blocks.
+// every thread at most 168 registers.  The 16-bit tensor-core consumer for
+// groups of more than 8 query heads needs more: its blocks put the producer
+// in a warpgroup of its own (three more warps that leave at once), and the
+// two warpgroups re-divide the registers the block is launched with
+// (setmaxnreg): the producer's group keeps kProducerRegs per thread, the
+// consumers take kConsumerRegs.  The other consumers (the transposed one for
+// groups of up to 8 among them) fit in 168 and run as nine-warp blocks.
 constexpr int kLaunchRegs = 168;     // 65536 / 384, rounded down to a multiple of 8
 constexpr int kProducerRegs = 56;
 constexpr int kConsumerRegs = 224;
 static_assert(kCWarps * 32 * kConsumerRegs + 128 * kProducerRegs <= (kCWarps + 4) * 32 * kLaunchRegs,
               "the register split must fit in what the block is launched with");
-__host__ __device__ constexpr bool split_regs(int mode, bool f8) { return mode == kModeMma && !f8; }
-__host__ __device__ constexpr int block_threads(int mode, bool f8) {
-  return (kCWarps + (split_regs(mode, f8) ? 4 : 1)) * 32;
+__host__ __device__ constexpr bool split_regs(int mode, bool f8, bool hi) {
+  return mode == kModeMma && !f8 && hi;
+}
+__host__ __device__ constexpr int block_threads(int mode, bool f8, bool hi) {
+  return (kCWarps + (split_regs(mode, f8, hi) ? 4 : 1)) * 32;
 }
 constexpr int kQBufs = 2;          // query-row buffers in flight
 // Query rows sit in shared memory at a pitch of one row plus 16 bytes, so
@@ -429,6 +434,226 @@ struct MmaConsumer {
 };
 
 // ---------------------------------------------------------------------------
+// Consumer state and tile math: tensor-core path with transposed products
+// (group size at most 8).  S^T = K . Q^T and O^T += V^T . P^T put the 16
+// tokens and head_dim on the MMA's 16-wide M side and the (up to 8) query
+// heads on its 8-wide N side, so no MMA row is padding: per tile, 8 products
+// for the scores and 8 per 16-bit half of P for the output, against 16 and
+// 32 with the heads on M.  The K and V fragments are the same ldmatrix loads
+// as there, taken as A operands; P^T's B fragments are the score
+// accumulators packed to 16 bits and transposed in registers (movmatrix).
+// ---------------------------------------------------------------------------
+template <int D, bool kBF16, bool kSwz>
+struct MmaConsumerT {
+  static constexpr int KS = D / 16;   // k-steps of S^T over head_dim
+  static constexpr int MT = D / 16;   // m-tiles of O^T over head_dim
+  static constexpr int QP = q_pitch<D>();
+  uint32_t qb[KS][2];   // Q^T: head gid, head_dim 16 ks + 2 tig (+1) and + 8
+  float o[MT][4];       // O^T: head_dim 16 i + gid (+8) x heads 2 tig, 2 tig + 1
+  float m[2];           // heads 2 tig + e: running maximum (the same in a tig's 8 lanes)
+  float l[2];           // and this lane's share of their running sums
+
+  // qslot: this head group's G query rows, QP bytes apart
+  __device__ __forceinline__ void begin(uint32_t qslot, int G) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int d0 = ks * 16 + 2 * tig;
+      uint32_t b0 = 0, b1 = 0;
+      if (gid < G) {
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(qslot + gid * QP + d0 * 2));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(qslot + gid * QP + (d0 + 8) * 2));
+      }
+      qb[ks][0] = b0;
+      qb[ks][1] = b1;
+    }
+#pragma unroll
+    for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  // 16 tokens [tile0, tile0 + 16) of the chunk; tokens [lo, nv) of them are
+  // valid, lo < nv (the others may hold anything, NaN included: their scores
+  // are masked and their V values zeroed in registers).
+  __device__ __forceinline__ void tile(uint32_t kpart, uint32_t vpart, int tile0, int lo, int nv,
+                                       const DecodeArgs& a, float sl2) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    // K fragments: kb[h][kp][j] holds tokens 8 h + (0..7) x head_dim
+    // 32 kp + 8 j + (0..7), so that k-step 2 kp + u takes kb[.][kp][2u], [2u + 1]
+    uint32_t kb[2][D / 32][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int tt = tile0 + h * 8 + (lane & 7);
+#pragma unroll
+      for (int kp = 0; kp < D / 32; ++kp) {
+        const int cidx = kp * 4 + (lane >> 3);
+        const uint32_t ra = row_addr(kpart, tt, cidx >> 3, a);
+        ldmatrix_x4(chunk_addr<kSwz>(ra, cidx & 7), kb[h][kp][0], kb[h][kp][1], kb[h][kp][2],
+                    kb[h][kp][3]);
+      }
+    }
+    // S^T: even and odd k-steps in two accumulation chains
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kp = 0; kp < D / 32; ++kp) {
+      mma_16816<kBF16>(s, kb[0][kp][0], kb[1][kp][0], kb[0][kp][1], kb[1][kp][1], qb[2 * kp][0],
+                       qb[2 * kp][1]);
+      mma_16816<kBF16>(s2, kb[0][kp][2], kb[1][kp][2], kb[0][kp][3], kb[1][kp][3],
+                       qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
+    }
+    // V fragments (A of O^T): vb[j][.] holds tokens (0..7 | 8..15) x head_dim
+    // 16 j + (0..7 | 8..15), loaded before the softmax math so that their
+    // latency hides behind it
+    uint32_t vb[MT][4];
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+      const int mat = lane >> 3;
+      const int tt = tile0 + ((mat & 1) << 3) + (lane & 7);
+      const int cidx = 2 * j + (mat >> 1);
+      const uint32_t ra = row_addr(vpart, tt, cidx >> 3, a);
+      ldmatrix_x4_trans(chunk_addr<kSwz>(ra, cidx & 7), vb[j][0], vb[j][1], vb[j][2], vb[j][3]);
+    }
+    // online softmax per head column (heads 2 tig + e; this lane holds tokens
+    // gid and gid + 8): the 8 lanes of a tig reduce the maximum by shuffles
+    const bool t0ok = gid >= lo && gid < nv, t1ok = gid + 8 >= lo && gid + 8 < nv;
+    const float x0 = t0ok ? (s[0] + s2[0]) * sl2 : -INFINITY;
+    const float x1 = t0ok ? (s[1] + s2[1]) * sl2 : -INFINITY;
+    const float x2 = t1ok ? (s[2] + s2[2]) * sl2 : -INFINITY;
+    const float x3 = t1ok ? (s[3] + s2[3]) * sl2 : -INFINITY;
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+    }
+    // token lo is valid, so both maxima are finite
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    const float alpha0 = exp2f(m[0] - mn0), alpha1 = exp2f(m[1] - mn1);
+    m[0] = mn0;
+    m[1] = mn1;
+    const float e0 = exp2f(x0 - mn0), e1 = exp2f(x1 - mn1);
+    const float e2 = exp2f(x2 - mn0), e3 = exp2f(x3 - mn1);
+    // P enters the products as a pair of 16-bit values, hi = round(P) and
+    // lo = round(P - hi) (P - hi is exact in fp32), so that hi + lo is within
+    // 2^-16 (bfloat16) or 2^-22 (binary16) of P; the normaliser l sums the
+    // fp32 values.  One 16-bit P would move the output by up to the unit
+    // roundoff times the spread of the values, many ulps of a small output.
+    const uint32_t h01 = pack2<kBF16>(e0, e1), h23 = pack2<kBF16>(e2, e3);
+    const float2 f01 = unpack2<kBF16>(h01), f23 = unpack2<kBF16>(h23);
+    const uint32_t l01 = pack2<kBF16>(e0 - f01.x, e1 - f01.y);
+    const uint32_t l23 = pack2<kBF16>(e2 - f23.x, e3 - f23.y);
+    l[0] = l[0] * alpha0 + (e0 + e2);
+    l[1] = l[1] * alpha1 + (e1 + e3);
+    // once the running maxima settle, alpha is exactly 1 in every lane and
+    // the rescale is skipped (multiplying by 1 changes nothing)
+    if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        o[i][0] *= alpha0;
+        o[i][1] *= alpha1;
+        o[i][2] *= alpha0;
+        o[i][3] *= alpha1;
+      }
+    }
+    // P^T's B fragments: head gid x tokens 2 tig (+1) and 2 tig + 8 (+9)
+    const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+    const uint32_t pl0 = movmatrix_trans(l01), pl1 = movmatrix_trans(l23);
+    if (nv < kTile || lo > 0) {
+      // zero the V values of tokens outside [lo, nv) (the low 16 bits of a
+      // fragment register hold token 2tig (+8), the high bits token 2tig+1)
+      auto in = [&](int t) { return t >= lo && t < nv; };
+      const uint32_t mlo = (in(2 * tig) ? 0x0000ffffu : 0u) | (in(2 * tig + 1) ? 0xffff0000u : 0u);
+      const uint32_t mhi = (in(8 + 2 * tig) ? 0x0000ffffu : 0u) | (in(9 + 2 * tig) ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        vb[j][0] &= mlo;
+        vb[j][2] &= mlo;
+        vb[j][1] &= mhi;
+        vb[j][3] &= mhi;
+      }
+    }
+    // O^T += V^T . P^T, m-tile j = head_dim 16 j .. 16 j + 15
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+      mma_16816<kBF16>(o[j], vb[j][0], vb[j][2], vb[j][1], vb[j][3], ph0, ph1);
+      mma_16816<kBF16>(o[j], vb[j][0], vb[j][2], vb[j][1], vb[j][3], pl0, pl1);
+    }
+  }
+
+  // the full sum of head 2 tig + e over the 8 lanes that share it
+  __device__ __forceinline__ float total_l(int e) const {
+    float lt = l[e];
+    lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+    return lt;
+  }
+
+  // this lane's fp32 values of head 2 tig + e into row `orow` (D floats)
+  __device__ __forceinline__ void store_row_f32(float* orow, int e) const {
+    const int gid = (threadIdx.x & 31) >> 2;
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+      orow[16 * i + gid] = o[i][e];
+      orow[16 * i + 8 + gid] = o[i][2 + e];
+    }
+  }
+
+  // Write this warp's (m, l, o) rows into its merge slot: ml[2][16], o[16][D].
+  __device__ __forceinline__ void store(float* slot, int G) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float lt = total_l(e);
+      const int row = 2 * tig + e;
+      if (row < G) {
+        if (gid == 0) {
+          slot[row] = m[e];
+          slot[16 + row] = lt;
+        }
+        store_row_f32(slot + 32 + row * D, e);
+      }
+    }
+  }
+
+  // A warp that holds a whole head group's segment writes it directly: the
+  // output rows (full context, each normalised and rounded once, then
+  // transposed in registers so that a lane writes pairs of columns) or the
+  // partial state record (rows rec_row0 ..).
+  __device__ __forceinline__ void write_direct(uint16_t* out_rows, float* rec, int rec_row0,
+                                               int rec_rows, bool full, int G) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const float lt0 = total_l(0), lt1 = total_l(1);
+    if (full) {
+      const float inv0 = 1.f / lt0, inv1 = 1.f / lt1;
+      uint16_t* dst = out_rows + (size_t)gid * D + 2 * tig;
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        const uint32_t t0 = movmatrix_trans(pack2<kBF16>(o[i][0] * inv0, o[i][1] * inv1));
+        const uint32_t t1 = movmatrix_trans(pack2<kBF16>(o[i][2] * inv0, o[i][3] * inv1));
+        if (gid < G) {
+          *reinterpret_cast<uint32_t*>(dst + 16 * i) = t0;
+          *reinterpret_cast<uint32_t*>(dst + 16 * i + 8) = t1;
+        }
+      }
+      return;
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = 2 * tig + e;
+      if (row >= G) continue;
+      const int r = rec_row0 + row;
+      if (gid == 0) {
+        rec[(size_t)rec_rows * D + r] = m[e];
+        rec[(size_t)rec_rows * D + rec_rows + r] = e ? lt1 : lt0;
+      }
+      store_row_f32(rec + (size_t)r * D, e);
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
 // Consumer state and tile math: CUDA-core path (group size 1)
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16, bool kF8 = false>
@@ -724,10 +949,10 @@ __device__ __forceinline__ void merge_split(uint16_t* out, const float* ws_rec, 
   if (nsets > last - first + 1) nsets = last - first + 1;
   const int d = (tid % kTPR) * 16;
   // Pieces are read kBatch at a time, every load of a batch issued before its
-  // first fold, so that a batch costs one L2 round trip.  Only the kernels
-  // whose consumers hold 224 registers batch: in the others the extra
-  // registers raise spills in the main loop (measured: +0.4 us on the E4M3
-  // decode with two, +3.9 us with four).
+  // first fold, so that a batch costs one L2 round trip.  Only the 16-bit
+  // tensor-core kernels batch, where two pieces fit in their registers: in
+  // the others the extra registers raise spills in the main loop (measured:
+  // +0.4 us on the E4M3 decode with two, +3.9 us with four).
   auto fold_pieces = [&](MergeState<D>& st, int r, int k0, int step) {
     for (int kb = k0; kb <= last; kb += kBatch * step) {
       float mk[kBatch], lk[kBatch];
@@ -804,7 +1029,7 @@ __device__ __forceinline__ void merge_split(uint16_t* out, const float* ws_rec, 
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16, int kMode, bool kSwz, bool kHi, bool kF8>
-__global__ void __launch_bounds__(block_threads(kMode, kF8), 1)
+__global__ void __launch_bounds__(block_threads(kMode, kF8, kHi), 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -813,7 +1038,7 @@ __global__ void __launch_bounds__(block_threads(kMode, kF8), 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
 
-  constexpr int kThreads = block_threads(kMode, kF8);
+  constexpr int kThreads = block_threads(kMode, kF8, kHi);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = a.stages;
   const uint32_t bar_full = base + a.ctrl_off;      // S x 8 bytes
@@ -951,7 +1176,7 @@ __global__ void __launch_bounds__(block_threads(kMode, kF8), 1)
   const uint32_t box_bytes = 1u << a.sub_log2;
 
   if (warp >= kCWarps) {
-    if constexpr (split_regs(kMode, kF8)) {
+    if constexpr (split_regs(kMode, kF8, kHi)) {
       setmaxnreg_dec<kProducerRegs>();
       if (warp != kProducerWarp) return;
     }
@@ -1065,11 +1290,12 @@ __global__ void __launch_bounds__(block_threads(kMode, kF8), 1)
   }
 
   // ======================= consumers =======================
-  if constexpr (split_regs(kMode, kF8)) setmaxnreg_inc<kConsumerRegs>();
+  if constexpr (split_regs(kMode, kF8, kHi)) setmaxnreg_inc<kConsumerRegs>();
   // out and the workspace may be touched by the preceding kernel
   if (a.early_tables) grid_dep_wait();
-  using Mma = typename std::conditional<kF8, MmaConsumerF8<D, kBF16, kSwz, kHi>,
-                                        MmaConsumer<D, kBF16, kSwz, kHi>>::type;
+  using Mma16 = typename std::conditional<kHi, MmaConsumer<D, kBF16, kSwz, kHi>,
+                                          MmaConsumerT<D, kBF16, kSwz>>::type;
+  using Mma = typename std::conditional<kF8, MmaConsumerF8<D, kBF16, kSwz, kHi>, Mma16>::type;
   using Consumer =
       typename std::conditional<kMode == kModeSimt, SimtConsumer<D, kBF16, kF8>, Mma>::type;
   Consumer cs;
@@ -1196,7 +1422,7 @@ __global__ void __launch_bounds__(block_threads(kMode, kF8), 1)
     const int* pm = ctrl + kCtrlMerges;
     const int owed = pm[0];
     for (int k = 0; k < owed; ++k)
-      merge_split<D, kBF16, split_regs(kMode, kF8) ? 2 : 1>(
+      merge_split<D, kBF16, (kMode == kModeMma && !kF8) ? 2 : 1>(
           a.out, a.ws_rec, a.Hq, a.HG * a.G, pm[1 + 4 * k], pm[2 + 4 * k], start + pm[3 + 4 * k],
           pm[4 + 4 * k], cpc, reinterpret_cast<float*>(gbase));
   }

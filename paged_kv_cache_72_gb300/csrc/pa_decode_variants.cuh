@@ -82,7 +82,7 @@ int ctas_per_sm_impl(const DecodePlan& p, int* ctas) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          p.smem_optin);
     if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute");
-    if (split_regs(p.mode, kF8)) {
+    if (split_regs(p.mode, kF8, p.hi)) {
       // the warpgroups re-divide the registers the block is launched with;
       // with fewer at launch the consumers' request could not be met
       cudaFuncAttributes fa;
@@ -91,7 +91,7 @@ int ctas_per_sm_impl(const DecodePlan& p, int* ctas) {
       if (fa.numRegs < kLaunchRegs) return PA_ERR_UNSUPPORTED;
     }
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, block_threads(p.mode, kF8),
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, block_threads(p.mode, kF8, p.hi),
                                                       p.smem_bytes);
     if (e != cudaSuccess) return launch_status(e, "occupancy query");
     *ctas = n;
@@ -106,7 +106,7 @@ int launch_impl(const DecodePlan& p, const CUtensorMap& tk, const CUtensorMap& t
   // no CTA waits for another, so any grid size runs as an ordinary launch
   return with_variant<D, kF8>(p, [&](auto kern) -> int {
     const cudaError_t e =
-        launch_pdl(kern, dim3(p.grid), dim3(block_threads(p.mode, kF8)), (size_t)p.smem_bytes,
+        launch_pdl(kern, dim3(p.grid), dim3(block_threads(p.mode, kF8, p.hi)), (size_t)p.smem_bytes,
                    s, tk, tv, a);
     return launch_status(e, "decode kernel launch");
   });
