@@ -385,4 +385,39 @@ __device__ __forceinline__ uint16_t round16(float x) {
   }
 }
 
+// max(a, b, c) in one instruction (a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// x0 = x0 * f + c and x1 = x1 * f + c, each rounded once, in one packed
+// instruction
+__device__ __forceinline__ void ffma2(float& x0, float& x1, float f, float c) {
+  asm("{\n\t.reg .b64 x, m, a;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 m, {%2, %2};\n\t"
+      "mov.b64 a, {%3, %3};\n\tfma.rn.f32x2 x, x, m, a;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(f), "f"(c));
+}
+
+// acc + lo + hi of a packed 16-bit pair, each 16-bit value widened exactly
+// and added in fp32 (two mixed-precision adds, no unpacking)
+template <bool kBF16>
+__device__ __forceinline__ float add_pair16(float acc, uint32_t pk) {
+  float r;
+  if constexpr (kBF16) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t"
+        "add.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "=f"(r)
+        : "r"(pk), "f"(acc));
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t"
+        "add.rn.f32.f16 %0, hi, %0;\n\t}"
+        : "=f"(r)
+        : "r"(pk), "f"(acc));
+  }
+  return r;
+}
+
 }  // namespace pa

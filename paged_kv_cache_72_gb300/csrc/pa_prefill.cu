@@ -541,8 +541,9 @@ constexpr int kTcProducer = 8;
 constexpr int kTcMma = 9;           // warps 9 and 10: the MMA issuers of tiles A and B
 constexpr uint32_t kTcTmemCols = 512;
 constexpr float kTcTau = 8.f;
+constexpr float kTcTauPow = 256.f;   // 2^kTcTau
 // barriers (8 bytes each): q full, q empty; per tile 8 slots (s full, s free,
-// p full, p empty[2], o free, two unused); done[2]
+// p full[2], p empty[2], o free, one unused); done[2]
 constexpr int kTcBars = 2 + 2 * 8 + 2;
 
 __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
@@ -581,8 +582,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t bar_seen = bar_empty + 8 * S;
   const uint32_t bar_qfull = bar_seen + 8 * S;
   const uint32_t bar_qempty = bar_qfull + 8;
-  // tile t's barriers: s full at +0, s free at +16, p full at +32, p empty of
-  // P region 0 at +40 and of region 1 at +56, o free at +48
+  // tile t's barriers: s full at +0, s free at +16, p full of P region 0 at
+  // +32 and of region 1 at +24, p empty of region 0 at +40 and of region 1 at
+  // +56, o free at +48.  P full is one barrier per region: a warp may reach
+  // stage k + 1 while another of its warpgroup still writes stage k's P (the
+  // next scores need only every warp to have read stage k's), so with one
+  // barrier its arrival for k + 1 could complete stage k's phase early.  It
+  // cannot reach stage k + 2, which waits for the P . V of stage k.
   const uint32_t bar_tile0 = bar_qfull + 16;
   const uint32_t bar_done = bar_tile0 + 128;
   uint8_t* const cgen = gbase + a.ctrl_off + tc_tags_off(S);
@@ -607,7 +613,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t bt = bar_tile0 + 64 * t;
       mbar_init(bt, 1);                      // s full: a commit
       mbar_init(bt + 16, 128);               // s free: the warpgroup's threads
-      mbar_init(bt + 32, 128);               // p full: the warpgroup's threads
+      mbar_init(bt + 32, 128);               // p full, region 0: the warpgroup's threads
+      mbar_init(bt + 24, 128);               // p full, region 1
       mbar_init(bt + 40, 1);                 // p empty, region 0: a commit
       mbar_init(bt + 56, 1);                 // p empty, region 1: a commit
       mbar_init(bt + 48, 128);               // o free: the warpgroup's threads
@@ -787,7 +794,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t rc = (ring >> (6 * (rh & 3))) & 63u;
           const int pst = (int)(rc & 7u);
           const bool first = (rc & 8u) != 0u;
-          if (mbar_test(bt + 32, (uint32_t)np & 1u) &&
+          if (mbar_test(bt + ((np & 1) ? 24 : 32), (uint32_t)(np >> 1) & 1u) &&
               (!(rc & 16u) || mbar_test(bt + 48, (rc >> 5) & 1u))) {
             tc_fence_after();
             const uint64_t dv = umma_desc_sw128(
@@ -934,59 +941,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bt + 16);   // the S buffer may be overwritten
-      // ---- causal mask (a padding row keeps finite scores against cached
-      // keys) and maximum.  A stage wholly at or before the tile's first
-      // position needs no mask, and with a positive scale its maximum is
-      // taken on the raw scores; otherwise the scores are scaled first.
-      // (eight partial maxima and sums: one warp per sub-partition leaves no
-      // other warp to hide a 64-long chain of dependent instructions)
       const int tb = kt * kPBN;
-      float mx8[8], f = 1.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
-      const bool raw = tb + kPBN - 1 <= p0 && sl2 > 0.f;
-      if (raw) {
-#pragma unroll
-        for (int c = 0; c < kPBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
-        f = sl2;
-      } else {
-#pragma unroll
-        for (int c = 0; c < kPBN; ++c) {
-          const int t = tb + c;
-          const bool in = prow >= 0 ? t <= prow : t < it.T;
-          const float v = in ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-          sr[c] = __float_as_uint(v);
-          mx8[c & 7] = fmaxf(mx8[c & 7], v);
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) mx8[c] = fmaxf(mx8[c], mx8[c + 4]);
-      float mx = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
-      if (raw) mx *= sl2;
-      float alpha = 1.f;
-      if (mx > m_used + kTcTau) {   // the exponentials' reference moves
-        if (m_used != -INFINITY) alpha = ex2_approx(m_used - mx);
-        m_used = mx;
-      }
-      const float mu = m_used == -INFINITY ? 0.f : m_used;   // no row is masked whole at kt 0
-      // ---- P = 2^(s f - m_used), one FFMA and one ex2 per score, 16-bit;
-      // its row sum in fp32 over the rounded values that O sums, so that a
-      // row dominated by one key keeps that key's value
+      // ---- P = 2^(s f - mu): one packed FFMA per two scores and one ex2 per
+      // score, 16-bit; its row sum in fp32 over the rounded values that O
+      // sums (mixed-precision adds of the 16-bit halves), so that a row
+      // dominated by one key keeps that key's value
       uint32_t pk[kPBN / 2];
-      float sum8[8];
+      auto p_pass = [&](float f, float mu) -> float {
+        float sum8[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) sum8[c] = 0.f;
+        for (int c = 0; c < 8; ++c) sum8[c] = 0.f;
 #pragma unroll
-      for (int c = 0; c < kPBN / 2; ++c) {
-        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), f, -mu));
-        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), f, -mu));
-        pk[c] = pack2<kBF16>(e0, e1);
-        const float2 pr = unpack2<kBF16>(pk[c]);
-        sum8[c & 7] += pr.x + pr.y;
+        for (int c = 0; c < kPBN / 2; ++c) {
+          float x0 = __uint_as_float(sr[2 * c]), x1 = __uint_as_float(sr[2 * c + 1]);
+          ffma2(x0, x1, f, -mu);
+          pk[c] = pack2<kBF16>(ex2_approx(x0), ex2_approx(x1));
+          sum8[c & 7] = add_pair16<kBF16>(sum8[c & 7], pk[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sum8[c] += sum8[c + 4];
+        return (sum8[0] + sum8[1]) + (sum8[2] + sum8[3]);
+      };
+      // A stage wholly at or before the tile's first position needs no mask;
+      // with a positive scale its scores are used raw, f = scale.  Once the
+      // row has a reference maximum, such a stage first computes P against
+      // it: every P is at most the stage's sum, so a sum of at most 2^kTcTau
+      // shows that the reference stays, and the maximum is not needed.
+      const bool raw = tb + kPBN - 1 <= p0 && sl2 > 0.f;
+      const bool guess = raw && m_used != -INFINITY;
+      float alpha = 1.f, ssum = 0.f;
+      if (guess) ssum = p_pass(sl2, m_used);
+      if (!guess || !(ssum <= kTcTauPow)) {
+        // ---- causal mask (a padding row keeps finite scores against cached
+        // keys) and maximum; unmasked stages take it on the raw scores,
+        // masked ones scale the scores first (f = 1).  Eight partial maxima:
+        // one warp per sub-partition leaves no other warp to hide a 64-long
+        // chain of dependent instructions; a three-input max takes two
+        // scores at a time.
+        float mx8[8], f = 1.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
+        if (raw) {
+#pragma unroll
+          for (int c = 0; c < kPBN / 2; ++c)
+            mx8[c & 7] = max3f(mx8[c & 7], __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+          f = sl2;
+        } else {
+#pragma unroll
+          for (int c = 0; c < kPBN / 2; ++c) {
+            float v[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int t = tb + 2 * c + u;
+              const bool in = prow >= 0 ? t <= prow : t < it.T;
+              v[u] = in ? __uint_as_float(sr[2 * c + u]) * sl2 : -INFINITY;
+              sr[2 * c + u] = __float_as_uint(v[u]);
+            }
+            mx8[c & 7] = max3f(mx8[c & 7], v[0], v[1]);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mx8[c] = fmaxf(mx8[c], mx8[c + 4]);
+        float mx = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+        if (raw) mx *= sl2;
+        bool moved = false;
+        if (mx > m_used + kTcTau) {   // the exponentials' reference moves
+          if (m_used != -INFINITY) alpha = ex2_approx(m_used - mx);
+          m_used = mx;
+          moved = true;
+        }
+        // (no row is masked whole at kt 0)
+        if (!guess || moved) ssum = p_pass(f, m_used == -INFINITY ? 0.f : m_used);
       }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) sum8[c] += sum8[c + 4];
-      l = l * alpha + ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3]));
+      l = l * alpha + ssum;
       // the P region's previous use (two stages back) is done: its O += P . V
       // has completed
       const uint32_t pe = bt + ((nt & 1) ? 56 : 40);
@@ -1029,11 +1056,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               vpart + (uint32_t)p * kKPlane + (uint32_t)(z0 + (rem >> 3)) * 128u + (uint32_t)(rem & 7) * 16u;
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
         }
+        fence_proxy_async_smem();   // the cleared rows, before the tensor core reads them
       }
       tmem_wait_st();
-      fence_proxy_async_smem();   // the cleared rows, before the tensor core reads them
       tc_fence_before();
-      mbar_arrive(bt + 32);
+      mbar_arrive(bt + ((nt & 1) ? 24 : 32));   // P region nt % 2 is written
       if (kt == nkt_t - 1) {
         // ---- the tile's last stage: out = O / l once O += P . V is done
         if (!wait_warp(pe, (uint32_t)(nt >> 1) & 1u)) {
