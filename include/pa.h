@@ -247,7 +247,11 @@ int pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t 
  *   workspace  device buffer of at least pa_decode_workspace_size() bytes,
  *              zero-filled before its first use; every call that runs to its
  *              end (device errors included) leaves it zero-ready for the next
- *              call.  Calls sharing one workspace must not overlap on the GPU.
+ *              call.  One exception: seq_lens changing while the call reads
+ *              it (a caller error) can leave a thread block unable to find
+ *              its work; it reports PA_DEVERR_SEQ_LEN without counting its
+ *              pieces, and the workspace must be zero-filled again.  Calls
+ *              sharing one workspace must not overlap on the GPU.
  * Query head hq reads KV head hq / G (contiguous query groups).  Accumulation
  * is fp32; the output is rounded once to dtype.  The result does not depend on
  * where the blocks sit in the pool.  The work (chunks of one block's worth of

@@ -1161,7 +1161,11 @@ __global__ void __launch_bounds__(block_threads(kMode, kF8, kHi), 1)
     }
   }
   if (n_chunks == 0) return;
-  if (ctrl[0] < 0) {   // cannot happen for a consistent scan; never walk blind
+  // Cannot happen for a consistent scan (seq_lens changing during the call
+  // could cause it); never walk blind.  This CTA's pieces go uncounted, so
+  // the caller must zero the workspace again (the no-allocation entry point
+  // clears its counters at every call).
+  if (ctrl[0] < 0) {
     if (a.early_tables) grid_dep_wait();
     if (tid == 0) set_error(a.err, PA_DEVERR_SEQ_LEN);
     return;
