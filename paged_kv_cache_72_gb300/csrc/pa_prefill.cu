@@ -515,10 +515,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
 //    tiles by TMA (one copy per 64-column plane, [row][128 bytes], 128-byte
 //    swizzle), per stage the K and V planes of the item's KV head, tagged with
 //    the item.
-//  * warps 9 and 10 (MMA, one thread each, one per tile): per stage S = Q .
-//    K^T (M 128, N 64, K = head_dim) into the tile's S buffer, and O += P . V
-//    (M 128, N head_dim, K 64; P from tensor memory, V from shared memory as
-//    an MN-major operand) once its P is written.
+//  * warps 9 and 10 (score products, one thread each, one per tile): per
+//    stage S = Q . K^T (M 128, N 64, K = head_dim) into the tile's S buffer;
+//  * warp 11 (one thread, both tiles): per stage and tile O += P . V (M 128,
+//    N head_dim, K 64; P from tensor memory, V from shared memory as an
+//    MN-major operand) once its P is written.  A tcgen05.mma holds its
+//    issuing thread for tens of cycles, and that issue time was the bound on
+//    the stage rate with one thread issuing all of a tile's products.
 // Tensor memory: tile t's S buffer at columns 256 t .. +63, its P regions
 // (64 keys of 16 bits, two to a column) at 256 t + 64 and 256 t + 96, its O at
 // 256 t + 128.  Every wait is bounded; a wait that gives up sets
@@ -535,16 +538,21 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u));
 }
 
-constexpr int kTcWarps = 11;
+constexpr int kTcWarps = 12;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcProducer = 8;
-constexpr int kTcMma = 9;           // warps 9 and 10: the MMA issuers of tiles A and B
+constexpr int kTcMma = 9;           // warps 9 and 10: the score-product issuers of tiles A and B
+constexpr int kTcPv = 11;           // the P . V issuer of both tiles
+// per tile, the queue of P . V records from its score issuer to the P . V
+// issuer: a ring of four records, then tail (records pushed), head (records
+// issued), and fin (the score issuer has stopped); eight words a tile
+constexpr int kTcPvqWords = 16;
 constexpr uint32_t kTcTmemCols = 512;
 constexpr float kTcTau = 8.f;
 constexpr float kTcTauPow = 256.f;   // 2^kTcTau
 // barriers (8 bytes each): q full, q empty; per tile 8 slots (s full, s free,
-// p full[2], p empty[2], o free, one unused); done[2]
-constexpr int kTcBars = 2 + 2 * 8 + 2;
+// p full[2], p empty[2], o free, one unused); done[3] (one per issuing thread)
+constexpr int kTcBars = 2 + 2 * 8 + 3;
 
 __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
   return ((4 * (num_seqs + 1) + 15) / 16) * 16;
@@ -556,7 +564,8 @@ __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
 // scratch
 __host__ __device__ constexpr int tc_tags_off(int S) { return (24 * S + 8 * kTcBars + 15) & ~15; }
 __host__ __device__ constexpr int tc_ctrl_bytes(int S, int num_seqs) {
-  return tc_tags_off(S) + 32 * S + 16 + tc_toff_bytes(num_seqs) + 8 * (kTcThreads / 32);
+  return tc_tags_off(S) + 32 * S + 4 * kTcPvqWords + 16 + tc_toff_bytes(num_seqs) +
+         8 * (kTcThreads / 32);
 }
 
 template <int D, bool kBF16>
@@ -594,17 +603,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* const cgen = gbase + a.ctrl_off + tc_tags_off(S);
   int4* const meta = reinterpret_cast<int4*>(cgen);                         // [S]
   int4* const meta2 = reinterpret_cast<int4*>(cgen + 16 * S);               // [S]
-  uint32_t* const tslot = reinterpret_cast<uint32_t*>(cgen + 32 * S);
+  volatile uint32_t* const pvq = reinterpret_cast<volatile uint32_t*>(cgen + 32 * S);
+  uint8_t* const cgen2 = cgen + 32 * S + 4 * kTcPvqWords;
+  uint32_t* const tslot = reinterpret_cast<uint32_t*>(cgen2);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   int* const total_items_s = reinterpret_cast<int*>(tslot + 2);
-  int* const toff = reinterpret_cast<int*>(cgen + 32 * S + 16);             // [N + 1]
+  int* const toff = reinterpret_cast<int*>(cgen2 + 16);                     // [N + 1]
   long long* const scan_tmp =
-      reinterpret_cast<long long*>(cgen + 32 * S + 16 + tc_toff_bytes(a.num_seqs));
+      reinterpret_cast<long long*>(cgen2 + 16 + tc_toff_bytes(a.num_seqs));
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 2);       // a commit of each MMA issuer
+      mbar_init(bar_empty + 8 * s, 4);       // per tile: its score issuer's K share, its P . V share
       mbar_init(bar_seen + 8 * s, 8);        // one arrival per softmax warp
     }
     mbar_init(bar_qfull, 1);                 // the producer's expect-tx
@@ -621,6 +632,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(bar_done, 1);
     mbar_init(bar_done + 8, 1);
+    mbar_init(bar_done + 16, 1);
+    for (int w = 0; w < kTcPvqWords; ++w) pvq[w] = 0u;
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -747,36 +760,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_wait_bounded(bar_full + 8 * (k % S), (uint32_t)(k / S) & 1u, nullptr);
       if (nq > 0) mbar_wait_bounded(bar_qfull, (uint32_t)(nq - 1) & 1u, nullptr);
     }
-  } else if (warp >= kTcMma) {
-    // ======================= MMA issue (one thread per tile) =================
-    // Warp 9 issues tile A's products, warp 10 tile B's: one thread issuing
-    // both tiles' was the bottleneck (an issue returns after about a hundred
-    // cycles).  Each walks every stage.  An event loop: the tile's oldest
-    // pending O += P . V is issued as soon as its P is written (first: the
-    // softmax waits on it to reuse the P region and to rescale O), and the
-    // next stage's S = Q . K^T as soon as its K/V have landed, the query tile
-    // has, and the S buffer's previous scores have been read -- once at most
-    // one stage's O += P . V is pending, so that a P . V is never queued
-    // behind score products two stages ahead (the tensor pipe executes in
-    // issue order).  A stage and the query tiles are released by a commit of
-    // each issuer (barriers of count 2), made after its last product that
-    // reads them (at once where its tile does not read the stage).
+  } else if (warp == kTcMma || warp == kTcMma + 1) {
+    // ======================= score products (one thread per tile) ============
+    // Warp 9 issues tile A's score products, warp 10 tile B's; each walks
+    // every stage.  An event loop: the next stage's S = Q . K^T as soon as
+    // its K/V have landed, the query tile has, and the S buffer's previous
+    // scores have been read -- once at most one of the tile's P . V products
+    // is pending, so that a P . V is never queued behind score products two
+    // stages ahead (the tensor pipe executes in issue order).  Each score
+    // product pushes a record for its P . V onto the tile's queue.  A stage
+    // takes four arrivals to be released, per tile a K share and a V share:
+    // the score issuer commits the K share after its product (at once, with
+    // the V share too, where its tile does not read the stage); the query
+    // tiles are released by a commit of each score issuer after its last
+    // product that reads them.
     const int t = warp - kTcMma;
     if (lane == 0) {
       constexpr uint32_t id_s = umma_idesc_f16(kBF16, 128, kPBN, false);
-      constexpr uint32_t id_o = umma_idesc_f16(kBF16, 128, D, true);
-      // Bookkeeping in registers (a dynamically indexed array would live in
-      // local memory, a round trip on this thread's every step): a ring of
-      // four pending P . V records of 6 bits: stage slot (bits 0-2), first
-      // stage of an item (3), O must be free first (4), the parity of that
-      // wait (5).
+      // a record of 6 bits: stage slot (bits 0-2), first stage of an item
+      // (3), O must be free first (4), the parity of that wait (5)
       static_assert(kPMaxStages <= 8, "stage slots take 3 bits");
-      uint32_t ring = 0u;
-      int rh = 0, rt = 0;      // pending records [rh, rt)
-      int ns = 0, np = 0;      // S and P . V products issued
+      volatile uint32_t* const q = pvq + 8 * t;   // ring[4], tail, head, fin
+      int rt = 0;              // records pushed
+      int ns = 0;              // score products issued
       int ni = 0;              // items started
       int js = 0;              // next stage to walk
-      bool s_done = false;     // the stop marker was seen
       bool ok = true;
       const uint32_t bt = bar_tile0 + 64 * t;
       const uint32_t tcol = tmem + (uint32_t)(256 * t);
@@ -785,38 +793,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       long long t_last = clock64();
       while (true) {
         bool progressed = false;
-        if (rh != rt) {
-          // O += P . V: P (128 x 64) from the tile's P region np % 2 in
-          // tensor memory (16 keys = 8 columns per K step), V (64 keys x D,
-          // MN-major: 64-column planes kKPlane apart, 8-key groups 1024 bytes
-          // apart); the tile's first stage of an item overwrites O once the
-          // tile's item before has been written out
-          const uint32_t rc = (ring >> (6 * (rh & 3))) & 63u;
-          const int pst = (int)(rc & 7u);
-          const bool first = (rc & 8u) != 0u;
-          if (mbar_test(bt + ((np & 1) ? 24 : 32), (uint32_t)(np >> 1) & 1u) &&
-              (!(rc & 16u) || mbar_test(bt + 48, (rc >> 5) & 1u))) {
-            tc_fence_after();
-            const uint64_t dv = umma_desc_sw128(
-                base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
-            const uint32_t preg = tcol + 64u + 32u * (uint32_t)(np & 1);
-#pragma unroll
-            for (int k = 0; k < kPBN / 16; ++k)
-              umma_f16_tmem_a(tcol + 128u, preg + 8u * k, dv + 128u * k, id_o, !first || k > 0);
-            umma_commit(bt + ((np & 1) ? 56 : 40));  // the P region is free, O updated
-            umma_commit(bar_empty + 8 * pst);        // this tile no longer reads K, V
-            ++np;
-            ++rh;
-            progressed = true;
-          }
-        }
-        if (!s_done && rt - rh < 2) {
+        bool done = false;
+        if (rt - (int)q[5] < 2) {
           const int st = js % S;
           if (mbar_test(bar_full + 8 * st, (uint32_t)(js / S) & 1u)) {
             const int4 md = meta[st];
             if (md.x < 0) {
-              s_done = true;
-              progressed = true;
+              done = true;
             } else {
               const int4 m2 = meta2[st];
               const int kt = md.y, nkt = md.z, n = md.w;
@@ -824,6 +807,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               if (!act) {
                 // keys past this tile's last position: nothing to compute
                 umma_commit(bar_empty + 8 * st);
+                mbar_arrive(bar_empty + 8 * st);
                 if (kt == nkt - 1) umma_commit(bar_qempty);
                 ++js;
                 progressed = true;
@@ -847,6 +831,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                              db + (((uint32_t)(ks >> 2) * kKPlane + off) >> 4), id_s, ks > 0);
                   }
                   umma_commit(bt);
+                  umma_commit(bar_empty + 8 * st);   // this tile no longer reads K
                   if (kt == nkt - 1) umma_commit(bar_qempty);   // the query tile is free
                   uint32_t rc = (uint32_t)st;
                   if (kt == 0) {
@@ -854,8 +839,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (ni > 0) rc |= 16u | ((uint32_t)((ni - 1) & 1) << 5);
                     ++ni;
                   }
-                  const int sh = 6 * (rt & 3);
-                  ring = (ring & ~(63u << sh)) | (rc << sh);
+                  q[rt & 3] = rc;
+                  __threadfence_block();   // the record before the tail that publishes it
+                  q[4] = (uint32_t)(rt + 1);
                   ++rt;
                   ++ns;
                   ++js;
@@ -865,7 +851,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
-        if (s_done && rh == rt) break;
+        if (done) break;
         if (progressed) {
           t_last = clock64();
         } else {
@@ -884,9 +870,83 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
+      __threadfence_block();
+      q[6] = 1u;   // no more records
       // every MMA issued has completed before the tensor memory is released
       umma_commit(bar_done + 8 * t);
       mbar_wait_bounded(bar_done + 8 * t, 0u, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kTcPv) {
+    // ======================= P . V products (one thread, both tiles) =========
+    // Per tile, the oldest record on its queue: O += P . V once its P is
+    // written (and, at an item's first stage, once O has been read out for
+    // the tile's item before).  The commits free the P region (the softmax
+    // waits on it to reuse the region and to rescale O) and give the stage
+    // the tile's V share.
+    if (lane == 0) {
+      constexpr uint32_t id_o = umma_idesc_f16(kBF16, 128, D, true);
+      int rh0 = 0, rh1 = 0;    // records issued, per tile (P . V products)
+      bool ok = true;
+      long long t_last = clock64();
+      // one tile's oldest record, if it can go; returns whether it went
+      auto try_pv = [&](int t, int& rh) -> bool {
+        volatile uint32_t* const q = pvq + 8 * t;
+        if ((int)q[4] == rh) return false;
+        __threadfence_block();   // the record after the tail that published it
+        const uint32_t rc = q[rh & 3];
+        const uint32_t bt = bar_tile0 + 64 * t;
+        const int np = rh;
+        if (!mbar_test(bt + ((np & 1) ? 24 : 32), (uint32_t)(np >> 1) & 1u)) return false;
+        if ((rc & 16u) && !mbar_test(bt + 48, (rc >> 5) & 1u)) return false;
+        // P (128 x 64) from the tile's P region np % 2 in tensor memory (16
+        // keys = 8 columns per K step), V (64 keys x D, MN-major: 64-column
+        // planes kKPlane apart, 8-key groups 1024 bytes apart); the tile's
+        // first stage of an item overwrites O
+        tc_fence_after();
+        const int pst = (int)(rc & 7u);
+        const bool first = (rc & 8u) != 0u;
+        const uint32_t tcol = tmem + (uint32_t)(256 * t);
+        const uint64_t dv = umma_desc_sw128(
+            base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
+        const uint32_t preg = tcol + 64u + 32u * (uint32_t)(np & 1);
+#pragma unroll
+        for (int k = 0; k < kPBN / 16; ++k)
+          umma_f16_tmem_a(tcol + 128u, preg + 8u * k, dv + 128u * k, id_o, !first || k > 0);
+        umma_commit(bt + ((np & 1) ? 56 : 40));  // the P region is free, O updated
+        umma_commit(bar_empty + 8 * pst);        // this tile no longer reads V
+        ++rh;
+        q[5] = (uint32_t)rh;
+        return true;
+      };
+      while (true) {
+        bool progressed = try_pv(0, rh0);
+        progressed = try_pv(1, rh1) || progressed;
+        if (!progressed) {
+          // both score issuers have stopped and every record is issued
+          if (pvq[6] && pvq[8 + 6]) {
+            __threadfence_block();
+            if ((int)pvq[4] == rh0 && (int)pvq[8 + 4] == rh1) break;
+          }
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          if (clock64() - t_last > kWaitLimitCycles) {
+            ok = false;
+            break;
+          }
+          __nanosleep(20);
+        } else {
+          t_last = clock64();
+        }
+      }
+      if (!ok) {
+        if (!*abort_flag) set_error(a.err, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(bar_done + 16);
+      mbar_wait_bounded(bar_done + 16, 0u, nullptr);
     }
     __syncwarp();
   } else {
