@@ -418,7 +418,11 @@ def run_gpu(args, rank, world, local_rank):
             "bound": "tensor", "achieved": round(tach, 1), "peak": tpeak, "unit": "TFLOP/s",
             "frac": round(tach / tpeak, 4), "traffic": traffic,
             "peak_source": tkind + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS bf16 burst)",
-            "kernel": "pa_prefill: paged_prefill_tc_kernel (tcgen05.mma, TMEM accumulators)",
+            "kernel": ("pa_prefill: paged_prefill_tc_kernel (tcgen05.mma, TMEM accumulators)"
+                       if pa.pa_prefill_kernel(wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                               wl.block_size, wl.dtype, wl.num_seqs)
+                       == pa.PA_PREFILL_TENSOR_CORE
+                       else "pa_prefill: paged_prefill_kernel (warp-level mma.sync)"),
             "algorithmic_flops_per_launch": flops,
             "kv_gbs": round(achieved, 1),
         }

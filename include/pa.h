@@ -338,6 +338,20 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
  * at most 16.  Query head hq reads KV head hq / G.
  */
 int pa_prefill_workspace_size(size_t* bytes);
+
+/*
+ * pa_prefill_kernel -- which kernel pa_prefill runs for this shape on the
+ * current device: *kind = PA_PREFILL_TENSOR_CORE (tcgen05.mma with the
+ * accumulators in tensor memory; blocks of 8 or more tokens, when its staging
+ * fits the device) or PA_PREFILL_WARP_MMA (warp-level m16n8k16 MMAs; the
+ * other supported shapes).  Shapes pa_prefill refuses return its error.  The
+ * choice is the same as pa_prefill's [P1] "How does it support prompts of
+ * arbitrary length?" chunks, at any batch size up to 4096 sequences.
+ */
+#define PA_PREFILL_WARP_MMA 0
+#define PA_PREFILL_TENSOR_CORE 1
+int pa_prefill_kernel(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t dtype, int32_t num_seqs, int32_t* kind);
 int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
                const int32_t* query_start, int32_t num_seqs, int64_t total_q,

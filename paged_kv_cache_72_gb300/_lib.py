@@ -31,6 +31,8 @@ PA_DECODE_MMA = 2
 PA_DECODE_TABLES_READY = 0x100
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 PA_DECODE_MAX_CTAS = 16384
+PA_PREFILL_WARP_MMA = 0
+PA_PREFILL_TENSOR_CORE = 1
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -63,6 +65,8 @@ SIGNATURES = {
                                      _i64, _i32, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                      _vp, _vp, _sz, _i32, _i32, _vp, _vp]),
     "pa_prefill_workspace_size": (ctypes.c_int, [ctypes.POINTER(_sz)]),
+    "pa_prefill_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32,
+                                         ctypes.POINTER(_i32)]),
     "pa_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                                   _i32, _i64, _i32, ctypes.c_float, _vp, _vp, _sz, _vp, _vp]),
     "pa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,

@@ -1300,6 +1300,24 @@ int pa_prefill_workspace_size(size_t* bytes) {
   return PA_OK;
 }
 
+int pa_prefill_kernel(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t dtype, int32_t num_seqs, int32_t* kind) {
+  if (!kind || num_seqs < 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs > kPMaxSeqs) return PA_ERR_UNSUPPORTED;
+  // the same choice as pa_prefill's
+  PrefillPlan p;
+  const int rc_tc = make_tc_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype,
+                                 num_seqs, &p);
+  if (rc_tc == PA_OK) {
+    *kind = PA_PREFILL_TENSOR_CORE;
+    return PA_OK;
+  }
+  if (rc_tc != PA_ERR_UNSUPPORTED) return rc_tc;
+  if (int rc = make_plan(num_q_heads, num_kv_heads, head_dim, block_size, dtype, &p)) return rc;
+  *kind = PA_PREFILL_WARP_MMA;
+  return PA_OK;
+}
+
 int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, int32_t table_stride, const int32_t* seq_lens,
                const int32_t* query_start, int32_t num_seqs, int64_t total_q,

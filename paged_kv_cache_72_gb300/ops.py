@@ -371,6 +371,16 @@ def pa_prefill(q, k_cache, v_cache, block_tables, seq_lens, query_start, scale, 
     return out
 
 
+def pa_prefill_kernel(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_seqs):
+    """Which kernel pa_prefill runs for this shape on the current device:
+    PA_PREFILL_TENSOR_CORE or PA_PREFILL_WARP_MMA."""
+    L = _lib.load()
+    kind = ctypes.c_int32(-1)
+    _check(L.pa_prefill_kernel(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_seqs,
+                               ctypes.byref(kind)), "pa_prefill_kernel")
+    return kind.value
+
+
 def pa_gather_kv(k_cache, v_cache, block_tables, seq_lens, out_offsets, total_rows,
                  flags=PA_DECODE_AUTO, err=None):
     """Contiguous copies [total_rows, H_kv, D] of every sequence's K and V."""

@@ -51,6 +51,27 @@ def test_prefill_parity_sweep(cuda_device, dtype, Hq, Hkv, D, B):
     _parity(wl)
 
 
+def test_prefill_kernel_choice(cuda_device):
+    # Every shape with blocks of 8 or more tokens runs the tensor-core kernel,
+    # at any batch size; blocks of 4 tokens (head_dim 128) take the
+    # warp-level kernel.
+    # A tensor-core plan that stops fitting the device (registers, shared
+    # memory) would otherwise fall back to the slower kernel with every
+    # parity test still passing.
+    for dtype in (W.F16, W.BF16):
+        for D in (64, 128):
+            for B in (8, 16, 64, 256):
+                for (Hq, Hkv) in ((32, 8), (14, 2), (8, 8)):
+                    for n in (1, 16, 4096):
+                        assert pa.pa_prefill_kernel(Hq, Hkv, D, B, dtype, n) == \
+                            pa.PA_PREFILL_TENSOR_CORE, (dtype, D, B, Hq, Hkv, n)
+    assert pa.pa_prefill_kernel(8, 2, 128, 4, W.F16, 6) == pa.PA_PREFILL_WARP_MMA
+    assert pa.pa_prefill_kernel(8, 8, 128, 4, W.BF16, 4096) == pa.PA_PREFILL_WARP_MMA
+    for shape in ((8, 2, 96, 16), (8, 2, 128, 2), (8, 2, 64, 4)):   # refused by pa_prefill too
+        with pytest.raises(pa.PAError):
+            pa.pa_prefill_kernel(*shape, W.F16, 6)
+
+
 def test_prefill_repeats_bitwise_through_one_workspace(cuda_device):
     wl = W.random_prefill(140, W.BF16, 32, 8, 128, 16, PREFIX, CHUNK)
     st, out = _parity(wl)
