@@ -385,14 +385,17 @@ int encode_pool_map(CUtensorMap* map, const void* cache, const DecodePlan& p, in
 // [plane][row][128 bytes] (the K-major and MN-major operand layouts of the
 // tensor-core prefill).
 int encode_pool_plane_map(CUtensorMap* map, const void* cache, bool bf16, int D, int B, int R,
-                          int Hkv, long long num_blocks) {
+                          int Hkv, long long num_blocks, int box_planes) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return PA_ERR_CUDA;
   const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
   const cuuint64_t dims[5] = {64, (cuuint64_t)B, (cuuint64_t)(D / 64), (cuuint64_t)Hkv,
                               (cuuint64_t)num_blocks};
   const cuuint64_t strides[4] = {row, 128, (cuuint64_t)D * 2, row * B};
-  const cuuint32_t box[5] = {64, (cuuint32_t)R, 1, 1, 1};
+  // box_planes 64-column planes of R rows of one head of one block: in shared
+  // memory [plane][row][128 bytes]
+  if (box_planes < 1 || box_planes > D / 64) return PA_ERR_INVALID_ARG;
+  const cuuint32_t box[5] = {64, (cuuint32_t)R, (cuuint32_t)box_planes, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   memset(map, 0, sizeof(*map));
   CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,

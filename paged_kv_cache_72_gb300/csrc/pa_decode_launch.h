@@ -29,7 +29,7 @@ int encode_pool_map(CUtensorMap* map, const void* cache, const DecodePlan& p, in
                     long long num_blocks);
 // Per-plane pool map and query-tile map of the tensor-core prefill.
 int encode_pool_plane_map(CUtensorMap* map, const void* cache, bool bf16, int D, int B, int R,
-                          int Hkv, long long num_blocks);
+                          int Hkv, long long num_blocks, int box_planes);
 int encode_q_tile_map(CUtensorMap* map, const void* q, bool bf16, int D, int G, int Hkv,
                       long long total_q, int BM);
 

@@ -742,12 +742,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t kdst = base + (uint32_t)st * a.stage_bytes + (uint32_t)lane * box_bytes;
           const int row_off = tok0 & (a.B - 1);
 #pragma unroll
-          for (int p = 0; p < NP; ++p) {
+          for (int p = 0; p < NP; ++p)
             tma_load_5d(kdst + (uint32_t)p * kKPlane, &tmk, bar_full + 8 * st, 0, row_off, p, it.h,
                         ent, pol_kv);
-            tma_load_5d(kdst + (uint32_t)(a.kv_bytes + p * kKPlane), &tmv, bar_full + 8 * st, 0,
-                        row_off, p, it.h, ent, pol_kv);
-          }
+          // the block's V rows, every plane, in one box: [plane][row][128 bytes]
+          tma_load_5d(base + (uint32_t)st * a.stage_bytes + (uint32_t)a.kv_bytes +
+                          (uint32_t)lane * box_bytes * (uint32_t)NP,
+                      &tmv, bar_full + 8 * st, 0, row_off, 0, it.h, ent, pol_kv);
         }
         ++j;
       }
@@ -900,19 +901,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_test(bt + ((np & 1) ? 24 : 32), (uint32_t)(np >> 1) & 1u)) return false;
         if ((rc & 16u) && !mbar_test(bt + 48, (rc >> 5) & 1u)) return false;
         // P (128 x 64) from the tile's P region np % 2 in tensor memory (16
-        // keys = 8 columns per K step), V (64 keys x D, MN-major: 64-column
-        // planes kKPlane apart, 8-key groups 1024 bytes apart); the tile's
-        // first stage of an item overwrites O
+        // keys = 8 columns per K step), V (64 keys x D, MN-major) from the
+        // stage's V part: block b's box at b * vblk, [plane][row][128 bytes],
+        // so the 64-column planes are vrow bytes apart (the leading offset)
+        // and 8-key groups 1024 bytes apart within a block of 16 or more
+        // rows, one block apart at 8 rows (the stride offset).  A K step's
+        // 16 keys are rows (16k) % R.. of block (16k) / R.  The tile's first
+        // stage of an item overwrites O.
         tc_fence_after();
         const int pst = (int)(rc & 7u);
         const bool first = (rc & 8u) != 0u;
         const uint32_t tcol = tmem + (uint32_t)(256 * t);
-        const uint64_t dv = umma_desc_sw128(
-            base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes, kKPlane, 1024);
+        const uint32_t vrow = (uint32_t)a.R * 128u, vblk = vrow * (uint32_t)NP;
+        const uint32_t vpart = base + (uint32_t)pst * a.stage_bytes + (uint32_t)a.kv_bytes;
+        const uint64_t dv = umma_desc_sw128(vpart, vrow, a.R >= 16 ? 1024u : vblk);
         const uint32_t preg = tcol + 64u + 32u * (uint32_t)(np & 1);
 #pragma unroll
-        for (int k = 0; k < kPBN / 16; ++k)
-          umma_f16_tmem_a(tcol + 128u, preg + 8u * k, dv + 128u * k, id_o, !first || k > 0);
+        for (int k = 0; k < kPBN / 16; ++k) {
+          const uint32_t off = (uint32_t)((16 * k) >> a.log2R) * vblk +
+                               (uint32_t)((16 * k) & (a.R - 1)) * 128u;
+          umma_f16_tmem_a(tcol + 128u, preg + 8u * k, dv + (off >> 4), id_o, !first || k > 0);
+        }
         umma_commit(bt + ((np & 1) ? 56 : 40));  // the P region is free, O updated
         umma_commit(bar_empty + 8 * pst);        // this tile no longer reads V
         ++rh;
@@ -1110,10 +1119,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int z0 = max(0, it.T - tb);
         const int per_plane = (kPBN - z0) * 8;   // 16-byte pieces
         const uint32_t vpart = base + (uint32_t)st * a.stage_bytes + (uint32_t)a.kv_bytes;
+        const uint32_t vrow = (uint32_t)a.R * 128u, vblk = vrow * (uint32_t)NP;
         for (int e = r; e < per_plane * NP; e += 128) {
+          // key z of the stage: row z % R of block z / R's box, plane p
           const int p = e / per_plane, rem = e - p * per_plane;
-          const uint32_t addr =
-              vpart + (uint32_t)p * kKPlane + (uint32_t)(z0 + (rem >> 3)) * 128u + (uint32_t)(rem & 7) * 16u;
+          const int z = z0 + (rem >> 3);
+          const uint32_t addr = vpart + (uint32_t)(z >> a.log2R) * vblk + (uint32_t)p * vrow +
+                                (uint32_t)(z & (a.R - 1)) * 128u + (uint32_t)(rem & 7) * 16u;
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
         }
         fence_proxy_async_smem();   // the cleared rows, before the tensor core reads them
@@ -1347,11 +1359,13 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
   if (workspace_bytes < 256) return PA_ERR_WORKSPACE;
   CUtensorMap tk, tv, tq;
   if (p.tc) {
+    // K: one box per 64-column plane of a block's rows; V: one box per
+    // block, all its planes
     if (int rc = encode_pool_plane_map(&tk, k_cache, p.bf16, p.D, p.B, p.R, num_kv_heads,
-                                       num_blocks))
+                                       num_blocks, 1))
       return rc;
     if (int rc = encode_pool_plane_map(&tv, v_cache, p.bf16, p.D, p.B, p.R, num_kv_heads,
-                                       num_blocks))
+                                       num_blocks, p.D / 64))
       return rc;
     if (int rc = encode_q_tile_map(&tq, q, p.bf16, p.D, p.G, num_kv_heads, total_q, p.BM))
       return rc;

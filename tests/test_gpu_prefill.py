@@ -42,6 +42,8 @@ CASES = [
     (W.BF16, 32, 2, 128, 32),   # G = 16
     (W.F16, 6, 3, 128, 4),
     (W.BF16, 12, 4, 64, 256),
+    (W.BF16, 16, 4, 128, 8),    # V boxes of 8 rows x 2 planes: 8-key groups one block apart
+    (W.F16, 8, 2, 128, 64),     # one 64-row block per stage
 ]
 
 
