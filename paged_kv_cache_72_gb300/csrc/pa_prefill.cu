@@ -513,8 +513,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
 //    pair's stages; its warpgroup skips the others.
 //  * warp 8 (producer): items from the atomic counter; per item the two query
 //    tiles by TMA (one copy per 64-column plane, [row][128 bytes], 128-byte
-//    swizzle), per stage the K and V planes of the item's KV head, tagged with
-//    the item.
+//    swizzle); per stage, tagged with the item, the K planes of the item's KV
+//    head (one copy per 64-column plane of a block: [plane][key][128 bytes])
+//    and its V rows (one copy per block, every plane: [block][plane][row][128
+//    bytes]).
 //  * warps 9 and 10 (score products, one thread each, one per tile): per
 //    stage S = Q . K^T (M 128, N 64, K = head_dim) into the tile's S buffer;
 //  * warp 11 (one thread, both tiles): per stage and tile O += P . V (M 128,
@@ -560,8 +562,8 @@ __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
 
 // shared-memory control area of the tensor-core kernel (after the query tiles):
 // full/empty/seen barriers, the other barriers, stage tags (two int4 per
-// stage, from a 16-byte boundary), TMEM address and flags, item offsets, scan
-// scratch
+// stage, from a 16-byte boundary), the P . V record queues, TMEM address and
+// flags, item offsets, scan scratch
 __host__ __device__ constexpr int tc_tags_off(int S) { return (24 * S + 8 * kTcBars + 15) & ~15; }
 __host__ __device__ constexpr int tc_ctrl_bytes(int S, int num_seqs) {
   return tc_tags_off(S) + 32 * S + 4 * kTcPvqWords + 16 + tc_toff_bytes(num_seqs) +
