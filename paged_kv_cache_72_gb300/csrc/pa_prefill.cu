@@ -42,6 +42,11 @@ constexpr int kPRows = 16 * kPW;         // query rows per work item
 constexpr int kPBN = 64;                 // key tokens per stage
 constexpr int kPMaxSeqs = 4096;          // per-sequence item offsets kept in shared memory
 constexpr int kPMaxStages = 8;
+// Up to this many sequences, the tensor-core kernel numbers its work items
+// longest sequence first (a rank per sequence, one thread each).  At 192, the
+// ranks' two bytes per sequence still leave room for five 32 KB stages at
+// head_dim 128 in 227 KB of shared memory.
+constexpr int kTcSortSeqs = 192;
 
 struct PrefillArgs {
   const uint16_t* q;            // [total_q][Hq][D]
@@ -97,32 +102,35 @@ __device__ __forceinline__ void decode_item(int item, const int* toff, const Pre
 
 // A work item of the tensor-core kernel: two consecutive token tiles A and B of
 // one sequence and KV head, which share the stream of keys (B's keys; A's are a
-// prefix of them).  Pair number -> (sequence, KV head, pair); toff[i] = Hkv *
-// (pairs of sequences < i); within a sequence the pairs run over KV heads, then
-// from the last pair (most keys) to the first.  Tile B is absent (no tokens)
-// when the sequence has an odd number of tiles and this is its first pair.
+// prefix of them).  Pair number -> (sequence, KV head, pair).  Sequences are
+// numbered in rank order: rank s is sequence perm[s] (longest first), or s
+// itself without perm; toff[s] = Hkv * (pairs of ranks < s).  Within a sequence
+// the pairs run from the last (most keys) to the first, each over the KV
+// heads, so the counter hands out the costliest items first and the short ones
+// fill the end of the launch.  Tile B is absent (no tokens) when the sequence
+// has an odd number of tiles and this is its first pair.
 struct Pair {
   int i, h, q0, ntok_a, ntok_b, p0, T, nkt_a, nkt;   // q0, p0: tile A's first q row and
                                                      // position; stages of A and of the pair
 };
 
-__device__ __forceinline__ void decode_pair(int item, const int* toff, const PrefillArgs& a,
-                                            Pair& it) {
-  int lo = 0, hi = a.num_seqs;   // the largest i with toff[i] <= item
+__device__ __forceinline__ void decode_pair(int item, const int* toff, const uint16_t* perm,
+                                            const PrefillArgs& a, Pair& it) {
+  int lo = 0, hi = a.num_seqs;   // the largest rank s with toff[s] <= item
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (toff[mid] <= item) lo = mid;
     else hi = mid;
   }
-  const int i = lo;
-  const int pairs = (toff[i + 1] - toff[i]) / a.Hkv;
-  const int r = item - toff[i];
-  const int pr = pairs - 1 - r % pairs;
+  const int i = perm ? (int)perm[lo] : lo;
+  const int pairs = (toff[lo + 1] - toff[lo]) / a.Hkv;
+  const int r = item - toff[lo];
+  const int pr = pairs - 1 - r / a.Hkv;
   const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
   const int T = __ldg(a.seq_lens + i);
   const int ta = 2 * pr * a.BM;   // tile A's first new token
   it.i = i;
-  it.h = r / pairs;
+  it.h = r % a.Hkv;
   it.q0 = __ldg(a.query_start + i) + ta;
   it.ntok_a = min(a.BM, L - ta);
   it.ntok_b = max(0, min(a.BM, L - ta - a.BM));
@@ -166,17 +174,41 @@ __device__ __forceinline__ long long scan_excl(long long v, long long* tmp, long
 }
 
 // Item offsets: each thread sums the items (kTPI token tiles each) of a run of
-// sequences, one block scan gives toff[] and the item count.  A sequence whose
-// length lies outside its table, or with more new tokens than tokens, is
-// reported and its rows get zeros.  Ends with a block barrier.
+// sequence ranks, one block scan gives toff[] and the item count.  With perm
+// (at most NT sequences), the ranks first order the sequences by length,
+// longest first, ties by index: perm[rank] = sequence.  Without it, rank s is
+// sequence s.  A sequence whose length lies outside its table, or with more
+// new tokens than tokens, ranks last; it is reported and its rows get zeros.
+// Ends with a block barrier.
 template <int NT, int D, int kTPI>
 __device__ __forceinline__ void item_offsets(const PrefillArgs& a, int* toff, long long* scan_tmp,
-                                             int* total_items_s) {
+                                             int* total_items_s, uint16_t* perm = nullptr) {
   const int tid = threadIdx.x;
+  if (perm) {
+    // one sequence per thread; toff holds the lengths until the ranks are known
+    int key = -1;
+    if (tid < a.num_seqs) {
+      const int L = __ldg(a.query_start + tid + 1) - __ldg(a.query_start + tid);
+      const int T = clamp_seq(__ldg(a.seq_lens + tid), a.stride, a.B);
+      key = (L >= 0 && T >= 0 && L <= T) ? T : -1;
+      toff[tid] = key;
+    }
+    __syncthreads();
+    int rank = 0;
+    if (tid < a.num_seqs)
+      for (int j = 0; j < a.num_seqs; ++j) {
+        const int kj = toff[j];
+        rank += (kj > key || (kj == key && j < tid)) ? 1 : 0;
+      }
+    __syncthreads();
+    if (tid < a.num_seqs) perm[rank] = (uint16_t)tid;
+    __syncthreads();
+  }
   const int per = (a.num_seqs + NT - 1) / NT;
   const int run0 = min(a.num_seqs, tid * per), run1 = min(a.num_seqs, run0 + per);
   long long mine = 0;
-  for (int i = run0; i < run1; ++i) {
+  for (int s = run0; s < run1; ++s) {
+    const int i = perm ? (int)perm[s] : s;
     const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
     const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
     const bool ok = L >= 0 && T >= 0 && L <= T;
@@ -194,8 +226,9 @@ __device__ __forceinline__ void item_offsets(const PrefillArgs& a, int* toff, lo
   }
   long long total;
   long long off = scan_excl<NT>(mine, scan_tmp, total);
-  for (int i = run0; i < run1; ++i) {
-    toff[i] = (int)off;
+  for (int s = run0; s < run1; ++s) {
+    const int i = perm ? (int)perm[s] : s;
+    toff[s] = (int)off;
     const int L = __ldg(a.query_start + i + 1) - __ldg(a.query_start + i);
     const int T = clamp_seq(__ldg(a.seq_lens + i), a.stride, a.B);
     if (L >= 0 && T >= 0 && L <= T)
@@ -542,6 +575,7 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
 
 constexpr int kTcWarps = 12;
 constexpr int kTcThreads = kTcWarps * 32;
+static_assert(kTcSortSeqs <= kTcThreads, "one thread ranks one sequence");
 constexpr int kTcProducer = 8;
 constexpr int kTcMma = 9;           // warps 9 and 10: the score-product issuers of tiles A and B
 constexpr int kTcPv = 11;           // the P . V issuer of both tiles
@@ -559,15 +593,18 @@ constexpr int kTcBars = 2 + 2 * 8 + 3;
 __host__ __device__ constexpr int tc_toff_bytes(int num_seqs) {
   return ((4 * (num_seqs + 1) + 15) / 16) * 16;
 }
+__host__ __device__ constexpr int tc_perm_bytes(int num_seqs) {
+  return num_seqs <= kTcSortSeqs ? ((2 * num_seqs + 15) / 16) * 16 : 0;
+}
 
 // shared-memory control area of the tensor-core kernel (after the query tiles):
 // full/empty/seen barriers, the other barriers, stage tags (two int4 per
 // stage, from a 16-byte boundary), the P . V record queues, TMEM address and
-// flags, item offsets, scan scratch
+// flags, item offsets, scan scratch, the sequences in rank order
 __host__ __device__ constexpr int tc_tags_off(int S) { return (24 * S + 8 * kTcBars + 15) & ~15; }
 __host__ __device__ constexpr int tc_ctrl_bytes(int S, int num_seqs) {
   return tc_tags_off(S) + 32 * S + 4 * kTcPvqWords + 16 + tc_toff_bytes(num_seqs) +
-         8 * (kTcThreads / 32);
+         8 * (kTcThreads / 32) + tc_perm_bytes(num_seqs);
 }
 
 template <int D, bool kBF16>
@@ -613,6 +650,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int* const toff = reinterpret_cast<int*>(cgen2 + 16);                     // [N + 1]
   long long* const scan_tmp =
       reinterpret_cast<long long*>(cgen2 + 16 + tc_toff_bytes(a.num_seqs));
+  uint16_t* const perm = a.num_seqs <= kTcSortSeqs
+                             ? reinterpret_cast<uint16_t*>(scan_tmp + kTcThreads / 32)
+                             : nullptr;   // [N]
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -649,7 +689,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
   }
   grid_dep_wait();
-  item_offsets<kTcThreads, D, 2>(a, toff, scan_tmp, total_items_s);   // ends with a barrier
+  item_offsets<kTcThreads, D, 2>(a, toff, scan_tmp, total_items_s, perm);   // ends with a barrier
   tc_fence_after();
   if (tid == 0) grid_dep_launch();
   const int total_items = *total_items_s;
@@ -674,7 +714,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) item = (int)atomicAdd(a.ws, 1u);
       item = __shfl_sync(0xffffffffu, item, 0);
       Pair it;
-      if (item < total_items) decode_pair(item, toff, a, it);
+      if (item < total_items) decode_pair(item, toff, perm, a, it);
       else stop = true;
       const int n_kt = stop ? 1 : it.nkt;
       // block-table entries two stages ahead of their copies (lane l < nsb:
@@ -987,7 +1027,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive(bar_seen + 8 * st);   // the tag is read
       const int kt = md.y;
       if (kt == 0) {
-        decode_pair(md.x, toff, a, it);
+        decode_pair(md.x, toff, perm, a, it);
         const int ntok = tile == 0 ? it.ntok_a : it.ntok_b;
         q0 = it.q0 + tile * a.BM;
         p0 = it.p0 + tile * a.BM;

@@ -176,6 +176,20 @@ def test_prefill_sequences_ending_on_stage_edges(cuda_device):
     _parity(wl)
 
 
+@pytest.mark.parametrize("n", [192, 193])
+def test_prefill_item_order_either_side_of_the_rank_limit(cuda_device, n):
+    # up to 192 sequences the tensor-core kernel takes its items longest
+    # sequence first (ranked in shared memory, ties by index), past that in
+    # batch order; both must cover every item once
+    rng = np.random.default_rng(n)
+    prefix = rng.integers(0, 150, size=n)
+    chunk = rng.integers(1, 40, size=n)
+    prefix[::5] = 64 - chunk[::5]   # ties: every fifth sequence 64 tokens long
+    wl = W.random_prefill(170 + n, W.BF16, 16, 4, 128, 16, prefix, chunk, garbage="nan")
+    assert pa.pa_prefill_kernel(16, 4, 128, 16, W.BF16, n) == pa.PA_PREFILL_TENSOR_CORE
+    _parity(wl)
+
+
 def test_prefill_at_the_sequence_limit(cuda_device):
     # every sequence's item offset sits in shared memory, up to 4,096
     # sequences: a batch of 4,096, mostly single decode tokens with a chunk in
