@@ -708,6 +708,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t pol_q = policy_evict_first();
     const uint32_t box_bytes = (uint32_t)a.R * 128u;
     int j = 0, n = 0, nq = 0;   // stages issued, items started, query tiles issued
+    int jst = 0;                // j % S and the parity of j / S, kept as j advances
+    uint32_t jph = 0u;
     bool stop = false;
     while (!stop) {
       int item = 0;
@@ -732,9 +734,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int ent = e0;
         e0 = e1;
         e1 = kt + 2 < n_kt ? load_ent(kt + 2) : -1;
-        const int st = j % S;
-        bool ok_wait = wait_warp(bar_empty + 8 * st, ((uint32_t)(j / S) & 1u) ^ 1u) &&
-                       wait_warp(bar_seen + 8 * st, ((uint32_t)(j / S) & 1u) ^ 1u);
+        const int st = jst;
+        bool ok_wait = wait_warp(bar_empty + 8 * st, jph ^ 1u) &&
+                       wait_warp(bar_seen + 8 * st, jph ^ 1u);
         if (ok_wait && !stop && kt == 0)   // the query tiles' buffers are free
           ok_wait = wait_warp(bar_qempty, ((uint32_t)n & 1u) ^ 1u);
         if (!ok_wait) {
@@ -793,6 +795,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       &tmv, bar_full + 8 * st, 0, row_off, 0, it.h, ent, pol_kv);
         }
         ++j;
+        if (++jst == S) {
+          jst = 0;
+          jph ^= 1u;
+        }
       }
       if (!stop) ++n;
     }
@@ -828,6 +834,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int ns = 0;              // score products issued
       int ni = 0;              // items started
       int js = 0;              // next stage to walk
+      int sst = 0;             // js % S and the parity of js / S
+      uint32_t sph = 0u;
+      auto next_stage = [&]() {
+        ++js;
+        if (++sst == S) {
+          sst = 0;
+          sph ^= 1u;
+        }
+      };
       bool ok = true;
       const uint32_t bt = bar_tile0 + 64 * t;
       const uint32_t tcol = tmem + (uint32_t)(256 * t);
@@ -838,8 +853,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool progressed = false;
         bool done = false;
         if (rt - (int)q[5] < 2) {
-          const int st = js % S;
-          if (mbar_test(bar_full + 8 * st, (uint32_t)(js / S) & 1u)) {
+          const int st = sst;
+          if (mbar_test(bar_full + 8 * st, sph)) {
             const int4 md = meta[st];
             if (md.x < 0) {
               done = true;
@@ -852,7 +867,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 umma_commit(bar_empty + 8 * st);
                 mbar_arrive(bar_empty + 8 * st);
                 if (kt == nkt - 1) umma_commit(bar_qempty);
-                ++js;
+                next_stage();
                 progressed = true;
               } else {
                 // the query tile has landed, and the S buffer's previous
@@ -887,7 +902,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   q[4] = (uint32_t)(rt + 1);
                   ++rt;
                   ++ns;
-                  ++js;
+                  next_stage();
                   progressed = true;
                 }
               }
@@ -1013,11 +1028,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool valid = false;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    int j = 0;             // stages of the ring seen
+    int jst = 0;           // the ring slot of the next stage to see
+    uint32_t jph = 0u;     // the parity of that slot's use
     int nt = 0;            // stages this tile has processed
     while (true) {
-      const int st = j % S;
-      if (!wait_warp(bar_full + 8 * st, (uint32_t)(j / S) & 1u)) {
+      const int st = jst;
+      if (!wait_warp(bar_full + 8 * st, jph)) {
         ok = false;
         break;
       }
@@ -1038,7 +1054,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         m_used = -INFINITY;
         l = 0.f;
       }
-      ++j;
+      if (++jst == S) {
+        jst = 0;
+        jph ^= 1u;
+      }
       if (kt >= nkt_t) continue;   // keys past this tile's last position
       // ---- this row of S
       if (!wait_warp(bt, (uint32_t)nt & 1u)) {
