@@ -874,6 +874,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // scores have been read
                 bool ready = kt != 0 || mbar_test(bar_qfull, (uint32_t)n & 1u);
                 if (ready && ns >= 1) ready = mbar_test(bt + 16, (uint32_t)(ns - 1) & 1u);
+                // and the P region these scores' P will go to is free (the
+                // P . V two products back has completed), so that the softmax,
+                // once it sees the scores, writes P without a wait of its own
+                if (ready && ns >= 2)
+                  ready = mbar_test(bt + ((ns & 1) ? 56 : 40), (uint32_t)((ns >> 1) - 1) & 1u);
                 if (ready) {
                   tc_fence_after();
                   const uint64_t db =
@@ -1145,12 +1150,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       l = l * alpha + ssum;
       // the P region's previous use (two stages back) is done: its O += P . V
-      // has completed
+      // had completed before the score issuer issued these scores
       const uint32_t pe = bt + ((nt & 1) ? 56 : 40);
-      if (nt >= 2 && !wait_warp(pe, (uint32_t)((nt >> 1) - 1) & 1u)) {
-        ok = false;
-        break;
-      }
       tc_fence_after();
       // row r of P into the tile's P region nt % 2 (lane r, two keys a column)
       tmem_st32(trow + 64u + 32u * (uint32_t)(nt & 1), *reinterpret_cast<uint32_t(*)[32]>(pk));
