@@ -531,6 +531,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // tiles (A, then B: 128 query rows each) of one sequence and KV head; both
 // read the same stream of keys, so every staged K/V byte serves 256 query
 // rows, and the tensor core works on one tile while the other's softmax runs.
+// Items are numbered longest sequence first (batches of up to kTcSortSeqs
+// sequences; see decode_pair), so the short ones fill the end of the launch.
 // The contraction runs on the fifth-generation tensor cores with the
 // accumulators in tensor memory:
 //  * warps 0-3 (softmax of tile A) and 4-7 (tile B): thread r of a warpgroup
@@ -551,7 +553,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
 //    and its V rows (one copy per block, every plane: [block][plane][row][128
 //    bytes]).
 //  * warps 9 and 10 (score products, one thread each, one per tile): per
-//    stage S = Q . K^T (M 128, N 64, K = head_dim) into the tile's S buffer;
+//    stage S = Q . K^T (M 128, N 64, K = head_dim) into the tile's S buffer,
+//    once the P region that the stage's P will go to is free again, so that
+//    the softmax never waits for it;
 //  * warp 11 (one thread, both tiles): per stage and tile O += P . V (M 128,
 //    N head_dim, K 64; P from tensor memory, V from shared memory as an
 //    MN-major operand) once its P is written.  A tcgen05.mma holds its
